@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the device-wide scan library on GB300.
+
+One step = one int32 exclusive add-scan of N = 2^28 elements (the +1/-1
+bracket sequence, seed 3) through the C ABI, inputs resident in HBM.  The
+inputs (1 GiB in, 1 GiB out) are far larger than the 126 MB L2, so no flush
+is needed between steps.  Prints one JSON line:
+
+  value      whole-job Gelem/s (all ranks' elements / max-over-ranks time)
+  roofline   the scan kernel's algorithmic bytes (2 * N * 4 per launch) over
+             its CUDA-event duration, against the measured HBM copy peak
+  e2e        the same scan from pinned host memory: host-to-device copy,
+             scan, device-to-host copy of the result, every step
+  cpu_baseline  the serial CPU oracle on the host cores (1 thread)
+  extra      compaction at N = 2^26 (1/50/99 %), the max / xor sweep at
+             N = 2^28, fp32 add at N = 2^24, N = 65,536 latency, split and
+             the 32-pass radix sort at N = 2^26, and the reduce-then-scan carry
+
+``--impl reference`` times the CPU oracle instead (the reference arm): each
+step is the oracle's serial exclusive scan of a 2^22-element sample of the
+same workload.  With ``--gpus N`` > 1 (launched by torchrun) every rank runs
+an independent replica on its own GPU (the scan needs no exchange between
+replicas); ``scaling`` is "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "int32 exclusive scan Gelem/s & HBM GB/s (% peak) at N=2^28; compaction Gelem/s"
+N_HEADLINE = 1 << 28
+REF_SAMPLE = 1 << 22
+FALLBACK_HBM_GBS = 6800.0
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the scan kernel at
+# N = 2^28, from the ncu capture summarised in profiles/; None until taken for
+# the current kernel.
+SCAN_TRAFFIC_BYTES = None
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def aggregate(elapsed_s: float, units: float, world: int, device=None):
+    """Max of the elapsed times and sum of the units over all ranks."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.6)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, _dt.datetime.now())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if self.t0 and self.t1 and self.t0 <= ts <= self.t1]
+        use = inside if inside else [p for _, p in rows]
+        mhz = [float(p[2]) for p in use if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for p in use if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_max": max((float(p[4]) for p in use if p[4].replace(".", "").isdigit()), default=None)}
+
+
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+def time_events(fn, reps, warmup, flush=None):
+    """Median and mean per-call milliseconds of fn() with CUDA events on the
+    current stream; ``flush`` (if any) runs between calls outside the events."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times), statistics.fmean(times)
+
+
+def cpu_oracle_rate(x: np.ndarray, budget_s: float):
+    """Serial oracle exclusive add-scan throughput (Gelem/s) on repeated runs
+    over ``x`` until ``budget_s`` seconds of CPU work have been spent."""
+    import oracle
+    oracle.scan(x[:1024], "add", False)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.scan(x, "add", False)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s and reps >= 2:
+            break
+    return x.size * reps / el / 1e9, reps, el
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    import stream_compaction_device_gb300 as ds
+    from stream_compaction_device_gb300 import workloads as wl
+
+    ds.load()
+    if args.carry != "default":
+        ds.set_carry_mode(args.carry)
+    n = args.n
+    peak, peak_kind = peak_hbm()
+    x_host = wl.brackets(n)
+    d_in = torch.from_numpy(x_host).cuda()
+    d_out = torch.empty_like(d_in)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 3 if args.carry == "rts" else 1
+
+    def step():
+        ds.scan_exclusive(d_in, d_out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    if rank == 0 and not args.no_clocks:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    barrier(world)
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    assert ds.device_status() == 0, "device-side error during the timed region"
+    t_max, units = aggregate(elapsed, float(n) * args.steps, world, torch.device("cuda", local))
+    clock_info = clocks.stop() if (rank == 0 and not args.no_clocks) else None
+
+    # parity spot check of the timed output (last step) against the oracle
+    # on sampled positions: z[i] = sum of x[0..i-1]
+    idx = np.unique(np.concatenate([np.arange(8), np.random.default_rng(0).integers(0, n, 64), [n - 1]]))
+    pref = np.concatenate([[0], np.cumsum(x_host, dtype=np.int64)])
+    got = d_out[torch.from_numpy(idx).cuda()].cpu().numpy()
+    parity_ok = bool(np.array_equal(got.astype(np.int64), pref[idx]))
+
+    value = units / t_max / 1e9
+    kernel_s = elapsed / args.steps
+    alg_bytes = 2 * n * 4
+    achieved = alg_bytes / kernel_s / 1e9
+
+    # end to end from pinned host memory through the public API
+    e2e = None
+    if not args.no_e2e:
+        h_in = torch.from_numpy(x_host).pin_memory()
+        h_out = torch.empty_like(h_in).pin_memory()
+        e2e_steps = max(3, min(20, args.steps))
+        for _ in range(2):
+            ds.scan_host(h_in, inclusive=False, out_host=h_out, work=(d_in, d_out))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            ds.scan_host(h_in, inclusive=False, out_host=h_out, work=(d_in, d_out))
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+        el, u = aggregate(el, float(n) * e2e_steps, world, torch.device("cuda", local))
+        e2e = {"value": round(u / el / 1e9, 3), "unit": "Gelem/s", "h2d_bytes_per_step": n * 4,
+               "d2h_bytes_per_step": n * 4, "steps": e2e_steps}
+        del h_in, h_out
+
+    extra = None
+    if not args.no_extras and rank == 0:
+        extra = run_extras(args, ds, wl, d_in, d_out, peak)
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu:
+        rate, reps, el = cpu_oracle_rate(x_host, args.cpu_budget)
+        cpu = {"value": round(rate, 4), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+               "sample": f"serial oracle exclusive add-scan of the full 2^{n.bit_length() - 1}-element "
+                         f"workload, {reps} runs, {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "Gelem/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max / args.steps * 1e3, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic",
+            "config": {"workload": f"int32 exclusive add-scan, N=2^{n.bit_length() - 1}, +1/-1 bracket "
+                                   "sequence (p=0.5, seed 3)", "n": n, "op": "add", "inclusive": False,
+                       "carry": args.carry, "tile_elems": 4096,
+                       "l2": "input and output 1 GiB each (> 126 MB L2); no flush between steps",
+                       "replicas": world},
+            "hbm_gbs": round(achieved, 1), "pct_peak": round(100 * achieved / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": SCAN_TRAFFIC_BYTES,
+                         "kernel": "scan_lookback_kernel<AddU32,256,4,exclusive>",
+                         "algorithmic_bytes_per_launch": alg_bytes, "peak_kind": peak_kind},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
+            "clocks": clock_info, "parity_sampled": parity_ok, "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_extras(args, ds, wl, d_in, d_out, peak):
+    """Secondary rows: each timed with CUDA events (median of reps)."""
+    import torch
+    out = {}
+    reps = args.extra_reps
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.zero_()
+
+    def row(n_elems, ms, nbytes):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"us": round(ms * 1e3, 2), "gelem_s": round(n_elems / (ms / 1e3) / 1e9, 2),
+                "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
+    n = d_in.numel()
+    # inclusive add on the same array, and the max / xor sweep
+    med, _ = time_events(lambda: ds.scan_inclusive(d_in, d_out), reps, 3)
+    out["i32_add_inclusive_2^28"] = row(n, med, 8 * n)
+    del d_in
+    xm = torch.from_numpy(wl.max_values(n)).cuda()
+    med, _ = time_events(lambda: ds.scan_inclusive(xm, d_out, op="max"), reps, 3)
+    out["i32_max_inclusive_2^28"] = row(n, med, 8 * n)
+    xm.copy_(torch.from_numpy(wl.xor_values(n).view(np.int32)))
+    med, _ = time_events(lambda: ds.scan_inclusive(xm, d_out, op="xor", as_uint32=True), reps, 3)
+    out["u32_xor_inclusive_2^28"] = row(n, med, 8 * n)
+    ds.set_carry_mode("rts")
+    med, _ = time_events(lambda: ds.scan_exclusive(xm, d_out), reps, 3)
+    out["i32_add_exclusive_2^28_reduce_then_scan"] = row(n, med, 8 * n)
+    ds.set_carry_mode(args.carry)
+    del xm, d_out
+
+    # compaction at N = 2^26
+    nc = wl.N_COMPACT
+    v = wl.compaction_values(nc)
+    dv = torch.from_numpy(v).cuda()
+    dout = torch.empty_like(dv)
+    cnt = torch.empty(1, dtype=torch.int32, device="cuda")
+    comp = {}
+    for sel in wl.SELECTIVITIES:
+        f = torch.from_numpy(wl.predicate_flags(v, wl.threshold_for(sel))).cuda()
+        med, _ = time_events(lambda: ds.compact(dv, f, dout, cnt), reps, 3)
+        k = int(cnt.item())
+        r = row(nc, med, 5 * nc + 4 * k + 4)
+        r["kept"] = k
+        comp[f"{int(sel * 100)}%"] = r
+        del f
+    out["compaction_2^26"] = comp
+
+    # split and radix sort at N = 2^26
+    keys = torch.from_numpy(wl.radix_keys(nc).view(np.int32)).cuda()
+    med, _ = time_events(lambda: ds.split_bit(keys, 17, dout), reps, 3)
+    out["split_bit_2^26"] = row(nc, med, 12 * nc)
+    work = torch.empty_like(keys)
+    tmp = torch.empty_like(keys)
+    sreps = max(3, reps // 4)
+
+    def sort_once():
+        work.copy_(keys)
+        ds.radix_sort(work, tmp)
+    copy_med, _ = time_events(lambda: work.copy_(keys), sreps, 2)
+    med, _ = time_events(sort_once, sreps, 2)
+    sort_ms = med - copy_med
+    out["radix_sort_32pass_2^26"] = {"ms": round(sort_ms, 3), "gelem_s": round(nc / (sort_ms / 1e3) / 1e9, 2),
+                                     "gbs": round((32 * 8 * nc + 4 * nc) / (sort_ms / 1e3) / 1e9, 1),
+                                     "frac": round((32 * 8 * nc + 4 * nc) / (sort_ms / 1e3) / 1e9 / peak, 4)}
+    del dv, dout, keys, work, tmp
+
+    # fp32 add at N = 2^24 (128 MB of traffic: L2 flushed between reps)
+    xf = torch.from_numpy(wl.unit_floats()).cuda()
+    yf = torch.empty_like(xf)
+    nf = xf.numel()
+    med, _ = time_events(lambda: ds.scan_inclusive(xf, yf), reps, 3, flush=flush)
+    out["f32_add_inclusive_2^24"] = row(nf, med, 8 * nf)
+    med, _ = time_events(lambda: ds.scan_exclusive(xf, yf), reps, 3, flush=flush)
+    out["f32_add_exclusive_2^24"] = row(nf, med, 8 * nf)
+    del xf, yf
+
+    # N = 65,536 latency (launch-bound)
+    xs = torch.from_numpy(wl.small_digits()).cuda()
+    ys = torch.empty_like(xs)
+    med, _ = time_events(lambda: ds.scan_exclusive(xs, ys), reps, 3, flush=flush)
+    out["i32_add_exclusive_65536"] = row(xs.numel(), med, 8 * xs.numel())
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from stream_compaction_device_gb300 import workloads as wl
+    n = args.n
+    x = wl.brackets(n)[:REF_SAMPLE].copy()
+    for _ in range(args.warmup):
+        oracle.scan(x, "add", False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan(x, "add", False)
+    el = time.perf_counter() - t0
+    value = REF_SAMPLE * args.steps / el / 1e9
+    sample = (f"serial oracle exclusive add-scan of the first 2^22 elements of the 2^{n.bit_length() - 1}"
+              f"-element workload per step, {args.steps} steps")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Gelem/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": f"int32 exclusive add-scan, N=2^{n.bit_length() - 1}, +1/-1 bracket sequence "
+                               "(p=0.5, seed 3)", "n": n, "op": "add", "inclusive": False},
+        "cpu_baseline": {"value": round(value, 4), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--n", type=int, default=N_HEADLINE)
+    p.add_argument("--carry", choices=["default", "lookback", "rts"], default="default")
+    p.add_argument("--extra-reps", type=int, default=20)
+    p.add_argument("--cpu-budget", type=float, default=10.0)
+    p.add_argument("--no-extras", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

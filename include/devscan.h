@@ -1,0 +1,168 @@
+/*
+ * devscan -- device-wide parallel prefix scan, stream compaction and radix
+ * one-bit split for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * C ABI.  Every pointer argument of a compute call is a DEVICE pointer owned
+ * by the caller; the library never frees, retains or reallocates it.  Every
+ * compute call is asynchronous and ordered on the caller's `stream`: it
+ * validates its arguments on the host, launches its kernels and returns.
+ * Launch errors are returned immediately as DEVSCAN_ERR_CUDA; errors raised
+ * inside a kernel (a bounded inter-block wait that ran out) are recorded in a
+ * per-stream device word and reported by devscan_device_status().
+ *
+ * Scratch memory.  The single-pass kernels keep a small per-stream workspace
+ * (one 8-byte status word per tile of the largest input seen, plus a few
+ * counters) that the library allocates stream-ordered on first use
+ * (cudaMallocAsync) and reuses for later calls on the same stream.  Calls on
+ * one stream never race on it; calls on different streams use different
+ * workspaces.  devscan_stream_release() frees a stream's workspace.
+ *
+ * Pages the operations follow:
+ *   [P1] geek-doc.cn/chip-design/intermediate/parallel-prefix-scan,
+ *        "并行前缀和 scan: Hillis-Steele、Blelloch 与 warp shuffle 三种写法";
+ *   [P2] lpnh.cn/news/2866224, "并行扫描 Scan/Prefix Sum";
+ *   [P3] pgsm.cn/news/414823, "SIMT数据依赖与并行前缀和：从原理到流压缩实战".
+ */
+#ifndef DEVSCAN_H
+#define DEVSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Associative operators (P1 section 三 and P2 section 3.3: any associative
+ * operator can be scanned).  ADD wraps modulo 2^32 on the integer types;
+ * MAX compares as signed for int32 and unsigned for uint32, and follows
+ * fmaxf for fp32; XOR is defined on the integer types only. */
+typedef enum devscan_op {
+    DEVSCAN_OP_ADD = 0,
+    DEVSCAN_OP_MAX = 1,
+    DEVSCAN_OP_XOR = 2
+} devscan_op;
+
+typedef enum devscan_status {
+    DEVSCAN_OK = 0,
+    DEVSCAN_ERR_INVALID = 1,     /* bad argument: null pointer with n > 0, bad
+                                    bit index, overlapping buffers, size limit */
+    DEVSCAN_ERR_UNSUPPORTED = 2, /* operator not defined for the type (xor on fp32) */
+    DEVSCAN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    DEVSCAN_ERR_TIMEOUT = 4,     /* an inter-block wait gave up (device side) */
+    DEVSCAN_ERR_NOMEM = 5        /* the workspace could not be allocated */
+} devscan_status;
+
+/* ---------------------------------------------------------------------------
+ * Scans.  P1 section 一: inclusive y[i] = x[0] ⊕ ... ⊕ x[i]; exclusive
+ * z[i] = x[0] ⊕ ... ⊕ x[i-1] with z[0] the identity of ⊕ (0 for add and
+ * xor, INT32_MIN for int32 max, 0 for uint32 max, -inf for fp32 max).
+ *
+ *   in, out : device arrays of n elements.  out == in (in place) is allowed;
+ *             any other overlap is not checked and gives undefined results.
+ *             16-byte aligned pointers take the vectorised path, any other
+ *             element-aligned pointers are accepted on a scalar path.
+ *   n       : element count; n == 0 is a no-op returning DEVSCAN_OK.
+ *   op      : DEVSCAN_OP_*; XOR on fp32 returns DEVSCAN_ERR_UNSUPPORTED.
+ *   stream  : the CUDA stream to order the work on (0 = legacy default).
+ *
+ * fp32 add is computed in fp32 in a parallel order; its result differs from
+ * a serial fp64 sum by at most a small multiple of fp32 rounding of the
+ * running sum of |x| (P1 pitfalls: floating-point addition is not
+ * associative), and may differ between runs in the last bits.
+ * ------------------------------------------------------------------------- */
+devscan_status scan_inclusive_i32(const int32_t *in, int32_t *out, size_t n,
+                                  devscan_op op, cudaStream_t stream);
+devscan_status scan_inclusive_u32(const uint32_t *in, uint32_t *out, size_t n,
+                                  devscan_op op, cudaStream_t stream);
+devscan_status scan_inclusive_f32(const float *in, float *out, size_t n,
+                                  devscan_op op, cudaStream_t stream);
+devscan_status scan_exclusive_i32(const int32_t *in, int32_t *out, size_t n,
+                                  devscan_op op, cudaStream_t stream);
+devscan_status scan_exclusive_u32(const uint32_t *in, uint32_t *out, size_t n,
+                                  devscan_op op, cudaStream_t stream);
+devscan_status scan_exclusive_f32(const float *in, float *out, size_t n,
+                                  devscan_op op, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Stream compaction (P1 section 一; P2 section 4.1; P3 sections 4.1-4.2):
+ * out[0 .. *count) receives, in input order, every in[i] whose flags[i] is
+ * nonzero; *count is the number kept.  Each kept element's slot is the
+ * exclusive add-scan of the 0/1 predicate, computed on the device.
+ *
+ *   in     : device int32[n];  flags : device uint8[n] (nonzero = keep);
+ *   out    : device int32 with room for n elements (only *count are written);
+ *   count  : device int32, written with the number kept (0 when n == 0).
+ *   n      : at most INT32_MAX, else DEVSCAN_ERR_INVALID.
+ *   out must not overlap in or flags (DEVSCAN_ERR_INVALID).
+ * ------------------------------------------------------------------------- */
+devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out,
+                           int32_t *count, size_t n, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Radix-sort one-bit split (P1 section 一, radix sort; P2 section 4.2): a
+ * stable partition of keys by bit `bit`.  With zerosBefore(i) the exclusive
+ * add-scan of (bit is 0) and Z the total number of zeros, a key whose bit is
+ * 0 goes to out[zerosBefore(i)] and a key whose bit is 1 goes to
+ * out[Z + i - zerosBefore(i)].
+ *
+ *   keys, out : device uint32[n], not overlapping (DEVSCAN_ERR_INVALID);
+ *   bit       : 0..31, else DEVSCAN_ERR_INVALID;
+ *   n         : at most INT32_MAX, else DEVSCAN_ERR_INVALID.
+ * Runs a zero-count pass, then the single-pass split.
+ * ------------------------------------------------------------------------- */
+devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_t n,
+                             cudaStream_t stream);
+
+/* Least-significant-bit-first radix sort of uint32 keys by 32 one-bit splits
+ * (P1 section 一: one bit per round; each round's core is a scan).  The zero
+ * count of each bit is the same in every pass (a permutation keeps it), so
+ * pass b counts the zeros of bit b+1 while it scatters and one count pass
+ * runs before pass 0.
+ *
+ *   keys : device uint32[n]; sorted ascending in place on return (stream order);
+ *   tmp  : device uint32[n] scratch owned by the caller, not overlapping keys;
+ *   n    : at most INT32_MAX, else DEVSCAN_ERR_INVALID.
+ * ------------------------------------------------------------------------- */
+devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Status and housekeeping.
+ * ------------------------------------------------------------------------- */
+
+/* Synchronises `stream`, then reports and clears the device-side error word
+ * of the stream's workspace: DEVSCAN_ERR_TIMEOUT if a bounded inter-block
+ * wait gave up since the last query (the affected results are not valid),
+ * DEVSCAN_ERR_CUDA if the synchronisation failed, else DEVSCAN_OK. */
+devscan_status devscan_device_status(cudaStream_t stream);
+
+/* Static English text for a status code. */
+const char *devscan_status_string(devscan_status status);
+
+/* Frees the workspace tied to `stream` (stream-ordered, so work already
+ * queued on it finishes first).  Call before destroying a stream that ran
+ * devscan work; a later call on the stream allocates a new workspace. */
+devscan_status devscan_stream_release(cudaStream_t stream);
+
+/* Inter-block carry strategy for the scans (P1 section 四 describes the
+ * three-phase "reduce, scan the block totals, add the offsets" scheme; a
+ * single-pass chained scan with look-back is the alternative):
+ *   0 = default (single-pass look-back), 1 = single-pass look-back,
+ *   2 = reduce-then-scan (three launches, one extra read of the input).
+ * Process-wide; meant for measurement.  Returns DEVSCAN_ERR_INVALID for
+ * any other mode. */
+devscan_status devscan_set_carry_mode(int mode);
+
+/* Self-test of the bounded inter-block wait: launches two blocks on
+ * `stream` where the second waits for a tile status that nothing ever
+ * publishes, giving up after `spin_limit` polls.  Afterwards
+ * devscan_device_status(stream) returns DEVSCAN_ERR_TIMEOUT.  No kernel
+ * faults or hangs. */
+devscan_status devscan_selftest_stalled_wait(unsigned int spin_limit, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DEVSCAN_H */

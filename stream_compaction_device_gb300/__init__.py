@@ -1,0 +1,161 @@
+"""devscan for GB300: device-wide prefix scan, stream compaction and the
+radix one-bit split as hand-written sm_103a CUDA kernels behind a C ABI.
+
+The functions below take CUDA tensors (PyTorch is used for device memory
+and streams only), pass their device pointers and the current CUDA stream
+to ``libdevscan.so`` and return.  All work is asynchronous on that stream.
+``scan_host`` is the one host-buffer entry: it copies a pinned host array
+to the device, scans it and copies the result back.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import DevscanError, OPS, load
+
+__all__ = ["scan_inclusive", "scan_exclusive", "compact", "split_bit", "radix_sort", "scan_host",
+           "device_status", "set_carry_mode", "stream_release", "selftest_stalled_wait", "DevscanError",
+           "load"]
+
+_SUFFIX = {torch.int32: "i32", torch.float32: "f32"}
+if hasattr(torch, "uint32"):
+    _SUFFIX[torch.uint32] = "u32"
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_cuda(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _scan(direction: str, x: torch.Tensor, out, op: str, stream, dtype_override=None):
+    _check_cuda(x, "x")
+    suffix = dtype_override or _SUFFIX.get(x.dtype)
+    if suffix is None:
+        raise TypeError(f"unsupported dtype {x.dtype} (int32, uint32, float32)")
+    if out is None:
+        out = torch.empty_like(x)
+    _check_cuda(out, "out")
+    if out.numel() != x.numel() or out.dtype != x.dtype:
+        raise ValueError("out must match x in size and dtype")
+    fn = getattr(load(), f"scan_{direction}_{suffix}")
+    _lib.check(fn(x.data_ptr(), out.data_ptr(), x.numel(), OPS[op], _stream_handle(stream)),
+               f"scan_{direction}_{suffix}")
+    return out
+
+
+def scan_inclusive(x: torch.Tensor, out: torch.Tensor | None = None, op: str = "add", stream=None,
+                   as_uint32: bool = False) -> torch.Tensor:
+    """y[i] = x[0] op ... op x[i].  ``as_uint32`` treats an int32 tensor's
+    bits as uint32 (unsigned max)."""
+    return _scan("inclusive", x, out, op, stream, "u32" if as_uint32 else None)
+
+
+def scan_exclusive(x: torch.Tensor, out: torch.Tensor | None = None, op: str = "add", stream=None,
+                   as_uint32: bool = False) -> torch.Tensor:
+    """z[i] = x[0] op ... op x[i-1]; z[0] = identity of op."""
+    return _scan("exclusive", x, out, op, stream, "u32" if as_uint32 else None)
+
+
+def compact(values: torch.Tensor, flags: torch.Tensor, out: torch.Tensor | None = None,
+            count: torch.Tensor | None = None, stream=None):
+    """Order-preserving compaction.  Returns (out, count): the first
+    ``count`` elements of ``out`` are the values whose flag is nonzero.
+    Both stay on the device; nothing synchronises."""
+    _check_cuda(values, "values")
+    _check_cuda(flags, "flags")
+    if values.dtype != torch.int32 or flags.dtype != torch.uint8:
+        raise TypeError("values must be int32 and flags uint8")
+    if values.numel() != flags.numel():
+        raise ValueError("values and flags differ in length")
+    if out is None:
+        out = torch.empty_like(values)
+    if count is None:
+        count = torch.empty(1, dtype=torch.int32, device=values.device)
+    _check_cuda(out, "out")
+    _check_cuda(count, "count")
+    _lib.check(load().compact_i32(values.data_ptr(), flags.data_ptr(), out.data_ptr(), count.data_ptr(),
+                                  values.numel(), _stream_handle(stream)), "compact_i32")
+    return out, count
+
+
+def split_bit(keys: torch.Tensor, bit: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Stable partition of 32-bit keys by bit ``bit``: zeros first."""
+    _check_cuda(keys, "keys")
+    if keys.element_size() != 4 or keys.is_floating_point():
+        raise TypeError("keys must be a 32-bit integer tensor (bits read as uint32)")
+    if out is None:
+        out = torch.empty_like(keys)
+    _check_cuda(out, "out")
+    _lib.check(load().split_bit_u32(keys.data_ptr(), out.data_ptr(), int(bit), keys.numel(),
+                                    _stream_handle(stream)), "split_bit_u32")
+    return out
+
+
+def radix_sort(keys: torch.Tensor, tmp: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """In-place ascending sort of 32-bit keys (bits read as uint32) by 32
+    one-bit splits; ``tmp`` is a same-size scratch tensor."""
+    _check_cuda(keys, "keys")
+    if keys.element_size() != 4 or keys.is_floating_point():
+        raise TypeError("keys must be a 32-bit integer tensor (bits read as uint32)")
+    if tmp is None:
+        tmp = torch.empty_like(keys)
+    _check_cuda(tmp, "tmp")
+    _lib.check(load().radix_sort_u32(keys.data_ptr(), tmp.data_ptr(), keys.numel(), _stream_handle(stream)),
+               "radix_sort_u32")
+    return keys
+
+
+def scan_host(x_host: torch.Tensor, inclusive: bool = False, op: str = "add", device="cuda",
+              stream=None, out_host: torch.Tensor | None = None, work=None) -> torch.Tensor:
+    """Scan a host array end to end: host-to-device copy, device scan,
+    device-to-host copy, all ordered on ``stream``; returns once the result
+    is in ``out_host``.  Pinned host tensors make the copies asynchronous.
+    ``work`` may pass preallocated (device input, device output) tensors."""
+    if x_host.is_cuda:
+        raise ValueError("x_host must be a host tensor")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    with torch.cuda.stream(s):
+        if work is None:
+            d_in = torch.empty(x_host.shape, dtype=x_host.dtype, device=device)
+            d_out = torch.empty_like(d_in)
+        else:
+            d_in, d_out = work
+        d_in.copy_(x_host, non_blocking=True)
+        (scan_inclusive if inclusive else scan_exclusive)(d_in, d_out, op=op, stream=s)
+        if out_host is None:
+            out_host = torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=x_host.is_pinned())
+        out_host.copy_(d_out, non_blocking=True)
+    s.synchronize()
+    return out_host
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) its device-side status."""
+    return load().devscan_device_status(_stream_handle(stream))
+
+
+def set_carry_mode(mode: str) -> None:
+    """'lookback' (default) or 'rts' (reduce-then-scan), process-wide."""
+    code = {"default": 0, "lookback": 1, "rts": 2}[mode]
+    _lib.check(load().devscan_set_carry_mode(code), "devscan_set_carry_mode")
+
+
+def stream_release(stream=None) -> None:
+    _lib.check(load().devscan_stream_release(_stream_handle(stream)), "devscan_stream_release")
+
+
+def selftest_stalled_wait(spin_limit: int = 1000, stream=None) -> int:
+    """Run the bounded-wait self-test and return the status that
+    ``device_status`` then reports (DEVSCAN_ERR_TIMEOUT = 4 expected)."""
+    _lib.check(load().devscan_selftest_stalled_wait(int(spin_limit), _stream_handle(stream)),
+               "devscan_selftest_stalled_wait")
+    return device_status(stream)

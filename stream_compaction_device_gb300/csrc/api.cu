@@ -1,0 +1,278 @@
+// C ABI of the devscan library: argument validation, the per-stream
+// workspace, and dispatch to the kernels.  Declared in include/devscan.h.
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/devscan.h"
+#include "core.cuh"
+#include "launch.h"
+
+namespace devscan {
+namespace {
+
+// Polls of a look-back wait before it gives up (each poll after the fourth
+// sleeps 32-256 ns, so the bound is well above any legitimate wait: a
+// predecessor tile only has to load and reduce its own data).
+constexpr unsigned kSpinLimit = 1u << 21;
+
+std::atomic<int> g_carry_mode{kCarryDefault};
+
+struct Slot {
+    void *base = nullptr;
+    size_t bytes = 0;
+    Workspace ws;
+};
+
+std::mutex g_mutex;
+std::map<std::pair<int, uintptr_t>, Slot> g_slots;
+std::map<int, int> g_num_sms;
+
+constexpr size_t kStateBytes = 256;
+
+size_t layout_bytes(unsigned capacity)
+{
+    // state | status[capacity] | never_published[2] | tile_sums[capacity]
+    return kStateBytes + static_cast<size_t>(capacity) * 8 + 16 + static_cast<size_t>(capacity) * 4 + 256;
+}
+
+devscan_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DEVSCAN_OK : DEVSCAN_ERR_CUDA; }
+
+// Finds (or grows) the workspace of (current device, stream) so that it holds
+// at least `tiles` tile slots.  Growth frees the old block and allocates a
+// new one stream-ordered, then zeroes it on the stream, so calls already
+// queued on the stream finish with the old block first.
+devscan_status acquire(cudaStream_t stream, unsigned tiles, Workspace *out)
+{
+    static_assert(sizeof(DevState) <= kStateBytes, "device state must fit its slot");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto sms = g_num_sms.find(dev);
+    if (sms == g_num_sms.end()) {
+        int count = 0;
+        if (cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DEVSCAN_ERR_CUDA;
+        sms = g_num_sms.emplace(dev, count).first;
+    }
+    Slot &slot = g_slots[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (slot.base == nullptr || slot.ws.capacity < tiles) {
+        unsigned capacity = 1024;
+        while (capacity < tiles) capacity *= 2;
+        const size_t bytes = layout_bytes(capacity);
+        if (slot.base != nullptr) {
+            if (cudaFreeAsync(slot.base, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+            slot.base = nullptr;
+        }
+        void *base = nullptr;
+        const cudaError_t e = cudaMallocAsync(&base, bytes, stream);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            g_slots.erase({dev, reinterpret_cast<uintptr_t>(stream)});
+            return e == cudaErrorMemoryAllocation ? DEVSCAN_ERR_NOMEM : DEVSCAN_ERR_CUDA;
+        }
+        if (cudaMemsetAsync(base, 0, bytes, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+        char *p = static_cast<char *>(base);
+        slot.base = base;
+        slot.bytes = bytes;
+        slot.ws.state = reinterpret_cast<DevState *>(p);
+        slot.ws.status = reinterpret_cast<unsigned long long *>(p + kStateBytes);
+        slot.ws.never_published = slot.ws.status + capacity;
+        slot.ws.tile_sums = reinterpret_cast<uint32_t *>(slot.ws.never_published + 2);
+        slot.ws.capacity = capacity;
+    }
+    slot.ws.num_sms = sms->second;
+    *out = slot.ws;
+    return DEVSCAN_OK;
+}
+
+bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bbytes && y < x + abytes;
+}
+
+devscan_status scan_common(ElemType type, bool inclusive, const void *in, void *out, size_t n, devscan_op op,
+                           cudaStream_t stream)
+{
+    if (op != DEVSCAN_OP_ADD && op != DEVSCAN_OP_MAX && op != DEVSCAN_OP_XOR) return DEVSCAN_ERR_INVALID;
+    if (type == ElemType::F32 && op == DEVSCAN_OP_XOR) return DEVSCAN_ERR_UNSUPPORTED;
+    if (n == 0) return DEVSCAN_OK;
+    if (in == nullptr || out == nullptr) return DEVSCAN_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(in) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+        return DEVSCAN_ERR_INVALID;
+    const size_t max_n = static_cast<size_t>(0xffffffffu) * kScanTile;
+    if (n > max_n) return DEVSCAN_ERR_INVALID;
+    const unsigned tiles = tiles_for(n, kScanTile);
+    Workspace ws;
+    const devscan_status st = acquire(stream, tiles, &ws);
+    if (st != DEVSCAN_OK) return st;
+    const bool aligned = reinterpret_cast<uintptr_t>(in) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0;
+    const int carry = g_carry_mode.load(std::memory_order_relaxed);
+    return from_cuda(launch_scan(type, static_cast<int>(op), inclusive, in, out, n, aligned, carry, ws,
+                                 kSpinLimit, stream));
+}
+
+}  // namespace
+}  // namespace devscan
+
+using namespace devscan;
+
+extern "C" {
+
+devscan_status scan_inclusive_i32(const int32_t *in, int32_t *out, size_t n, devscan_op op, cudaStream_t stream)
+{
+    return scan_common(ElemType::I32, true, in, out, n, op, stream);
+}
+devscan_status scan_inclusive_u32(const uint32_t *in, uint32_t *out, size_t n, devscan_op op, cudaStream_t stream)
+{
+    return scan_common(ElemType::U32, true, in, out, n, op, stream);
+}
+devscan_status scan_inclusive_f32(const float *in, float *out, size_t n, devscan_op op, cudaStream_t stream)
+{
+    return scan_common(ElemType::F32, true, in, out, n, op, stream);
+}
+devscan_status scan_exclusive_i32(const int32_t *in, int32_t *out, size_t n, devscan_op op, cudaStream_t stream)
+{
+    return scan_common(ElemType::I32, false, in, out, n, op, stream);
+}
+devscan_status scan_exclusive_u32(const uint32_t *in, uint32_t *out, size_t n, devscan_op op, cudaStream_t stream)
+{
+    return scan_common(ElemType::U32, false, in, out, n, op, stream);
+}
+devscan_status scan_exclusive_f32(const float *in, float *out, size_t n, devscan_op op, cudaStream_t stream)
+{
+    return scan_common(ElemType::F32, false, in, out, n, op, stream);
+}
+
+devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out, int32_t *count, size_t n,
+                           cudaStream_t stream)
+{
+    if (count == nullptr) return DEVSCAN_ERR_INVALID;
+    if (n > static_cast<size_t>(INT32_MAX)) return DEVSCAN_ERR_INVALID;
+    if (n > 0) {
+        if (in == nullptr || flags == nullptr || out == nullptr) return DEVSCAN_ERR_INVALID;
+        if (reinterpret_cast<uintptr_t>(in) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0 ||
+            reinterpret_cast<uintptr_t>(count) % 4 != 0)
+            return DEVSCAN_ERR_INVALID;
+        if (overlaps(out, n * 4, in, n * 4) || overlaps(out, n * 4, flags, n) || overlaps(count, 4, out, n * 4) ||
+            overlaps(count, 4, in, n * 4) || overlaps(count, 4, flags, n))
+            return DEVSCAN_ERR_INVALID;
+    }
+    if (n == 0) return from_cuda(cudaMemsetAsync(count, 0, sizeof(int32_t), stream));
+    const unsigned tiles = tiles_for(n, kCompactTile);
+    Workspace ws;
+    const devscan_status st = acquire(stream, tiles, &ws);
+    if (st != DEVSCAN_OK) return st;
+    return from_cuda(launch_compact(in, flags, out, count, n, ws, kSpinLimit, stream));
+}
+
+devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_t n, cudaStream_t stream)
+{
+    if (bit < 0 || bit > 31) return DEVSCAN_ERR_INVALID;
+    if (n > static_cast<size_t>(INT32_MAX)) return DEVSCAN_ERR_INVALID;
+    if (n == 0) return DEVSCAN_OK;
+    if (keys == nullptr || out == nullptr) return DEVSCAN_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(keys) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+        return DEVSCAN_ERR_INVALID;
+    if (overlaps(keys, n * 4, out, n * 4)) return DEVSCAN_ERR_INVALID;
+    const unsigned tiles = tiles_for(n, kSplitTile);
+    Workspace ws;
+    devscan_status st = acquire(stream, tiles, &ws);
+    if (st != DEVSCAN_OK) return st;
+    unsigned *z = &ws.state->zeros[40];
+    if (cudaMemsetAsync(z, 0, sizeof(unsigned), stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    cudaError_t e = launch_count_zeros(keys, n, bit, z, ws, stream);
+    if (e != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    return from_cuda(launch_split(keys, out, n, bit, z, nullptr, ws, kSpinLimit, stream));
+}
+
+devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStream_t stream)
+{
+    if (n > static_cast<size_t>(INT32_MAX)) return DEVSCAN_ERR_INVALID;
+    if (n == 0) return DEVSCAN_OK;
+    if (keys == nullptr || tmp == nullptr) return DEVSCAN_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(keys) % 4 != 0 || reinterpret_cast<uintptr_t>(tmp) % 4 != 0)
+        return DEVSCAN_ERR_INVALID;
+    if (overlaps(keys, n * 4, tmp, n * 4)) return DEVSCAN_ERR_INVALID;
+    const unsigned tiles = tiles_for(n, kSplitTile);
+    Workspace ws;
+    devscan_status st = acquire(stream, tiles, &ws);
+    if (st != DEVSCAN_OK) return st;
+    unsigned *z = ws.state->zeros;   // z[b] = zero count of bit b
+    if (cudaMemsetAsync(z, 0, 33 * sizeof(unsigned), stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    if (launch_count_zeros(keys, n, 0, &z[0], ws, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    uint32_t *src = keys, *dst = tmp;
+    for (int bit = 0; bit < 32; ++bit) {
+        unsigned *next = (bit < 31) ? &z[bit + 1] : nullptr;
+        if (launch_split(src, dst, n, bit, &z[bit], next, ws, kSpinLimit, stream) != cudaSuccess)
+            return DEVSCAN_ERR_CUDA;
+        std::swap(src, dst);
+    }
+    return DEVSCAN_OK;
+}
+
+devscan_status devscan_device_status(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    DevState *state = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = g_slots.find({dev, reinterpret_cast<uintptr_t>(stream)});
+        if (it == g_slots.end()) return DEVSCAN_OK;
+        state = it->second.ws.state;
+    }
+    unsigned err = 0;
+    if (cudaMemcpy(&err, &state->error, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DEVSCAN_ERR_CUDA;
+    if (err != 0 && cudaMemset(&state->error, 0, sizeof(unsigned)) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    return (err & kErrTimeout) ? DEVSCAN_ERR_TIMEOUT : DEVSCAN_OK;
+}
+
+const char *devscan_status_string(devscan_status status)
+{
+    switch (status) {
+    case DEVSCAN_OK: return "ok";
+    case DEVSCAN_ERR_INVALID: return "invalid argument";
+    case DEVSCAN_ERR_UNSUPPORTED: return "operator not supported for this element type";
+    case DEVSCAN_ERR_CUDA: return "CUDA runtime error";
+    case DEVSCAN_ERR_TIMEOUT: return "inter-block wait timed out on the device";
+    case DEVSCAN_ERR_NOMEM: return "out of device memory for the workspace";
+    }
+    return "unknown status";
+}
+
+devscan_status devscan_stream_release(cudaStream_t stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_slots.find({dev, reinterpret_cast<uintptr_t>(stream)});
+    if (it == g_slots.end()) return DEVSCAN_OK;
+    void *base = it->second.base;
+    g_slots.erase(it);
+    return from_cuda(cudaFreeAsync(base, stream));
+}
+
+devscan_status devscan_set_carry_mode(int mode)
+{
+    if (mode != kCarryDefault && mode != kCarryLookback && mode != kCarryReduceThenScan) return DEVSCAN_ERR_INVALID;
+    g_carry_mode.store(mode, std::memory_order_relaxed);
+    return DEVSCAN_OK;
+}
+
+devscan_status devscan_selftest_stalled_wait(unsigned int spin_limit, cudaStream_t stream)
+{
+    if (spin_limit == 0) return DEVSCAN_ERR_INVALID;
+    Workspace ws;
+    const devscan_status st = acquire(stream, 1, &ws);
+    if (st != DEVSCAN_OK) return st;
+    return from_cuda(launch_stalled_wait(ws, spin_limit, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+// Stream compaction, fused into one single-pass kernel (sm_103a).
+//
+// geek-doc.cn "并行前缀和 scan ..." section 一 and lpnh.cn "并行扫描" section
+// 4.1: each kept element's output slot is the exclusive add-scan of the 0/1
+// predicate; pgsm.cn "SIMT数据依赖与并行前缀和" section 4.2: the two-kernel
+// block-count variant and the last thread writing the total.  Here the
+// predicate scan, the inter-block carry (decoupled look-back on kept
+// counts), the staged scatter and the count all happen in one launch that
+// reads values and flags once and writes only the kept values.
+#include "core.cuh"
+#include "launch.h"
+#include "stage.cuh"
+
+namespace devscan {
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t *p) { return __ldcs(p); }
+
+// Bit k set when byte k of f is nonzero.
+__device__ __forceinline__ uint32_t nonzero_byte_mask(uint32_t f)
+{
+    return ((f & 0x000000ffu) ? 1u : 0u) | ((f & 0x0000ff00u) ? 2u : 0u) | ((f & 0x00ff0000u) ? 4u : 0u) |
+           ((f & 0xff000000u) ? 8u : 0u);
+}
+
+template <int THREADS, int VECS, bool ALIGNED, bool OUT_ALIGNED>
+__global__ void __launch_bounds__(THREADS)
+compact_kernel(const uint32_t *__restrict__ in, const uint8_t *__restrict__ flags, uint32_t *__restrict__ out,
+               int32_t *__restrict__ count, size_t n, unsigned num_tiles, unsigned long long *status,
+               DevState *st, unsigned capacity, unsigned spin_limit)
+{
+    constexpr int NWARPS = THREADS / 32;
+    constexpr int WARP_ITEMS = 32 * 4 * VECS;
+    constexpr int TILE = THREADS * 4 * VECS;
+    using B = StageBuffer<TILE>;
+    __shared__ __align__(16) uint32_t s_stage_raw[B::kWords];
+    __shared__ unsigned s_warp[NWARPS];
+    __shared__ unsigned s_prefix;
+    __shared__ unsigned s_tile;
+    uint32_t *s_stage = s_stage_raw + B::kLead;
+    const AddU32 op;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) s_tile = atomicAdd(&st->ticket, 1u);
+    __syncthreads();
+    const unsigned tile = s_tile;
+    if (tile >= num_tiles) return;   // never taken: each launch hands out exactly num_tiles tickets
+    const size_t tile_base = static_cast<size_t>(tile) * TILE;
+    const size_t warp_base = tile_base + static_cast<size_t>(warp) * WARP_ITEMS;
+    const bool full = tile_base + TILE <= n;
+
+    uint32_t x[VECS][4];
+    load_rows<uint32_t, VECS, ALIGNED>(in, warp_base, n, lane, full, x, 0u);
+    uint32_t keep[VECS];
+    if (ALIGNED && full) {
+        uint32_t f[VECS];
+#pragma unroll
+        for (int r = 0; r < VECS; ++r)
+            f[r] = ld_stream_u32(reinterpret_cast<const uint32_t *>(flags + warp_base) + r * 32 + lane);
+#pragma unroll
+        for (int r = 0; r < VECS; ++r) keep[r] = nonzero_byte_mask(f[r]);
+    } else {
+#pragma unroll
+        for (int r = 0; r < VECS; ++r) {
+            const size_t e = warp_base + static_cast<size_t>(r * 32 + lane) * 4;
+            uint32_t m = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (e + k < n && flags[e + k] != 0) m |= 1u << k;
+            keep[r] = m;
+        }
+    }
+
+    uint32_t t[VECS];
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) t[r] = __popc(keep[r]);
+    uint32_t row_excl[VECS], warp_total;
+    warp_scan_rows<AddU32, VECS>(op, t, lane, row_excl, warp_total);
+    if (lane == 0) s_warp[warp] = warp_total;
+    __syncthreads();
+    uint32_t warp_excl, tile_total;
+    block_scan_warps<AddU32, NWARPS>(op, s_warp, warp, lane, warp_excl, tile_total);
+
+    unsigned tag = 0;
+    if (warp == 0) {
+        tag = __shfl_sync(kFullMask, lane == 0 ? read_tag(st) : 0u, 0);
+        publish<AddU32>(status, tile, tag, tile == 0 ? kFlagInclusive : kFlagAggregate, tile_total, lane);
+    }
+
+    // stage the kept values at their tile-local rank
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) {
+        uint32_t rank = warp_excl + row_excl[r];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if ((keep[r] >> k) & 1u) {
+                s_stage[rank] = x[r][k];
+                ++rank;
+            }
+        }
+    }
+
+    if (warp == 0) {
+        uint32_t prefix = 0;
+        if (tile != 0) {
+            prefix = lookback<AddU32>(op, status, tile, tag, &st->error, spin_limit, lane);
+            publish<AddU32>(status, tile, tag, kFlagInclusive, prefix + tile_total, lane);
+        }
+        if (lane == 0) {
+            s_prefix = prefix;
+            if (tile == num_tiles - 1) *count = static_cast<int32_t>(prefix + tile_total);
+        }
+        if (tile == num_tiles - 1) finish_launch(st, status, num_tiles, capacity, lane);
+    }
+    __syncthreads();
+
+    if (OUT_ALIGNED)
+        write_run_aligned<THREADS, TILE>(out, s_prefix, tile_total, s_stage, 0, tid, n);
+    else
+        write_run_scalar<THREADS>(out, s_prefix, tile_total, s_stage, 0, tid, n);
+}
+
+cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out, int32_t *count, size_t n,
+                           const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+{
+    constexpr int THREADS = kCompactThreads, VECS = kCompactVecs;
+    const unsigned tiles = tiles_for(n, kCompactTile);
+    const bool aligned = (reinterpret_cast<uintptr_t>(in) % 16 == 0) && (reinterpret_cast<uintptr_t>(flags) % 4 == 0);
+    const bool out_aligned = reinterpret_cast<uintptr_t>(out) % 16 == 0;
+    const uint32_t *vin = reinterpret_cast<const uint32_t *>(in);
+    uint32_t *vout = reinterpret_cast<uint32_t *>(out);
+    if (aligned && out_aligned)
+        compact_kernel<THREADS, VECS, true, true><<<tiles, THREADS, 0, s>>>(
+            vin, flags, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit);
+    else if (aligned)
+        compact_kernel<THREADS, VECS, true, false><<<tiles, THREADS, 0, s>>>(
+            vin, flags, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit);
+    else if (out_aligned)
+        compact_kernel<THREADS, VECS, false, true><<<tiles, THREADS, 0, s>>>(
+            vin, flags, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit);
+    else
+        compact_kernel<THREADS, VECS, false, false><<<tiles, THREADS, 0, s>>>(
+            vin, flags, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit);
+    return cudaGetLastError();
+}
+
+}  // namespace devscan

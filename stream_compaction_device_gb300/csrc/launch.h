@@ -1,0 +1,74 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernel
+// translation units.  Not installed; the public interface is include/devscan.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace devscan {
+
+struct DevState;
+
+// Tile geometry of the scan, compaction and split kernels: THREADS threads,
+// each holding VECS rows of four 32-bit elements.
+constexpr int kScanThreads = 256;
+constexpr int kScanVecs = 4;
+constexpr int kScanTile = kScanThreads * 4 * kScanVecs;   // 4096 elements
+constexpr int kCompactThreads = 256;
+constexpr int kCompactVecs = 4;
+constexpr int kCompactTile = kCompactThreads * 4 * kCompactVecs;
+constexpr int kSplitThreads = 256;
+constexpr int kSplitVecs = 4;
+constexpr int kSplitTile = kSplitThreads * 4 * kSplitVecs;
+constexpr int kMaxTile = 4096;   // largest of the three (workspace sizing)
+
+// Tile order: true = an atomic ticket hands out tile indices in the order
+// blocks start (forward progress does not depend on the order in which the
+// hardware dispatches blocks); false = blockIdx.x.
+constexpr bool kUseTickets = true;
+
+constexpr int kOpAdd = 0, kOpMax = 1, kOpXor = 2;
+constexpr int kCarryDefault = 0, kCarryLookback = 1, kCarryReduceThenScan = 2;
+
+enum class ElemType { I32, U32, F32 };
+
+// Per-(device, stream) scratch, carved from one allocation:
+//   state           DevState (epoch, ticket, error word, zero counts)
+//   status          `capacity` 8-byte tile status words
+//   never_published 2 words kept at zero (bounded-wait self-test)
+//   tile_sums       `capacity` 4-byte tile totals (reduce-then-scan)
+struct Workspace {
+    DevState *state = nullptr;
+    unsigned long long *status = nullptr;
+    unsigned long long *never_published = nullptr;
+    uint32_t *tile_sums = nullptr;
+    unsigned capacity = 0;
+    int num_sms = 0;
+};
+
+inline unsigned tiles_for(size_t n, int tile)
+{
+    return static_cast<unsigned>((n + static_cast<size_t>(tile) - 1) / static_cast<size_t>(tile));
+}
+
+cudaError_t launch_scan(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
+                        bool aligned, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
+cudaError_t launch_stalled_wait(const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
+cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out, int32_t *count, size_t n,
+                           const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
+// Zero count of bit `bit` over keys[0, n) added into *zeros (which the caller
+// has cleared).
+cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned *zeros, const Workspace &ws,
+                               cudaStream_t s);
+
+// One split pass by bit `bit` given the total zero count *zeros.  When
+// next_zeros is not null, the pass also adds the zero count of bit
+// `bit + 1` into *next_zeros.
+cudaError_t launch_split(const uint32_t *keys, uint32_t *out, size_t n, int bit, const unsigned *zeros,
+                         unsigned *next_zeros, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
+}  // namespace devscan

@@ -1,0 +1,310 @@
+// Device-wide inclusive / exclusive scan kernels (sm_103a).
+//
+// Two inter-block carry strategies (geek-doc.cn "并行前缀和 scan ..." section
+// 四 describes the first and mentions the second):
+//   * single pass with decoupled look-back: one launch, each element read
+//     once and written once (2 * n * sizeof(T) bytes);
+//   * reduce-then-scan: tile totals, one-block scan of the totals, then the
+//     tile scan with its offset -- three launches and one extra read of the
+//     input (3 * n * sizeof(T) bytes).
+#include "core.cuh"
+#include "launch.h"
+
+namespace devscan {
+
+// ---------------------------------------------------------------------------
+// Single-pass scan: one tile per block.
+// ---------------------------------------------------------------------------
+template <class Op, int THREADS, int VECS, bool INCLUSIVE, bool ALIGNED, bool TICKETS>
+__global__ void __launch_bounds__(THREADS)
+scan_lookback_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,
+                     unsigned num_tiles, unsigned long long *status, DevState *st, unsigned capacity,
+                     unsigned spin_limit)
+{
+    using S = typename Op::S;
+    constexpr int NWARPS = THREADS / 32;
+    constexpr int WARP_ITEMS = 32 * 4 * VECS;
+    constexpr int TILE = THREADS * 4 * VECS;
+    __shared__ S s_warp[NWARPS];
+    __shared__ S s_prefix;
+    __shared__ unsigned s_tile;
+    const Op op;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    unsigned tile;
+    if (TICKETS) {
+        if (tid == 0) s_tile = atomicAdd(&st->ticket, 1u);
+        __syncthreads();
+        tile = s_tile;
+        if (tile >= num_tiles) return;   // never taken: each launch hands out exactly num_tiles tickets
+    } else {
+        tile = blockIdx.x;
+    }
+    const size_t tile_base = static_cast<size_t>(tile) * TILE;
+    const size_t warp_base = tile_base + static_cast<size_t>(warp) * WARP_ITEMS;
+    const bool full = tile_base + TILE <= n;
+
+    S x[VECS][4];
+    load_rows<S, VECS, ALIGNED>(in, warp_base, n, lane, full, x, Op::identity());
+
+    // thread level: serial combine of the 4 elements of each row
+    S t[VECS];
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) t[r] = op(op(x[r][0], x[r][1]), op(x[r][2], x[r][3]));
+
+    S row_excl[VECS], warp_total;
+    warp_scan_rows<Op, VECS>(op, t, lane, row_excl, warp_total);
+    if (lane == 0) s_warp[warp] = warp_total;
+    __syncthreads();
+
+    S warp_excl, tile_total;
+    block_scan_warps<Op, NWARPS>(op, s_warp, warp, lane, warp_excl, tile_total);
+
+    if (warp == 0) {
+        const unsigned tag = __shfl_sync(kFullMask, lane == 0 ? read_tag(st) : 0u, 0);
+        S prefix = Op::identity();
+        if (tile == 0) {
+            publish<Op>(status, tile, tag, kFlagInclusive, tile_total, lane);
+        } else {
+            publish<Op>(status, tile, tag, kFlagAggregate, tile_total, lane);
+            prefix = lookback<Op>(op, status, tile, tag, &st->error, spin_limit, lane);
+            publish<Op>(status, tile, tag, kFlagInclusive, op(prefix, tile_total), lane);
+        }
+        if (lane == 0) s_prefix = prefix;
+        if (tile == num_tiles - 1) finish_launch(st, status, num_tiles, capacity, lane);
+    }
+    __syncthreads();
+
+    const S pfx = op(s_prefix, warp_excl);
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) {
+        S cur = op(pfx, row_excl[r]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const S v = x[r][k];
+            if (INCLUSIVE) {
+                cur = op(cur, v);
+                x[r][k] = cur;
+            } else {
+                x[r][k] = cur;
+                cur = op(cur, v);
+            }
+        }
+    }
+    store_rows<S, VECS, ALIGNED>(out, warp_base, n, lane, full, x);
+}
+
+// ---------------------------------------------------------------------------
+// Reduce-then-scan: (1) tile totals, (2) exclusive scan of the totals in one
+// block, (3) tile scan seeded with the tile's offset.
+// ---------------------------------------------------------------------------
+template <class Op, int THREADS, int VECS, bool ALIGNED>
+__global__ void __launch_bounds__(THREADS)
+rts_reduce_kernel(const typename Op::S *__restrict__ in, size_t n, typename Op::S *__restrict__ tile_sums)
+{
+    using S = typename Op::S;
+    constexpr int NWARPS = THREADS / 32;
+    constexpr int WARP_ITEMS = 32 * 4 * VECS;
+    constexpr int TILE = THREADS * 4 * VECS;
+    __shared__ S s_warp[NWARPS];
+    const Op op;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned tile = blockIdx.x;
+    const size_t tile_base = static_cast<size_t>(tile) * TILE;
+    const size_t warp_base = tile_base + static_cast<size_t>(warp) * WARP_ITEMS;
+    const bool full = tile_base + TILE <= n;
+    S x[VECS][4];
+    load_rows<S, VECS, ALIGNED>(in, warp_base, n, lane, full, x, Op::identity());
+    S v = Op::identity();
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) v = op(v, op(op(x[r][0], x[r][1]), op(x[r][2], x[r][3])));
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
+    if (lane == 0) s_warp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        S w = (lane < NWARPS) ? s_warp[lane] : Op::identity();
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) w = op(w, __shfl_xor_sync(kFullMask, w, d));
+        if (lane == 0) tile_sums[tile] = w;
+    }
+}
+
+// One block of 1024 threads scans `count` tile totals in place (exclusive),
+// 4 per thread per round, carrying the running total between rounds.
+template <class Op>
+__global__ void __launch_bounds__(1024) rts_scan_sums_kernel(typename Op::S *sums, unsigned count)
+{
+    using S = typename Op::S;
+    constexpr int NWARPS = 32;
+    __shared__ S s_warp[NWARPS];
+    __shared__ S s_carry;
+    const Op op;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_carry = Op::identity();
+    __syncthreads();
+    for (unsigned base = 0; base < count; base += 4096) {
+        S x[1][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const unsigned i = base + tid * 4 + k;
+            x[0][k] = (i < count) ? sums[i] : Op::identity();
+        }
+        S t[1] = {op(op(x[0][0], x[0][1]), op(x[0][2], x[0][3]))};
+        S row_excl[1], warp_total;
+        warp_scan_rows<Op, 1>(op, t, lane, row_excl, warp_total);
+        if (lane == 0) s_warp[warp] = warp_total;
+        __syncthreads();
+        S warp_excl, block_total;
+        block_scan_warps<Op, NWARPS>(op, s_warp, warp, lane, warp_excl, block_total);
+        const S carry = s_carry;
+        S cur = op(op(carry, warp_excl), row_excl[0]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const unsigned i = base + tid * 4 + k;
+            const S v = x[0][k];
+            if (i < count) sums[i] = cur;
+            cur = op(cur, v);
+        }
+        __syncthreads();
+        if (tid == 0) s_carry = op(carry, block_total);
+        __syncthreads();
+    }
+}
+
+template <class Op, int THREADS, int VECS, bool INCLUSIVE, bool ALIGNED>
+__global__ void __launch_bounds__(THREADS)
+rts_downsweep_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,
+                     const typename Op::S *__restrict__ tile_prefix)
+{
+    using S = typename Op::S;
+    constexpr int NWARPS = THREADS / 32;
+    constexpr int WARP_ITEMS = 32 * 4 * VECS;
+    constexpr int TILE = THREADS * 4 * VECS;
+    __shared__ S s_warp[NWARPS];
+    const Op op;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned tile = blockIdx.x;
+    const size_t tile_base = static_cast<size_t>(tile) * TILE;
+    const size_t warp_base = tile_base + static_cast<size_t>(warp) * WARP_ITEMS;
+    const bool full = tile_base + TILE <= n;
+    S x[VECS][4];
+    load_rows<S, VECS, ALIGNED>(in, warp_base, n, lane, full, x, Op::identity());
+    S t[VECS];
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) t[r] = op(op(x[r][0], x[r][1]), op(x[r][2], x[r][3]));
+    S row_excl[VECS], warp_total;
+    warp_scan_rows<Op, VECS>(op, t, lane, row_excl, warp_total);
+    if (lane == 0) s_warp[warp] = warp_total;
+    __syncthreads();
+    S warp_excl, tile_total;
+    block_scan_warps<Op, NWARPS>(op, s_warp, warp, lane, warp_excl, tile_total);
+    const S pfx = op(tile_prefix[tile], warp_excl);
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) {
+        S cur = op(pfx, row_excl[r]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const S v = x[r][k];
+            if (INCLUSIVE) {
+                cur = op(cur, v);
+                x[r][k] = cur;
+            } else {
+                x[r][k] = cur;
+                cur = op(cur, v);
+            }
+        }
+    }
+    store_rows<S, VECS, ALIGNED>(out, warp_base, n, lane, full, x);
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded wait: one warp looks back from tile 1 onto a
+// status slot that nothing ever publishes (its word is zero, which no epoch
+// tag matches), gives up after `spin_limit` polls and records the timeout.
+// ---------------------------------------------------------------------------
+__global__ void stalled_wait_kernel(const unsigned long long *never_published, DevState *st,
+                                    unsigned spin_limit)
+{
+    const AddU32 op;
+    const unsigned tag = read_tag(st);
+    (void)lookback<AddU32>(op, never_published, 1u, tag, &st->error, spin_limit, threadIdx.x & 31);
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers.
+// ---------------------------------------------------------------------------
+namespace {
+
+template <class Op, bool INCLUSIVE, bool ALIGNED>
+cudaError_t launch_lookback(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,
+                            cudaStream_t s)
+{
+    using S = typename Op::S;
+    constexpr int THREADS = kScanThreads, VECS = kScanVecs;
+    const unsigned tiles = tiles_for(n, kScanTile);
+    scan_lookback_kernel<Op, THREADS, VECS, INCLUSIVE, ALIGNED, kUseTickets><<<tiles, THREADS, 0, s>>>(
+        static_cast<const S *>(in), static_cast<S *>(out), n, tiles, ws.status, ws.state, ws.capacity,
+        spin_limit);
+    return cudaGetLastError();
+}
+
+template <class Op, bool INCLUSIVE>
+cudaError_t launch_rts(const void *in, void *out, size_t n, const Workspace &ws, cudaStream_t s)
+{
+    using S = typename Op::S;
+    constexpr int THREADS = kScanThreads, VECS = kScanVecs;
+    const unsigned tiles = tiles_for(n, kScanTile);
+    S *sums = reinterpret_cast<S *>(ws.tile_sums);
+    rts_reduce_kernel<Op, THREADS, VECS, true><<<tiles, THREADS, 0, s>>>(static_cast<const S *>(in), n, sums);
+    rts_scan_sums_kernel<Op><<<1, 1024, 0, s>>>(sums, tiles);
+    rts_downsweep_kernel<Op, THREADS, VECS, INCLUSIVE, true><<<tiles, THREADS, 0, s>>>(
+        static_cast<const S *>(in), static_cast<S *>(out), n, sums);
+    return cudaGetLastError();
+}
+
+template <class Op, bool INCLUSIVE>
+cudaError_t dispatch_op(const void *in, void *out, size_t n, bool aligned, int carry, const Workspace &ws,
+                        unsigned spin_limit, cudaStream_t s)
+{
+    if (carry == kCarryReduceThenScan && aligned) return launch_rts<Op, INCLUSIVE>(in, out, n, ws, s);
+    if (aligned) return launch_lookback<Op, INCLUSIVE, true>(in, out, n, ws, spin_limit, s);
+    return launch_lookback<Op, INCLUSIVE, false>(in, out, n, ws, spin_limit, s);
+}
+
+template <class Op>
+cudaError_t dispatch_dir(const void *in, void *out, size_t n, bool inclusive, bool aligned, int carry,
+                         const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+{
+    return inclusive ? dispatch_op<Op, true>(in, out, n, aligned, carry, ws, spin_limit, s)
+                     : dispatch_op<Op, false>(in, out, n, aligned, carry, ws, spin_limit, s);
+}
+
+}  // namespace
+
+cudaError_t launch_scan(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
+                        bool aligned, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+{
+    switch (type) {
+    case ElemType::I32:
+        if (op == kOpAdd) return dispatch_dir<AddU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+        if (op == kOpMax) return dispatch_dir<MaxI32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+        return dispatch_dir<XorU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+    case ElemType::U32:
+        if (op == kOpAdd) return dispatch_dir<AddU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+        if (op == kOpMax) return dispatch_dir<MaxU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+        return dispatch_dir<XorU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+    case ElemType::F32:
+        if (op == kOpAdd) return dispatch_dir<AddF32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+        return dispatch_dir<MaxF32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_stalled_wait(const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+{
+    stalled_wait_kernel<<<1, 32, 0, s>>>(ws.never_published, ws.state, spin_limit);
+    return cudaGetLastError();
+}
+
+}  // namespace devscan

@@ -1,0 +1,198 @@
+// Radix-sort one-bit split and the LSD radix sort built on it (sm_103a).
+//
+// geek-doc.cn "并行前缀和 scan ..." section 一 (radix sort): scan the "bit is
+// 0" predicate to get each zero's slot; a one goes to (total zeros + its
+// rank among the ones).  lpnh.cn "并行扫描" section 4.2: per-digit counts,
+// a prefix over them, then the scatter.
+//
+// The split kernel needs the total zero count Z before it can place any
+// one, and a single pass cannot know Z.  So a zero-count pass runs first;
+// inside the sort the zero count of bit b + 1 is accumulated by pass b
+// while it scatters (a stable permutation keeps every bit's count), so the
+// sort reads the keys 33 times instead of 64.
+#include <algorithm>
+
+#include "core.cuh"
+#include "launch.h"
+#include "stage.cuh"
+
+namespace devscan {
+
+__device__ __forceinline__ unsigned zeros_of(uint4 q, int bit)
+{
+    return 4u - (((q.x >> bit) & 1u) + ((q.y >> bit) & 1u) + ((q.z >> bit) & 1u) + ((q.w >> bit) & 1u));
+}
+
+// Grid-stride zero count of one bit; one atomic per warp.
+template <int THREADS, bool ALIGNED>
+__global__ void __launch_bounds__(THREADS)
+count_zeros_kernel(const uint32_t *__restrict__ keys, size_t n, int bit, unsigned *zeros)
+{
+    const size_t gtid = static_cast<size_t>(blockIdx.x) * THREADS + threadIdx.x;
+    const size_t stride = static_cast<size_t>(gridDim.x) * THREADS;
+    unsigned c = 0;
+    size_t scalar_from = 0;
+    if (ALIGNED) {
+        const size_t nvec = n / 4;
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+        size_t i = gtid;
+        for (; i + 3 * stride < nvec; i += 4 * stride) {
+            const uint4 a = ld_stream(k4 + i), b = ld_stream(k4 + i + stride);
+            const uint4 d = ld_stream(k4 + i + 2 * stride), e = ld_stream(k4 + i + 3 * stride);
+            c += zeros_of(a, bit) + zeros_of(b, bit) + zeros_of(d, bit) + zeros_of(e, bit);
+        }
+        for (; i < nvec; i += stride) c += zeros_of(ld_stream(k4 + i), bit);
+        scalar_from = nvec * 4;
+    }
+    for (size_t e = scalar_from + gtid; e < n; e += stride) c += ((keys[e] >> bit) & 1u) ? 0u : 1u;
+    c = __reduce_add_sync(kFullMask, c);
+    if ((threadIdx.x & 31) == 0 && c != 0) atomicAdd(zeros, c);
+}
+
+template <int THREADS, int VECS, bool ALIGNED>
+__global__ void __launch_bounds__(THREADS)
+split_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size_t n, int bit,
+             const unsigned *__restrict__ zeros_total, unsigned *next_zeros, int next_bit, unsigned num_tiles,
+             unsigned long long *status, DevState *st, unsigned capacity, unsigned spin_limit)
+{
+    constexpr int NWARPS = THREADS / 32;
+    constexpr int WARP_ITEMS = 32 * 4 * VECS;
+    constexpr int TILE = THREADS * 4 * VECS;
+    using B = StageBuffer<TILE>;
+    __shared__ __align__(16) uint32_t s_stage_raw[B::kWords];
+    __shared__ unsigned s_warp[NWARPS];
+    __shared__ unsigned s_next[NWARPS];
+    __shared__ unsigned s_prefix;
+    __shared__ unsigned s_tile;
+    uint32_t *s_stage = s_stage_raw + B::kLead;
+    const AddU32 op;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) s_tile = atomicAdd(&st->ticket, 1u);
+    __syncthreads();
+    const unsigned tile = s_tile;
+    if (tile >= num_tiles) return;   // never taken: each launch hands out exactly num_tiles tickets
+    const size_t tile_base = static_cast<size_t>(tile) * TILE;
+    const size_t warp_base = tile_base + static_cast<size_t>(warp) * WARP_ITEMS;
+    const bool full = tile_base + TILE <= n;
+    const unsigned tile_len = full ? TILE : static_cast<unsigned>(n - tile_base);
+
+    uint32_t x[VECS][4];
+    load_rows<uint32_t, VECS, ALIGNED>(keys, warp_base, n, lane, full, x, 0u);
+
+    // zero masks of `bit` (bit k of zmask[r] set when element k of row r is
+    // inside [0, n) and has the bit clear) and the next bit's zero count
+    uint32_t zmask[VECS], t[VECS];
+    unsigned nz = 0;
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) {
+        const size_t e = warp_base + static_cast<size_t>(r * 32 + lane) * 4;
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const bool valid = full || (e + k < n);
+            if (valid && !((x[r][k] >> bit) & 1u)) m |= 1u << k;
+            if (valid && !((x[r][k] >> next_bit) & 1u)) ++nz;
+        }
+        zmask[r] = m;
+        t[r] = __popc(m);
+    }
+    uint32_t row_excl[VECS], warp_total;
+    warp_scan_rows<AddU32, VECS>(op, t, lane, row_excl, warp_total);
+    if (next_zeros != nullptr) nz = __reduce_add_sync(kFullMask, nz);
+    if (lane == 0) {
+        s_warp[warp] = warp_total;
+        s_next[warp] = nz;
+    }
+    __syncthreads();
+    uint32_t warp_excl, tile_zeros;
+    block_scan_warps<AddU32, NWARPS>(op, s_warp, warp, lane, warp_excl, tile_zeros);
+
+    unsigned tag = 0;
+    if (warp == 0) {
+        tag = __shfl_sync(kFullMask, lane == 0 ? read_tag(st) : 0u, 0);
+        publish<AddU32>(status, tile, tag, tile == 0 ? kFlagInclusive : kFlagAggregate, tile_zeros, lane);
+    }
+    if (next_zeros != nullptr && warp == NWARPS - 1 && lane == 0) {
+        unsigned sum = 0;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w) sum += s_next[w];
+        if (sum != 0) atomicAdd(next_zeros, sum);
+    }
+
+    // stage: zeros at their zero rank, ones after all of the tile's zeros
+#pragma unroll
+    for (int r = 0; r < VECS; ++r) {
+        uint32_t zr = warp_excl + row_excl[r];
+        const uint32_t li0 = static_cast<uint32_t>(warp * WARP_ITEMS + (r * 32 + lane) * 4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t li = li0 + k;
+            if (li < tile_len) {
+                if ((zmask[r] >> k) & 1u) {
+                    s_stage[zr] = x[r][k];
+                    ++zr;
+                } else {
+                    s_stage[tile_zeros + (li - zr)] = x[r][k];
+                }
+            }
+        }
+    }
+
+    if (warp == 0) {
+        uint32_t prefix = 0;
+        if (tile != 0) {
+            prefix = lookback<AddU32>(op, status, tile, tag, &st->error, spin_limit, lane);
+            publish<AddU32>(status, tile, tag, kFlagInclusive, prefix + tile_zeros, lane);
+        }
+        if (lane == 0) s_prefix = prefix;
+        if (tile == num_tiles - 1) finish_launch(st, status, num_tiles, capacity, lane);
+    }
+    __syncthreads();
+
+    const size_t zeros_before = s_prefix;
+    const size_t z_total = *zeros_total;
+    const size_t ones_at = z_total + (tile_base - zeros_before);
+    if (ALIGNED) {
+        write_run_aligned<THREADS, TILE>(out, zeros_before, tile_zeros, s_stage, 0, tid, n);
+        write_run_aligned<THREADS, TILE>(out, ones_at, tile_len - tile_zeros, s_stage,
+                                         static_cast<int>(tile_zeros), tid, n);
+    } else {
+        write_run_scalar<THREADS>(out, zeros_before, tile_zeros, s_stage, 0, tid, n);
+        write_run_scalar<THREADS>(out, ones_at, tile_len - tile_zeros, s_stage, static_cast<int>(tile_zeros),
+                                  tid, n);
+    }
+}
+
+cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned *zeros, const Workspace &ws,
+                               cudaStream_t s)
+{
+    constexpr int THREADS = 256;
+    const size_t want = (n + THREADS * 16 - 1) / (THREADS * 16);
+    const unsigned grid = static_cast<unsigned>(std::max<size_t>(1, std::min<size_t>(want, 4 * ws.num_sms)));
+    if (reinterpret_cast<uintptr_t>(keys) % 16 == 0)
+        count_zeros_kernel<THREADS, true><<<grid, THREADS, 0, s>>>(keys, n, bit, zeros);
+    else
+        count_zeros_kernel<THREADS, false><<<grid, THREADS, 0, s>>>(keys, n, bit, zeros);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split(const uint32_t *keys, uint32_t *out, size_t n, int bit, const unsigned *zeros,
+                         unsigned *next_zeros, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+{
+    constexpr int THREADS = kSplitThreads, VECS = kSplitVecs;
+    const unsigned tiles = tiles_for(n, kSplitTile);
+    const bool aligned = (reinterpret_cast<uintptr_t>(keys) % 16 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+    const int next_bit = (bit < 31) ? bit + 1 : 31;
+    if (aligned)
+        split_kernel<THREADS, VECS, true><<<tiles, THREADS, 0, s>>>(keys, out, n, bit, zeros, next_zeros, next_bit,
+                                                                   tiles, ws.status, ws.state, ws.capacity,
+                                                                   spin_limit);
+    else
+        split_kernel<THREADS, VECS, false><<<tiles, THREADS, 0, s>>>(keys, out, n, bit, zeros, next_zeros, next_bit,
+                                                                    tiles, ws.status, ws.state, ws.capacity,
+                                                                    spin_limit);
+    return cudaGetLastError();
+}
+
+}  // namespace devscan

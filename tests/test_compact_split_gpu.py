@@ -1,0 +1,167 @@
+"""Compaction, one-bit split and radix-sort parity: the CUDA library against
+the CPU oracle, bit-exact, on seeded inputs from tiny and ragged sizes up to
+the full workloads (N = 2^26)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TILE = 4096
+SIZES = [1, 2, 3, 5, 31, 32, 33, 127, 128, 129, 1023, 1024, 1025, TILE - 1, TILE, TILE + 1,
+         3 * TILE + 5, 65_536, 65_537, 300_007]
+
+
+@pytest.fixture(scope="module")
+def ds():
+    import stream_compaction_device_gb300 as m
+    m.load()
+    return m
+
+
+def gpu_compact(ds, v: np.ndarray, f: np.ndarray, voff=0, foff=0, ooff=0):
+    dv = to_dev(np.concatenate([np.zeros(voff, np.int32), v]))[voff:]
+    df = torch.from_numpy(np.concatenate([np.zeros(foff, np.uint8), f])).cuda()[foff:]
+    out = torch.full((v.size + ooff + 8,), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ds.compact(dv, df, out=out[ooff:ooff + max(v.size, 1)], count=cnt)
+    torch.cuda.synchronize()
+    k = int(cnt.item())
+    host = out.cpu().numpy()
+    # nothing written outside the kept range (guard words stay -7)
+    assert np.all(host[:ooff] == -7) and np.all(host[ooff + k:] == -7)
+    return host[ooff:ooff + k]
+
+
+def check_compact(ds, v, f, **kw):
+    got = gpu_compact(ds, v, f, **kw)
+    ref = oracle.compact(v, f)
+    assert got.size == ref.size, f"count {got.size} != {ref.size} (n={v.size})"
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"n={v.size}: first mismatch at {bad[0]}"
+
+
+@pytest.mark.parametrize("pattern", ["random", "none", "all", "alternate", "sparse", "runs"])
+def test_compact_sizes(ds, pattern):
+    rng = np.random.default_rng(21)
+    for n in SIZES:
+        v = rng.integers(-2**31, 2**31, n, dtype=np.int32)
+        if pattern == "random":
+            f = rng.integers(0, 4, n).astype(np.uint8)     # 1, 2, 3 all keep
+        elif pattern == "none":
+            f = np.zeros(n, np.uint8)
+        elif pattern == "all":
+            f = np.full(n, 255, np.uint8)
+        elif pattern == "alternate":
+            f = (np.arange(n) % 2).astype(np.uint8)
+        elif pattern == "sparse":
+            f = (rng.random(n) < 0.001).astype(np.uint8)
+        else:
+            f = ((np.arange(n) // 1000) % 2).astype(np.uint8)
+        check_compact(ds, v, f)
+
+
+@pytest.mark.parametrize("voff,foff,ooff", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (2, 3, 3), (0, 4, 2)])
+def test_compact_unaligned(ds, voff, foff, ooff):
+    rng = np.random.default_rng(voff * 100 + foff * 10 + ooff)
+    for n in (1, 77, TILE + 3, 200_001):
+        v = rng.integers(-2**31, 2**31, n, dtype=np.int32)
+        f = rng.integers(0, 2, n).astype(np.uint8)
+        check_compact(ds, v, f, voff=voff, foff=foff, ooff=ooff)
+
+
+def test_compact_empty(ds):
+    v = torch.empty(0, dtype=torch.int32, device="cuda")
+    f = torch.empty(0, dtype=torch.uint8, device="cuda")
+    cnt = torch.full((1,), 5, dtype=torch.int32, device="cuda")
+    ds.compact(v, f, out=torch.empty(1, dtype=torch.int32, device="cuda"), count=cnt)
+    assert int(cnt.item()) == 0
+
+
+def test_compact_worked_example(ds, golden):
+    g = golden("worked_example.txt")
+    x = np.array(g["x"], dtype=np.int32)
+    flags = (x > g["predicate_threshold"][0]).astype(np.uint8)
+    assert gpu_compact(ds, x, flags).tolist() == g["compacted"]
+
+
+@pytest.mark.parametrize("sel", [0.01, 0.50, 0.99])
+def test_config_compaction(ds, sel):
+    from stream_compaction_device_gb300 import workloads as wl
+    v = wl.compaction_values()
+    f = wl.predicate_flags(v, wl.threshold_for(sel))
+    check_compact(ds, v, f)
+
+
+# ---------------------------------------------------------------------------
+# split and sort
+# ---------------------------------------------------------------------------
+def gpu_split(ds, k: np.ndarray, bit: int, koff=0, ooff=0):
+    dk = to_dev(np.concatenate([np.zeros(koff, np.uint32), k]))[koff:]
+    out = torch.full((k.size + ooff,), 0, dtype=torch.int32, device="cuda")
+    ds.split_bit(dk, bit, out=out[ooff:])
+    torch.cuda.synchronize()
+    return from_dev(out, np.uint32)[ooff:]
+
+
+@pytest.mark.parametrize("bit", [0, 1, 5, 16, 30, 31])
+def test_split_sizes(ds, bit):
+    rng = np.random.default_rng(bit)
+    for n in SIZES:
+        k = rng.integers(0, 2**32, n, dtype=np.uint32)
+        got = gpu_split(ds, k, bit)
+        ref, _ = oracle.split_bit(k, bit)
+        assert np.array_equal(got, ref), f"n={n} bit={bit}"
+
+
+def test_split_skewed(ds):
+    rng = np.random.default_rng(3)
+    for n in (TILE + 1, 100_003):
+        for frac in (0.0, 0.001, 0.999, 1.0):
+            k = rng.integers(0, 2**31, n, dtype=np.uint32)
+            k[rng.random(n) < frac] |= np.uint32(1 << 31)
+            assert np.array_equal(gpu_split(ds, k, 31), oracle.split_bit(k, 31)[0])
+
+
+@pytest.mark.parametrize("koff,ooff", [(1, 0), (0, 1), (3, 2)])
+def test_split_unaligned(ds, koff, ooff):
+    rng = np.random.default_rng(koff + 7 * ooff)
+    for n in (1, 99, TILE + 5, 70_001):
+        k = rng.integers(0, 2**32, n, dtype=np.uint32)
+        assert np.array_equal(gpu_split(ds, k, 9, koff, ooff), oracle.split_bit(k, 9)[0])
+
+
+def gpu_sort(ds, k: np.ndarray):
+    d = to_dev(k)
+    ds.radix_sort(d)
+    torch.cuda.synchronize()
+    return from_dev(d, np.uint32)
+
+
+def test_sort_sizes(ds):
+    rng = np.random.default_rng(5)
+    for n in (1, 2, 3, 100, TILE, TILE + 1, 65_537, 1_000_003):
+        k = rng.integers(0, 2**32, n, dtype=np.uint32)
+        k[: min(n, 6)] = np.array([0, 2**32 - 1, 7, 7, 2**31, 2**31 - 1], dtype=np.uint32)[: min(n, 6)]
+        got = gpu_sort(ds, k)
+        assert np.array_equal(got, oracle.sort_lsd(k)), f"n={n}"
+
+
+def test_config_split_bits(ds):
+    from stream_compaction_device_gb300 import workloads as wl
+    k = wl.radix_keys()
+    for bit in (0, 13, 31):
+        assert np.array_equal(gpu_split(ds, k, bit), oracle.split_bit(k, bit)[0]), bit
+
+
+def test_config_sort(ds):
+    from stream_compaction_device_gb300 import workloads as wl
+    k = wl.radix_keys()
+    got = gpu_sort(ds, k)
+    assert np.array_equal(got, np.sort(k))
+    sample = k[: 1 << 20]
+    assert np.array_equal(gpu_sort(ds, sample), oracle.sort_lsd(sample))
+    assert ds.device_status() == 0
