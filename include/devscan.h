@@ -161,6 +161,38 @@ devscan_status devscan_set_carry_mode(int mode);
  * faults or hangs. */
 devscan_status devscan_selftest_stalled_wait(unsigned int spin_limit, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Allocation-free int32 exclusive scan.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory -- code
+ * whose GPU memory is owned by another allocator (a framework's caching
+ * pool that has reserved the device, where an extra cudaMalloc can fail or
+ * force the pool to give memory back) and code that must not allocate after
+ * start-up (latency-critical or certified paths).  The other entry points
+ * allocate their per-stream workspace on first use; this one never calls
+ * cudaMalloc, cudaMallocAsync, cudaFree or any allocating routine.
+ *
+ * Same semantics and arguments as scan_exclusive_i32 (DEVSCAN_OP_ADD, MAX or
+ * XOR; in == out allowed).  Its scratch -- the tile status words of the
+ * single-pass look-back and a few counters -- is one fixed array compiled
+ * into the library (static device memory, 512 KiB + 256 B on every GPU that
+ * loads the library, held until the process exits):
+ *   - n > DEVSCAN_NOALLOC_MAX_N returns DEVSCAN_ERR_INVALID (nothing runs);
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture;
+ *   - every call shares the one array: calls that may overlap on the GPU
+ *     (different streams without ordering between them) race and give wrong
+ *     results; calls on one stream are safe.  Each call clears the tile
+ *     counter it needs at zero; stale status words of earlier calls are
+ *     ignored through their epoch tag.
+ *   - a device-side wait that runs out (never seen in normal operation) is
+ *     not reported by this entry point.
+ * ------------------------------------------------------------------------- */
+#define DEVSCAN_NOALLOC_MAX_N ((size_t)1 << 28)
+
+devscan_status scan_exclusive_i32_noalloc(const int32_t *in, int32_t *out, size_t n,
+                                          devscan_op op, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

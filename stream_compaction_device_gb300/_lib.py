@@ -62,6 +62,8 @@ def load() -> ctypes.CDLL:
         lib.devscan_set_carry_mode.restype = i
         lib.devscan_selftest_stalled_wait.argtypes = [u, vp]
         lib.devscan_selftest_stalled_wait.restype = i
+        lib.scan_exclusive_i32_noalloc.argtypes = [vp, vp, sz, i, vp]
+        lib.scan_exclusive_i32_noalloc.restype = i
         _lib = lib
         return lib
 
