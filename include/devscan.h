@@ -133,7 +133,8 @@ devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStrea
 
 /* Synchronises `stream`, then reports and clears the device-side error word
  * of the stream's workspace: DEVSCAN_ERR_TIMEOUT if a bounded inter-block
- * wait gave up since the last query (the affected results are not valid),
+ * wait gave up since the last query (the affected results are not valid;
+ * the workspace is reset so that later calls start clean),
  * DEVSCAN_ERR_CUDA if the synchronisation failed, else DEVSCAN_OK. */
 devscan_status devscan_device_status(cudaStream_t stream);
 
@@ -146,10 +147,14 @@ const char *devscan_status_string(devscan_status status);
 devscan_status devscan_stream_release(cudaStream_t stream);
 
 /* Inter-block carry strategy for the scans (P1 section 四 describes the
- * three-phase "reduce, scan the block totals, add the offsets" scheme; a
- * single-pass chained scan with look-back is the alternative):
- *   0 = default (single-pass look-back), 1 = single-pass look-back,
- *   2 = reduce-then-scan (three launches, one extra read of the input).
+ * three-phase "reduce, scan the block totals, add the offsets" scheme and
+ * mentions chaining blocks inside one launch):
+ *   0 = default (3 for 16-byte-aligned in/out, else 1);
+ *   1 = one tile per block, single-pass decoupled look-back;
+ *   2 = reduce-then-scan (three launches, one extra read of the input);
+ *   3 = pipelined single pass: persistent warp-specialised blocks with bulk
+ *       copies and a two-level look-back (16-byte-aligned in/out; others
+ *       use 1).
  * Process-wide; meant for measurement.  Returns DEVSCAN_ERR_INVALID for
  * any other mode. */
 devscan_status devscan_set_carry_mode(int mode);
@@ -174,7 +179,7 @@ devscan_status devscan_selftest_stalled_wait(unsigned int spin_limit, cudaStream
  * Same semantics and arguments as scan_exclusive_i32 (DEVSCAN_OP_ADD, MAX or
  * XOR; in == out allowed).  Its scratch -- the tile status words of the
  * single-pass look-back and a few counters -- is one fixed array compiled
- * into the library (static device memory, 512 KiB + 256 B on every GPU that
+ * into the library (static device memory, 528 KiB + 256 B on every GPU that
  * loads the library, held until the process exits):
  *   - n > DEVSCAN_NOALLOC_MAX_N returns DEVSCAN_ERR_INVALID (nothing runs);
  *   - the first call on each device looks up the array's device address

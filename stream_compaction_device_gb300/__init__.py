@@ -144,8 +144,9 @@ def device_status(stream=None) -> int:
 
 
 def set_carry_mode(mode: str) -> None:
-    """'lookback' (default) or 'rts' (reduce-then-scan), process-wide."""
-    code = {"default": 0, "lookback": 1, "rts": 2}[mode]
+    """'default', 'lookback' (one tile per block), 'rts' (reduce-then-scan)
+    or 'pipelined' (persistent warp-specialised single pass), process-wide."""
+    code = {"default": 0, "lookback": 1, "rts": 2, "pipelined": 3}[mode]
     _lib.check(load().devscan_set_carry_mode(code), "devscan_set_carry_mode")
 
 

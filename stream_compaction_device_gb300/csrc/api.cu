@@ -35,8 +35,9 @@ constexpr size_t kStateBytes = 256;
 
 size_t layout_bytes(unsigned capacity)
 {
-    // state | status[capacity] | never_published[2] | tile_sums[capacity]
-    return kStateBytes + static_cast<size_t>(capacity) * 8 + 16 + static_cast<size_t>(capacity) * 4 + 256;
+    // state | status[capacity] | group status[capacity / 32] | never_published[2] | tile_sums[capacity]
+    return kStateBytes + static_cast<size_t>(capacity) * 8 + static_cast<size_t>(capacity / 32) * 8 + 16 +
+           static_cast<size_t>(capacity) * 4 + 256;
 }
 
 devscan_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DEVSCAN_OK : DEVSCAN_ERR_CUDA; }
@@ -80,7 +81,7 @@ devscan_status acquire(cudaStream_t stream, unsigned tiles, Workspace *out)
         slot.bytes = bytes;
         slot.ws.state = reinterpret_cast<DevState *>(p);
         slot.ws.status = reinterpret_cast<unsigned long long *>(p + kStateBytes);
-        slot.ws.never_published = slot.ws.status + capacity;
+        slot.ws.never_published = slot.ws.status + capacity + capacity / 32;
         slot.ws.tile_sums = reinterpret_cast<uint32_t *>(slot.ws.never_published + 2);
         slot.ws.capacity = capacity;
     }
@@ -221,16 +222,22 @@ devscan_status devscan_device_status(cudaStream_t stream)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DEVSCAN_ERR_CUDA;
     DevState *state = nullptr;
+    void *base = nullptr;
+    size_t bytes = 0;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         auto it = g_slots.find({dev, reinterpret_cast<uintptr_t>(stream)});
         if (it == g_slots.end()) return DEVSCAN_OK;
         state = it->second.ws.state;
+        base = it->second.base;
+        bytes = it->second.bytes;
     }
     unsigned err = 0;
     if (cudaMemcpy(&err, &state->error, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
         return DEVSCAN_ERR_CUDA;
-    if (err != 0 && cudaMemset(&state->error, 0, sizeof(unsigned)) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    // A launch that gave up may have left its tile counter, epoch and status
+    // words half-way; the stream is idle now, so start the workspace afresh.
+    if (err != 0 && cudaMemset(base, 0, bytes) != cudaSuccess) return DEVSCAN_ERR_CUDA;
     return (err & kErrTimeout) ? DEVSCAN_ERR_TIMEOUT : DEVSCAN_OK;
 }
 
@@ -261,7 +268,8 @@ devscan_status devscan_stream_release(cudaStream_t stream)
 
 devscan_status devscan_set_carry_mode(int mode)
 {
-    if (mode != kCarryDefault && mode != kCarryLookback && mode != kCarryReduceThenScan) return DEVSCAN_ERR_INVALID;
+    if (mode != kCarryDefault && mode != kCarryLookback && mode != kCarryReduceThenScan && mode != kCarryPipelined)
+        return DEVSCAN_ERR_INVALID;
     g_carry_mode.store(mode, std::memory_order_relaxed);
     return DEVSCAN_OK;
 }

@@ -102,7 +102,7 @@ compact_kernel(const uint32_t *__restrict__ in, const uint8_t *__restrict__ flag
     if (warp == 0) {
         uint32_t prefix = 0;
         if (tile != 0) {
-            prefix = lookback<AddU32>(op, status, tile, tag, &st->error, spin_limit, lane);
+            prefix = lookback<AddU32, kLookbackPerLane>(op, status, tile, tag, &st->error, spin_limit, lane);
             publish<AddU32>(status, tile, tag, kFlagInclusive, prefix + tile_total, lane);
         }
         if (lane == 0) {

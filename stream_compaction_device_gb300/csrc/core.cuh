@@ -96,6 +96,7 @@ struct DevState {
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kEpochTags = (1u << 30) - 1u;   // tags 1 .. 2^30 - 1
 constexpr unsigned kRefreshPerLaunch = 256;
+constexpr int kLookbackPerLane = 1;   // status words per lane per look-back round trip
 
 // Status word: high 32 bits = (epoch tag << 2) | flag, low 32 bits = value.
 constexpr unsigned kFlagInvalid = 0, kFlagAggregate = 1, kFlagInclusive = 2;
@@ -244,11 +245,11 @@ __device__ __forceinline__ void block_scan_warps(const Op &op, const typename Op
 //
 // publish_aggregate: the tile's own total, flagged "aggregate" (tile 0
 // publishes its total as "inclusive" straight away).
-// lookback: lane j reads the status of tile (base - j).  The warp waits
-// until every tile from `base` down to the nearest "inclusive" one has
-// published something, folds those values (aggregates plus the inclusive
-// prefix), and either stops (an inclusive prefix was found) or moves the
-// window 32 tiles further back.  Positions before tile 0 read as an
+// lookback: the warp reads a window of predecessor status words.  It waits
+// until every tile from the nearest predecessor down to the nearest
+// "inclusive" one has published something, folds those values (aggregates
+// plus the inclusive prefix), and either stops (an inclusive prefix was
+// found) or moves the window further back.  Positions before tile 0 read as an
 // inclusive identity.  Each wait is bounded by `spin_limit` polls; when it
 // runs out the error word gets kErrTimeout and the result is not valid.
 // ---------------------------------------------------------------------------
@@ -259,35 +260,53 @@ __device__ __forceinline__ void publish(unsigned long long *status, unsigned til
     if (lane == 0) st_status(status + tile, pack_status(tag, flag, to_bits(value)));
 }
 
-template <class Op>
+// Look-back window: lane j reads the PER_LANE status words of tiles
+// (end - 1 - PER_LANE * j - k), k = 0 .. PER_LANE - 1, so one round trip to
+// L2 covers 32 * PER_LANE predecessors.  The rate at which tiles can finish
+// is about (window size) / (L2 round-trip latency), so a wide window keeps
+// the inter-block carry off the critical path.
+template <class Op, int PER_LANE>
 __device__ typename Op::S lookback(const Op &op, const unsigned long long *status, unsigned tile,
                                    unsigned tag, unsigned *error, unsigned spin_limit, int lane)
 {
     using S = typename Op::S;
     S excl = Op::identity();
-    long long base = static_cast<long long>(tile) - 1;
+    long long end = static_cast<long long>(tile);
     bool gave_up = false;
     while (!gave_up) {
-        const long long idx = base - lane;
-        unsigned flag;
-        uint32_t bits;
-        unsigned found, upto;
+        unsigned flag[PER_LANE];
+        uint32_t bits[PER_LANE];
+        unsigned found;
+        int upto;   // this lane's entries 0 .. upto contribute
         unsigned spins = 0;
         while (true) {
-            if (idx >= 0) {
-                const unsigned long long w = ld_status(status + idx);
-                const unsigned hi = static_cast<unsigned>(w >> 32);
-                flag = ((hi >> 2) == tag) ? (hi & 3u) : kFlagInvalid;
-                bits = static_cast<uint32_t>(w);
-            } else {
-                flag = kFlagInclusive;
-                bits = to_bits(Op::identity());
+            unsigned long long w[PER_LANE];
+#pragma unroll
+            for (int k = 0; k < PER_LANE; ++k) {
+                const long long idx = end - 1 - static_cast<long long>(PER_LANE) * lane - k;
+                w[k] = (idx >= 0) ? ld_status(status + idx) : 0ull;
             }
-            found = __ballot_sync(kFullMask, flag == kFlagInclusive);
-            const unsigned missing = __ballot_sync(kFullMask, flag == kFlagInvalid);
-            // lanes 0 .. (nearest inclusive lane); all 32 lanes if none
-            upto = found ? (((found & (0u - found)) << 1) - 1u) : kFullMask;
-            if ((missing & upto) == 0) break;
+            int kp = PER_LANE;   // this lane's nearest inclusive entry
+#pragma unroll
+            for (int k = PER_LANE - 1; k >= 0; --k) {
+                const long long idx = end - 1 - static_cast<long long>(PER_LANE) * lane - k;
+                if (idx >= 0) {
+                    const unsigned hi = static_cast<unsigned>(w[k] >> 32);
+                    flag[k] = ((hi >> 2) == tag) ? (hi & 3u) : kFlagInvalid;
+                    bits[k] = static_cast<uint32_t>(w[k]);
+                } else {
+                    flag[k] = kFlagInclusive;
+                    bits[k] = to_bits(Op::identity());
+                }
+                if (flag[k] == kFlagInclusive) kp = k;
+            }
+            found = __ballot_sync(kFullMask, kp < PER_LANE);
+            const int jp = found ? __ffs(found) - 1 : 32;   // nearest lane holding an inclusive prefix
+            upto = (lane < jp) ? PER_LANE - 1 : ((lane == jp) ? kp : -1);
+            bool miss = false;
+#pragma unroll
+            for (int k = 0; k < PER_LANE; ++k) miss |= (k <= upto) && (flag[k] == kFlagInvalid);
+            if (__ballot_sync(kFullMask, miss) == 0) break;
             if (++spins >= spin_limit) {
                 if (lane == 0) atomicOr(error, kErrTimeout);
                 gave_up = true;
@@ -295,14 +314,120 @@ __device__ typename Op::S lookback(const Op &op, const unsigned long long *statu
             }
             if (spins > 4) __nanosleep(spins < 64 ? 32 : 256);
         }
-        S v = (((upto >> lane) & 1u) && flag != kFlagInvalid) ? from_bits<S>(bits) : Op::identity();
+        S v = Op::identity();
+#pragma unroll
+        for (int k = 0; k < PER_LANE; ++k)
+            if (k <= upto && flag[k] != kFlagInvalid) v = op(from_bits<S>(bits[k]), v);
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
         excl = op(v, excl);
         if (found) break;
-        base -= 32;
+        end -= 32LL * PER_LANE;
     }
     return excl;
+}
+
+// ---------------------------------------------------------------------------
+// Two-level look-back.  Tiles form groups of 32.  Besides its own status
+// word, the last tile of each group publishes a group status word: first
+// the group's aggregate (the fold of its 32 tile aggregates, all of which
+// its own level-1 window has seen), then the group's inclusive prefix.  A
+// tile's look-back reads (1) the status words of its own group's earlier
+// tiles -- at most 31, one round trip -- and, unless it met an inclusive
+// prefix there, (2) the group status words of earlier groups, 32 groups
+// (1,024 tiles) per round trip.  The inclusive frontier thus advances 1,024
+// tiles per L2 round trip instead of 32.  Waits are bounded as above.
+// Returns the tile's exclusive prefix; the caller publishes the tile's own
+// status words, this function the group word.
+// ---------------------------------------------------------------------------
+template <class Op>
+__device__ typename Op::S lookback2(const Op &op, const unsigned long long *status,
+                                    unsigned long long *status2, unsigned tile, unsigned tag,
+                                    typename Op::S agg, unsigned *error, unsigned spin_limit, int lane)
+{
+    using S = typename Op::S;
+    const unsigned group = tile >> 5;
+    const long long first = static_cast<long long>(group) << 5;
+    const bool closes_group = (tile & 31u) == 31u;
+    bool gave_up = false;
+
+    // level 1: this group's tiles first .. tile-1, lane j reading tile-1-j
+    const long long idx = static_cast<long long>(tile) - 1 - lane;
+    const bool mine = idx >= first;
+    unsigned flag = kFlagInclusive, found, upto;
+    uint32_t bits = to_bits(Op::identity());
+    unsigned spins = 0;
+    while (true) {
+        if (mine) {
+            const unsigned long long w = ld_status(status + idx);
+            const unsigned hi = static_cast<unsigned>(w >> 32);
+            flag = ((hi >> 2) == tag) ? (hi & 3u) : kFlagInvalid;
+            bits = static_cast<uint32_t>(w);
+        }
+        found = __ballot_sync(kFullMask, mine && flag == kFlagInclusive);
+        const unsigned in_group = __ballot_sync(kFullMask, mine);
+        upto = found ? (((found & (0u - found)) << 1) - 1u) : in_group;
+        const unsigned missing = __ballot_sync(kFullMask, mine && flag == kFlagInvalid);
+        if ((missing & upto) == 0) break;
+        if (++spins >= spin_limit) {
+            if (lane == 0) atomicOr(error, kErrTimeout);
+            gave_up = true;
+            break;
+        }
+        if (spins > 4) __nanosleep(spins < 64 ? 32 : 256);
+    }
+    S v = (((upto >> lane) & 1u) && mine && flag != kFlagInvalid) ? from_bits<S>(bits) : Op::identity();
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
+    const S level1 = v;   // fold of own-group predecessors back to an inclusive prefix, or all of them
+    if (found || gave_up) {
+        if (closes_group && lane == 0)
+            st_status(status2 + group, pack_status(tag, kFlagInclusive, to_bits(op(level1, agg))));
+        return level1;
+    }
+    if (closes_group && lane == 0)
+        st_status(status2 + group, pack_status(tag, kFlagAggregate, to_bits(op(level1, agg))));
+
+    // level 2: earlier groups, lane j reading group (end - 1 - j)
+    S excl = Op::identity();
+    long long end = static_cast<long long>(group);
+    while (!gave_up) {
+        const long long g = end - 1 - lane;
+        unsigned gflag, gfound, gupto;
+        uint32_t gbits;
+        spins = 0;
+        while (true) {
+            if (g >= 0) {
+                const unsigned long long w = ld_status(status2 + g);
+                const unsigned hi = static_cast<unsigned>(w >> 32);
+                gflag = ((hi >> 2) == tag) ? (hi & 3u) : kFlagInvalid;
+                gbits = static_cast<uint32_t>(w);
+            } else {
+                gflag = kFlagInclusive;
+                gbits = to_bits(Op::identity());
+            }
+            gfound = __ballot_sync(kFullMask, gflag == kFlagInclusive);
+            gupto = gfound ? (((gfound & (0u - gfound)) << 1) - 1u) : kFullMask;
+            const unsigned missing = __ballot_sync(kFullMask, gflag == kFlagInvalid);
+            if ((missing & gupto) == 0) break;
+            if (++spins >= spin_limit) {
+                if (lane == 0) atomicOr(error, kErrTimeout);
+                gave_up = true;
+                break;
+            }
+            if (spins > 4) __nanosleep(spins < 64 ? 32 : 256);
+        }
+        S gv = (((gupto >> lane) & 1u) && gflag != kFlagInvalid) ? from_bits<S>(gbits) : Op::identity();
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) gv = op(gv, __shfl_xor_sync(kFullMask, gv, d));
+        excl = op(gv, excl);
+        if (gfound) break;
+        end -= 32;
+    }
+    const S prefix = op(excl, level1);
+    if (closes_group && lane == 0)
+        st_status(status2 + group, pack_status(tag, kFlagInclusive, to_bits(op(prefix, agg))));
+    return prefix;
 }
 
 // Run by lane 0 .. 31 of warp 0 of the block that owns the launch's last
@@ -320,6 +445,14 @@ __device__ __forceinline__ void finish_launch(DevState *st, unsigned long long *
         for (unsigned i = lane; i < kRefreshPerLaunch; i += 32)
             status[num_tiles + (cursor + i) % spare] = 0ull;
     }
+    // group status words follow the tile status words (see group_status())
+    unsigned long long *status2 = status + capacity;
+    const unsigned groups = (num_tiles + 31u) >> 5, capacity2 = capacity >> 5;
+    if (capacity2 > groups) {
+        const unsigned spare = capacity2 - groups;
+        for (unsigned i = lane; i < kRefreshPerLaunch; i += 32)
+            status2[groups + (cursor + i) % spare] = 0ull;
+    }
     __syncwarp();
     if (lane == 0) {
         st->cursor = cursor + kRefreshPerLaunch;
@@ -327,6 +460,13 @@ __device__ __forceinline__ void finish_launch(DevState *st, unsigned long long *
         const unsigned e = st->epoch + 1u;
         st->epoch = (e >= kEpochTags) ? 0u : e;
     }
+}
+
+// The group status words (capacity / 32 of them) sit right after the
+// `capacity` tile status words in every workspace.
+__device__ __forceinline__ unsigned long long *group_status(unsigned long long *status, unsigned capacity)
+{
+    return status + capacity;
 }
 
 __device__ __forceinline__ unsigned read_tag(const DevState *st)

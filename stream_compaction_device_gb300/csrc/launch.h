@@ -29,13 +29,15 @@ constexpr int kMaxTile = 4096;   // largest of the three (workspace sizing)
 constexpr bool kUseTickets = true;
 
 constexpr int kOpAdd = 0, kOpMax = 1, kOpXor = 2;
-constexpr int kCarryDefault = 0, kCarryLookback = 1, kCarryReduceThenScan = 2;
+constexpr int kCarryDefault = 0, kCarryLookback = 1, kCarryReduceThenScan = 2, kCarryPipelined = 3;
 
 enum class ElemType { I32, U32, F32 };
 
 // Per-(device, stream) scratch, carved from one allocation:
 //   state           DevState (epoch, ticket, error word, zero counts)
-//   status          `capacity` 8-byte tile status words
+//   status          `capacity` 8-byte tile status words, followed by
+//                   capacity / 32 group status words (capacity is a power of
+//                   two, at least 1024)
 //   never_published 2 words kept at zero (bounded-wait self-test)
 //   tile_sums       `capacity` 4-byte tile totals (reduce-then-scan)
 struct Workspace {

@@ -20,12 +20,15 @@ namespace devscan {
 // Room for DEVSCAN_NOALLOC_MAX_N elements: 65,536 tiles of 4,096.
 constexpr unsigned kNoAllocTiles = static_cast<unsigned>(DEVSCAN_NOALLOC_MAX_N / kScanTile);
 constexpr size_t kNoAllocStateBytes = 256;
-constexpr size_t kNoAllocBytes = kNoAllocStateBytes + static_cast<size_t>(kNoAllocTiles) * 8;
+// tile status words, then one group status word per 32 tiles
+constexpr size_t kNoAllocBytes =
+    kNoAllocStateBytes + static_cast<size_t>(kNoAllocTiles) * 8 + static_cast<size_t>(kNoAllocTiles / 32) * 8;
 static_assert(DEVSCAN_NOALLOC_MAX_N % kScanTile == 0, "whole tiles");
+static_assert(kNoAllocTiles % 32 == 0, "whole groups of tiles");
 static_assert(sizeof(DevState) <= kNoAllocStateBytes, "state block fits");
 
 // The scratch: zero at module load (zero status words read as "not ready";
-// epoch 0 is tag 1).  512 KiB + 256 B per device, held until exit.
+// epoch 0 is tag 1).  528 KiB + 256 B per device, held until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 namespace {

@@ -1,15 +1,24 @@
 // Device-wide inclusive / exclusive scan kernels (sm_103a).
 //
-// Two inter-block carry strategies (geek-doc.cn "并行前缀和 scan ..." section
-// 四 describes the first and mentions the second):
-//   * single pass with decoupled look-back: one launch, each element read
-//     once and written once (2 * n * sizeof(T) bytes);
+// Inter-block carry strategies (geek-doc.cn "并行前缀和 scan ..." section 四
+// describes the three-phase one and mentions chaining blocks in one launch):
+//   * pipelined single pass (default for 16-byte-aligned data): persistent
+//     warp-specialised blocks; bulk copies, tile aggregates published as
+//     soon as a tile lands, two-level decoupled look-back, and L2 holding
+//     each tile while its prefix resolves (scan_l2.cuh); one launch, HBM
+//     traffic about 2 * n * sizeof(T) bytes;
+//   * one tile per block with decoupled look-back (any 4-byte alignment):
+//     one launch, 2 * n * sizeof(T) bytes, but each block holds its tile in
+//     registers for the whole look-back;
 //   * reduce-then-scan: tile totals, one-block scan of the totals, then the
 //     tile scan with its offset -- three launches and one extra read of the
 //     input (3 * n * sizeof(T) bytes).
 #include "core.cuh"
 #include "launch.h"
 #include "scan_kernel.cuh"
+#include "scan_l2.cuh"
+
+#include <atomic>
 
 namespace devscan {
 
@@ -147,7 +156,7 @@ __global__ void stalled_wait_kernel(const unsigned long long *never_published, D
 {
     const AddU32 op;
     const unsigned tag = read_tag(st);
-    (void)lookback<AddU32>(op, never_published, 1u, tag, &st->error, spin_limit, threadIdx.x & 31);
+    (void)lookback<AddU32, kLookbackPerLane>(op, never_published, 1u, tag, &st->error, spin_limit, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------------------
@@ -165,6 +174,37 @@ cudaError_t launch_lookback(const void *in, void *out, size_t n, const Workspace
     scan_lookback_kernel<Op, THREADS, VECS, INCLUSIVE, ALIGNED, kUseTickets><<<tiles, THREADS, 0, s>>>(
         static_cast<const S *>(in), static_cast<S *>(out), n, tiles, ws.status, ws.state, ws.capacity,
         spin_limit);
+    return cudaGetLastError();
+}
+
+// Geometry of the pipelined kernel: 16 scan warps x 4 rows (8,192-element
+// tiles), 2 reduce warps, 3 A buffers, 4 B buffers, 12 in-flight records
+// (1,024 threads, 224 KiB of shared memory: one block per SM).
+using PipeG = L2Geom<16, 2, 4, 3, 4, 12>;
+constexpr unsigned kWaitLimit = 1u << 18;   // bounded mbarrier polls (~1 us each at most)
+
+template <class Op, bool INCLUSIVE>
+cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,
+                             cudaStream_t s)
+{
+    using S = typename Op::S;
+    auto kernel = scan_l2_kernel<Op, INCLUSIVE, 16, 2, 4, 3, 4, 12>;
+    static std::atomic<unsigned long long> attribute_set{0};   // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if ((attribute_set.load() & bit) == 0) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(PipeG::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attribute_set.fetch_or(bit);
+    }
+    const unsigned tiles = tiles_for(n, PipeG::kTile);
+    const unsigned grid = tiles < static_cast<unsigned>(ws.num_sms) ? tiles : static_cast<unsigned>(ws.num_sms);
+    kernel<<<grid, PipeG::kThreads, PipeG::kSmemBytes, s>>>(static_cast<const S *>(in), static_cast<S *>(out), n,
+                                                           tiles, ws.status, ws.state, ws.capacity, spin_limit,
+                                                           kWaitLimit);
     return cudaGetLastError();
 }
 
@@ -187,6 +227,7 @@ cudaError_t dispatch_op(const void *in, void *out, size_t n, bool aligned, int c
                         unsigned spin_limit, cudaStream_t s)
 {
     if (carry == kCarryReduceThenScan && aligned) return launch_rts<Op, INCLUSIVE>(in, out, n, ws, s);
+    if (aligned && carry != kCarryLookback) return launch_pipelined<Op, INCLUSIVE>(in, out, n, ws, spin_limit, s);
     if (aligned) return launch_lookback<Op, INCLUSIVE, true>(in, out, n, ws, spin_limit, s);
     return launch_lookback<Op, INCLUSIVE, false>(in, out, n, ws, spin_limit, s);
 }

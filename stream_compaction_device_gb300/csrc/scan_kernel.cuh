@@ -9,8 +9,11 @@ namespace devscan {
 // ---------------------------------------------------------------------------
 // Single-pass scan: one tile per block.
 // ---------------------------------------------------------------------------
-template <class Op, int THREADS, int VECS, bool INCLUSIVE, bool ALIGNED, bool TICKETS>
-__global__ void __launch_bounds__(THREADS)
+// LB: status words per lane of a look-back round trip; MINB: resident blocks
+// per SM the register allocation must allow.
+template <class Op, int THREADS, int VECS, bool INCLUSIVE, bool ALIGNED, bool TICKETS,
+          int LB = kLookbackPerLane, int MINB = 1, bool TWO_LEVEL = false>
+__global__ void __launch_bounds__(THREADS, MINB)
 scan_lookback_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,
                      unsigned num_tiles, unsigned long long *status, DevState *st, unsigned capacity,
                      unsigned spin_limit)
@@ -61,7 +64,11 @@ scan_lookback_kernel(const typename Op::S *__restrict__ in, typename Op::S *__re
             publish<Op>(status, tile, tag, kFlagInclusive, tile_total, lane);
         } else {
             publish<Op>(status, tile, tag, kFlagAggregate, tile_total, lane);
-            prefix = lookback<Op>(op, status, tile, tag, &st->error, spin_limit, lane);
+            if (TWO_LEVEL)
+                prefix = lookback2<Op>(op, status, group_status(status, capacity), tile, tag, tile_total,
+                                       &st->error, spin_limit, lane);
+            else
+                prefix = lookback<Op, LB>(op, status, tile, tag, &st->error, spin_limit, lane);
             publish<Op>(status, tile, tag, kFlagInclusive, op(prefix, tile_total), lane);
         }
         if (lane == 0) s_prefix = prefix;

@@ -142,7 +142,7 @@ split_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size
     if (warp == 0) {
         uint32_t prefix = 0;
         if (tile != 0) {
-            prefix = lookback<AddU32>(op, status, tile, tag, &st->error, spin_limit, lane);
+            prefix = lookback<AddU32, kLookbackPerLane>(op, status, tile, tag, &st->error, spin_limit, lane);
             publish<AddU32>(status, tile, tag, kFlagInclusive, prefix + tile_zeros, lane);
         }
         if (lane == 0) s_prefix = prefix;

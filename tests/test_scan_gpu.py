@@ -94,29 +94,35 @@ def test_int32_wraps(ds):
     check(ds, x, "add", False)
 
 
-def test_reduce_then_scan_carry(ds):
-    """The three-launch carry path gives the same results."""
+@pytest.mark.parametrize("mode", ["lookback", "rts", "pipelined"])
+def test_carry_modes(ds, mode):
+    """Every inter-block carry path gives the oracle's results."""
     from stream_compaction_device_gb300 import workloads as wl
-    ds.set_carry_mode("rts")
+    ds.set_carry_mode(mode)
     try:
         for dtype, op in CASES:
-            for n in (1, TILE, 3 * TILE + 5, 1_000_003):
+            for n in (1, 5, TILE, 2 * TILE + 1, 8192 * 3 + 7, 1_000_003):
                 for inclusive in (True, False):
                     check(ds, wl.random_input(dtype, n, n + 1, op), op, inclusive)
     finally:
         ds.set_carry_mode("default")
 
 
-def test_repeated_runs_identical(ds):
+@pytest.mark.parametrize("mode", ["default", "lookback"])
+def test_repeated_runs_identical(ds, mode):
     """Integer results do not depend on block timing: 50 launches, one answer."""
     from stream_compaction_device_gb300 import workloads as wl
     x = wl.random_input(np.int32, (1 << 22) + 3, 11, "add")
     d = to_dev(x)
-    ref = oracle.scan(x, "add", False)
+    ref = torch.from_numpy(oracle.scan(x, "add", False)).cuda()
     out = torch.empty_like(d)
-    for _ in range(50):
-        ds.scan_exclusive(d, out)
-        assert torch.equal(out, torch.from_numpy(ref).cuda())
+    ds.set_carry_mode(mode)
+    try:
+        for _ in range(50):
+            ds.scan_exclusive(d, out)
+            assert torch.equal(out, ref)
+    finally:
+        ds.set_carry_mode("default")
     assert ds.device_status() == 0
 
 
