@@ -43,10 +43,10 @@ METRIC = "int32 exclusive scan Gelem/s & HBM GB/s (% peak) at N=2^28; compaction
 N_HEADLINE = 1 << 28
 REF_SAMPLE = 1 << 22
 FALLBACK_HBM_GBS = 6800.0
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the scan kernel at
-# N = 2^28, from the ncu capture summarised in profiles/; None until taken for
-# the current kernel.
-SCAN_TRAFFIC_BYTES = None
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the pipelined
+# scan kernel at N = 2^28 (one-pass ncu capture of this benchmark's own
+# command); set to None whenever the kernel changes until it is re-captured.
+SCAN_TRAFFIC_BYTES = 2.18e9
 
 
 def peak_hbm():
@@ -286,13 +286,13 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": f"int32 exclusive add-scan, N=2^{n.bit_length() - 1}, +1/-1 bracket "
                                    "sequence (p=0.5, seed 3)", "n": n, "op": "add", "inclusive": False,
-                       "carry": args.carry, "tile_elems": 4096,
+                       "carry": args.carry, "tile_elems": 8192,
                        "l2": "input and output 1 GiB each (> 126 MB L2); no flush between steps",
                        "replicas": world},
             "hbm_gbs": round(achieved, 1), "pct_peak": round(100 * achieved / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": SCAN_TRAFFIC_BYTES,
-                         "kernel": "scan_lookback_kernel<AddU32,256,4,exclusive>",
+                         "kernel": "scan_l2_kernel<AddU32,exclusive,16,2,4,3,4,12>",
                          "algorithmic_bytes_per_launch": alg_bytes, "peak_kind": peak_kind},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
             "clocks": clock_info, "parity_sampled": parity_ok, "extra": extra,

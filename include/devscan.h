@@ -149,7 +149,7 @@ devscan_status devscan_stream_release(cudaStream_t stream);
 /* Inter-block carry strategy for the scans (P1 section 四 describes the
  * three-phase "reduce, scan the block totals, add the offsets" scheme and
  * mentions chaining blocks inside one launch):
- *   0 = default (3 for 16-byte-aligned in/out, else 1);
+ *   0 = default (3 for 16-byte-aligned in/out and n >= 2^19, else 1);
  *   1 = one tile per block, single-pass decoupled look-back;
  *   2 = reduce-then-scan (three launches, one extra read of the input);
  *   3 = pipelined single pass: persistent warp-specialised blocks with bulk

@@ -182,6 +182,7 @@ cudaError_t launch_lookback(const void *in, void *out, size_t n, const Workspace
 // (1,024 threads, 224 KiB of shared memory: one block per SM).
 using PipeG = L2Geom<16, 2, 4, 3, 4, 12>;
 constexpr unsigned kWaitLimit = 1u << 18;   // bounded mbarrier polls (~1 us each at most)
+constexpr size_t kPipelineMinN = size_t(1) << 19;
 
 template <class Op, bool INCLUSIVE>
 cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,
@@ -227,7 +228,10 @@ cudaError_t dispatch_op(const void *in, void *out, size_t n, bool aligned, int c
                         unsigned spin_limit, cudaStream_t s)
 {
     if (carry == kCarryReduceThenScan && aligned) return launch_rts<Op, INCLUSIVE>(in, out, n, ws, s);
-    if (aligned && carry != kCarryLookback) return launch_pipelined<Op, INCLUSIVE>(in, out, n, ws, spin_limit, s);
+    // below ~2^19 elements the pipeline's fill latency outweighs its
+    // bandwidth: one tile per block is faster there (measured on GB300)
+    const bool pipelined = aligned && (carry == kCarryPipelined || (carry == kCarryDefault && n >= kPipelineMinN));
+    if (pipelined) return launch_pipelined<Op, INCLUSIVE>(in, out, n, ws, spin_limit, s);
     if (aligned) return launch_lookback<Op, INCLUSIVE, true>(in, out, n, ws, spin_limit, s);
     return launch_lookback<Op, INCLUSIVE, false>(in, out, n, ws, spin_limit, s);
 }
