@@ -155,8 +155,10 @@ devscan_status devscan_stream_release(cudaStream_t stream);
  *   3 = pipelined single pass: persistent warp-specialised blocks with bulk
  *       copies and a two-level look-back (16-byte-aligned in/out; others
  *       use 1).
- * Process-wide; meant for measurement.  Returns DEVSCAN_ERR_INVALID for
- * any other mode. */
+ * Compaction and the split follow the same choice between 1 and 3 (their
+ * pipelined kernels need 16-byte-aligned inputs, and flags too for
+ * compaction).  Process-wide; meant for measurement.  Returns
+ * DEVSCAN_ERR_INVALID for any other mode. */
 devscan_status devscan_set_carry_mode(int mode);
 
 /* Self-test of the bounded inter-block wait: launches two blocks on

@@ -168,7 +168,8 @@ devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out
     Workspace ws;
     const devscan_status st = acquire(stream, tiles, &ws);
     if (st != DEVSCAN_OK) return st;
-    return from_cuda(launch_compact(in, flags, out, count, n, ws, kSpinLimit, stream));
+    return from_cuda(launch_compact(in, flags, out, count, n, g_carry_mode.load(std::memory_order_relaxed), ws,
+                                    kSpinLimit, stream));
 }
 
 devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_t n, cudaStream_t stream)
@@ -188,7 +189,8 @@ devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_
     if (cudaMemsetAsync(z, 0, sizeof(unsigned), stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
     cudaError_t e = launch_count_zeros(keys, n, bit, z, ws, stream);
     if (e != cudaSuccess) return DEVSCAN_ERR_CUDA;
-    return from_cuda(launch_split(keys, out, n, bit, z, nullptr, ws, kSpinLimit, stream));
+    return from_cuda(launch_split(keys, out, n, bit, z, nullptr, g_carry_mode.load(std::memory_order_relaxed), ws,
+                                  kSpinLimit, stream));
 }
 
 devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStream_t stream)
@@ -206,10 +208,11 @@ devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStrea
     unsigned *z = ws.state->zeros;   // z[b] = zero count of bit b
     if (cudaMemsetAsync(z, 0, 33 * sizeof(unsigned), stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
     if (launch_count_zeros(keys, n, 0, &z[0], ws, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    const int carry = g_carry_mode.load(std::memory_order_relaxed);
     uint32_t *src = keys, *dst = tmp;
     for (int bit = 0; bit < 32; ++bit) {
         unsigned *next = (bit < 31) ? &z[bit + 1] : nullptr;
-        if (launch_split(src, dst, n, bit, &z[bit], next, ws, kSpinLimit, stream) != cudaSuccess)
+        if (launch_split(src, dst, n, bit, &z[bit], next, carry, ws, kSpinLimit, stream) != cudaSuccess)
             return DEVSCAN_ERR_CUDA;
         std::swap(src, dst);
     }

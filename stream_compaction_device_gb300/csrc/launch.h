@@ -59,8 +59,10 @@ cudaError_t launch_scan(ElemType type, int op, bool inclusive, const void *in, v
 
 cudaError_t launch_stalled_wait(const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
+// `carry` (kCarry*): the pipelined kernel for kCarryPipelined, the one-tile
+// kernel for kCarryLookback, the measured size threshold otherwise.
 cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out, int32_t *count, size_t n,
-                           const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+                           int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
 // Zero count of bit `bit` over keys[0, n) added into *zeros (which the caller
 // has cleared).
@@ -71,6 +73,6 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
 // next_zeros is not null, the pass also adds the zero count of bit
 // `bit + 1` into *next_zeros.
 cudaError_t launch_split(const uint32_t *keys, uint32_t *out, size_t n, int bit, const unsigned *zeros,
-                         unsigned *next_zeros, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+                         unsigned *next_zeros, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
 }  // namespace devscan

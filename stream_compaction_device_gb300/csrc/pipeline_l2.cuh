@@ -1,0 +1,507 @@
+// Persistent two-pass pipeline for sm_103a in which L2 holds each tile while
+// its prefix is resolved.  One kernel template serves the scan, stream
+// compaction and the one-bit split; a policy class P says what each pass
+// loads and computes.
+//
+// Per tile t, in one block:
+//   pass A     the A-producer warp takes tile tickets in order and
+//              bulk-copies P's pass-A bytes of the tile into an A buffer
+//              (L2 policy evict_last: pass B reads them again); the reduce
+//              group folds them to the tile's aggregate (P::reduce), frees the
+//              buffer, publishes the aggregate and only then claims one of R
+//              in-flight tile records;
+//   look-back  one warp per record runs the two-level decoupled look-back
+//              (tile words plus group-of-32 words) for the tile's exclusive
+//              prefix;
+//   pass B     the B-producer warp, in record order, bulk-copies P's pass-B
+//              bytes into a B buffer once the prefix is known (the bytes pass
+//              A read are L2 hits); the consume group applies the prefix and
+//              writes the output (P::consume).
+// No block holds a tile's data while the look-back runs, so shared memory
+// only has to cover load latency.  Every wait is bounded (the error word
+// records a timeout); decisions after a group-wide wait are made uniform with
+// a reducing barrier; both producers drain their bulk copies before the block
+// exits.  The block that takes the launch's last ticket closes the launch
+// (advances the epoch, resets the ticket counter).
+#pragma once
+
+#include "core.cuh"
+#include "pipeline.cuh"
+
+namespace devscan {
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void bulk_load_hint(void *dst_smem, const void *src_global, unsigned bytes, uint64_t *bar,
+                                               uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst_smem)),
+        "l"(src_global), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Named barrier ids of the pipeline (0 is __syncthreads).
+constexpr unsigned kBarReduceDecide = 4, kBarReduceTotals = 5, kBarConsumeDecide = 6, kBarConsumeTotals = 7;
+
+// Block-wide exclusive scan of the consume group's warp totals.  Every warp
+// writes its total into buf[warp], the group meets at a named barrier, then
+// each warp scans the NW totals.  Callers alternate between two buffers so a
+// single barrier per call suffices.
+template <class Op, int NW>
+__device__ __forceinline__ void group_scan(const Op &op, typename Op::S warp_total, uint32_t *buf, int warp,
+                                           int lane, typename Op::S &warp_excl, typename Op::S &group_total)
+{
+    using S = typename Op::S;
+    if (lane == 0) buf[warp] = to_bits(warp_total);
+    named_sync(kBarConsumeTotals, NW * 32);
+    S v = (lane < NW) ? from_bits<S>(buf[lane]) : Op::identity();
+#pragma unroll
+    for (int d = 1; d < NW; d <<= 1) {
+        const S u = __shfl_up_sync(kFullMask, v, d);
+        if (lane >= d) v = op(u, v);
+    }
+    const S before = __shfl_sync(kFullMask, v, warp > 0 ? warp - 1 : 0);
+    warp_excl = (warp > 0) ? before : Op::identity();
+    group_total = __shfl_sync(kFullMask, v, NW - 1);
+}
+
+// What the consume group gets for one tile.
+template <class S>
+struct ConsumeTile {
+    unsigned tile;
+    S prefix;           // exclusive prefix of the tile's aggregate
+    S aggregate;        // the tile's own aggregate (from pass A)
+    unsigned char *buf; // the B buffer (P::kBBytes bytes)
+    unsigned round;     // alternates the warp-totals buffers
+};
+
+template <class P>
+struct PipeShape {
+    static constexpr int NS = P::kConsumeWarps, NR = P::kReduceWarps, R = P::kRecords;
+    static constexpr int SA = P::kAStages, SB = P::kBStages;
+    static constexpr int kFirstReduceWarp = NS;
+    static constexpr int kFirstLookbackWarp = NS + NR;
+    static constexpr int kProducerA = NS + NR + R;
+    static constexpr int kProducerB = NS + NR + R + 1;
+    static constexpr int kThreads = (NS + NR + R + 2) * 32;
+    static constexpr unsigned kNoCopy = 0xffffffffu;
+    struct Ctrl {
+        uint64_t a_full[SA], a_empty[SA];
+        uint64_t b_full[SB], b_empty[SB];
+        uint64_t rec_pending[R], rec_ready[R], rec_free[R];
+        unsigned a_tile[SA], a_last[SA];
+        unsigned b_tile[SB], b_rec[SB], b_last[SB];
+        unsigned rec_tile[R];
+        uint32_t rec_agg[R], rec_prefix[R];
+        uint32_t red[NR], red_extra[NR];
+        uint32_t wtot[2][NS];
+        unsigned tag;
+    };
+    // Leading 16 bytes let a consume step read one chunk before B buffer 0.
+    static constexpr size_t kLead = 16;
+    static constexpr size_t kABase = kLead;
+    static constexpr size_t kBBase = kABase + static_cast<size_t>(SA) * P::kABytes;
+    static constexpr size_t kCtrlBase = kBBase + static_cast<size_t>(SB) * P::kBBytes;
+    static constexpr size_t kSmemBytes = kCtrlBase + sizeof(Ctrl) + 64;
+    static_assert(P::kABytes % 16 == 0 && P::kBBytes % 16 == 0, "16-byte aligned buffers");
+    static_assert(kThreads <= 1024, "one block of at most 1024 threads");
+};
+
+template <class P>
+__global__ void __launch_bounds__(PipeShape<P>::kThreads, 1)
+pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long *status, DevState *st,
+                   unsigned capacity, unsigned spin_limit, unsigned wait_limit)
+{
+    using Op = typename P::Op;
+    using S = typename Op::S;
+    using G = PipeShape<P>;
+    constexpr int NS = G::NS, NR = G::NR, R = G::R, SA = G::SA, SB = G::SB;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *abuf = smem + G::kABase;
+    unsigned char *bbuf = smem + G::kBBase;
+    auto *ctrl = reinterpret_cast<typename G::Ctrl *>(smem + G::kCtrlBase);
+    const Op op;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) {
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(&ctrl->a_full[s], 1);
+            mbar_init(&ctrl->a_empty[s], NR);
+            ctrl->a_last[s] = G::kNoCopy;
+        }
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(&ctrl->b_full[s], 1);
+            mbar_init(&ctrl->b_empty[s], NS);
+            ctrl->b_last[s] = G::kNoCopy;
+        }
+        for (int r = 0; r < R; ++r) {
+            mbar_init(&ctrl->rec_pending[r], 1);
+            mbar_init(&ctrl->rec_ready[r], 1);
+            mbar_init(&ctrl->rec_free[r], NS);
+        }
+        ctrl->tag = read_tag(st);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const unsigned tag = ctrl->tag;
+
+    if (warp == G::kProducerA) {
+        // ------------------------------------------------------- A producer
+        // One ticket >= num_tiles per block ends the tickets; then R end
+        // markers follow so that every look-back warp receives one.
+        const uint64_t pol = l2_policy_evict_last();
+        unsigned ends = 0;
+        for (unsigned i = 0; ends < static_cast<unsigned>(R); ++i) {
+            const unsigned a = i % SA, ka = i / SA;
+            if (ka > 0 && !mbar_wait(&ctrl->a_empty[a], (ka - 1) & 1u, wait_limit)) {
+                if (lane == 0) atomicOr(&st->error, kErrTimeout);
+                break;
+            }
+            unsigned t = num_tiles;
+            if (ends == 0) {
+                if (lane == 0) t = atomicAdd(&st->ticket, 1u);
+                t = __shfl_sync(kFullMask, t, 0);
+            }
+            if (t >= num_tiles) {
+                if (lane == 0) {
+                    ctrl->a_tile[a] = num_tiles;
+                    ctrl->a_last[a] = G::kNoCopy;
+                    mbar_arrive(&ctrl->a_full[a]);
+                }
+                if (ends == 0 && t == num_tiles + gridDim.x - 1) finish_launch(st, status, num_tiles, capacity, lane);
+                ++ends;
+                continue;
+            }
+            if (lane == 0) {
+                const unsigned bytes = P::a_bytes(args, t);
+                ctrl->a_tile[a] = t;
+                if (bytes != 0) {
+                    ctrl->a_last[a] = ka;
+                    mbar_arrive_expect_tx(&ctrl->a_full[a], bytes);
+                    bulk_load_hint(abuf + static_cast<size_t>(a) * P::kABytes, P::a_src(args, t), bytes,
+                                   &ctrl->a_full[a], pol);
+                } else {
+                    ctrl->a_last[a] = G::kNoCopy;
+                    mbar_arrive(&ctrl->a_full[a]);
+                }
+            }
+        }
+        if (lane == 0)
+            for (int a = 0; a < SA; ++a)
+                if (ctrl->a_last[a] != G::kNoCopy) (void)mbar_wait(&ctrl->a_full[a], ctrl->a_last[a] & 1u, wait_limit);
+        return;
+    }
+
+    if (warp == G::kProducerB) {
+        // ------------------------------------------------------- B producer
+        const uint64_t pol = l2_policy_evict_first();
+        for (unsigned i = 0;; ++i) {
+            const unsigned b = i % SB, kb = i / SB, r = i % R, kr = i / R;
+            bool ok = mbar_wait(&ctrl->rec_ready[r], kr & 1u, wait_limit);
+            if (ok && kb > 0) ok = mbar_wait(&ctrl->b_empty[b], (kb - 1) & 1u, wait_limit);
+            if (!ok) {
+                if (lane == 0) atomicOr(&st->error, kErrTimeout);
+                break;
+            }
+            const unsigned t = ctrl->rec_tile[r];
+            if (lane == 0) {
+                ctrl->b_tile[b] = t < num_tiles ? t : num_tiles;
+                ctrl->b_rec[b] = r;
+                unsigned total = 0;
+                const void *src[2] = {nullptr, nullptr};
+                unsigned bytes[2] = {0, 0}, off[2] = {0, 0};
+                if (t < num_tiles) {
+                    P::b_copies(args, t, src, bytes, off);
+                    total = bytes[0] + bytes[1];
+                }
+                if (total != 0) {
+                    ctrl->b_last[b] = kb;
+                    mbar_arrive_expect_tx(&ctrl->b_full[b], total);
+                    unsigned char *dst = bbuf + static_cast<size_t>(b) * P::kBBytes;
+                    for (int j = 0; j < 2; ++j)
+                        if (bytes[j] != 0) bulk_load_hint(dst + off[j], src[j], bytes[j], &ctrl->b_full[b], pol);
+                } else {
+                    ctrl->b_last[b] = G::kNoCopy;
+                    mbar_arrive(&ctrl->b_full[b]);
+                }
+            }
+            if (t >= num_tiles) break;
+        }
+        if (lane == 0)
+            for (int b = 0; b < SB; ++b)
+                if (ctrl->b_last[b] != G::kNoCopy) (void)mbar_wait(&ctrl->b_full[b], ctrl->b_last[b] & 1u, wait_limit);
+        return;
+    }
+
+    if (warp >= G::kFirstLookbackWarp) {
+        // ------------------------------------------------ look-back warp r
+        const unsigned r = static_cast<unsigned>(warp - G::kFirstLookbackWarp);
+        for (unsigned k = 0;; ++k) {
+            if (!mbar_wait(&ctrl->rec_pending[r], k & 1u, wait_limit)) {
+                if (lane == 0) atomicOr(&st->error, kErrTimeout);
+                break;
+            }
+            const unsigned t = ctrl->rec_tile[r];
+            if (t >= num_tiles) {
+                if (lane == 0) mbar_arrive(&ctrl->rec_ready[r]);
+                break;
+            }
+            const S agg = from_bits<S>(ctrl->rec_agg[r]);
+            S prefix = Op::identity();
+            if (t != 0) {
+                prefix = lookback2<Op>(op, status, group_status(status, capacity), t, tag, agg, &st->error,
+                                       spin_limit, lane);
+                publish<Op>(status, t, tag, kFlagInclusive, op(prefix, agg), lane);
+            }
+            if (lane == 0) {
+                ctrl->rec_prefix[r] = to_bits(prefix);
+                mbar_arrive(&ctrl->rec_ready[r]);
+            }
+        }
+        return;
+    }
+
+    if (warp >= G::kFirstReduceWarp) {
+        // ---------------------------------------------------- reduce group
+        const int rw = warp - G::kFirstReduceWarp;
+        const int rtid = rw * 32 + lane;
+        unsigned ends = 0;
+        for (unsigned i = 0; ends < static_cast<unsigned>(R); ++i) {
+            const unsigned a = i % SA, ka = i / SA, r = i % R, kr = i / R;
+            const bool landed = mbar_wait(&ctrl->a_full[a], ka & 1u, wait_limit);
+            if (!named_sync_and(kBarReduceDecide, NR * 32, landed)) {
+                if (rtid == 0) atomicOr(&st->error, kErrTimeout);
+                break;
+            }
+            const unsigned t = ctrl->a_tile[a];
+            if (t >= num_tiles) {
+                // forward the end marker to record r's look-back warp
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->a_empty[a]);
+                bool freed = true;
+                if (rtid == 0) {
+                    if (kr > 0) freed = mbar_wait(&ctrl->rec_free[r], (kr - 1) & 1u, wait_limit);
+                    if (!freed) atomicOr(&st->error, kErrTimeout);
+                    ctrl->rec_tile[r] = num_tiles;
+                    mbar_arrive(&ctrl->rec_pending[r]);
+                }
+                if (!named_sync_and(kBarReduceDecide, NR * 32, rtid != 0 || freed)) break;
+                ++ends;
+                continue;
+            }
+            S v = Op::identity();
+            unsigned extra = 0;
+            P::reduce(args, abuf + static_cast<size_t>(a) * P::kABytes, t, rtid, NR * 32, v, extra);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->a_empty[a]);   // buffer read: free it
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
+            if (P::kHasExtra) extra = __reduce_add_sync(kFullMask, extra);
+            if (lane == 0) {
+                ctrl->red[rw] = to_bits(v);
+                ctrl->red_extra[rw] = extra;
+            }
+            named_sync(kBarReduceTotals, NR * 32);
+            bool freed = true;
+            if (rtid == 0) {
+                S agg = from_bits<S>(ctrl->red[0]);
+                unsigned ex = ctrl->red_extra[0];
+#pragma unroll
+                for (int w = 1; w < NR; ++w) {
+                    agg = op(agg, from_bits<S>(ctrl->red[w]));
+                    ex += ctrl->red_extra[w];
+                }
+                // publish first; a record (and so a look-back warp) is only
+                // claimed for the time the prefix takes to resolve
+                st_status(status + t, pack_status(tag, t == 0 ? kFlagInclusive : kFlagAggregate, to_bits(agg)));
+                if (P::kHasExtra) P::after_reduce(args, t, ex);
+                if (kr > 0) freed = mbar_wait(&ctrl->rec_free[r], (kr - 1) & 1u, wait_limit);
+                if (!freed) atomicOr(&st->error, kErrTimeout);
+                ctrl->rec_tile[r] = t;
+                ctrl->rec_agg[r] = to_bits(agg);
+                mbar_arrive(&ctrl->rec_pending[r]);
+            }
+            // red[] free for the next tile; a timed-out record wait ends the group
+            if (!named_sync_and(kBarReduceTotals, NR * 32, rtid != 0 || freed)) break;
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consume group
+    unsigned round = 0;
+    for (unsigned i = 0;; ++i) {
+        const unsigned b = i % SB, kb = i / SB;
+        const bool landed = mbar_wait(&ctrl->b_full[b], kb & 1u, wait_limit);
+        if (!named_sync_and(kBarConsumeDecide, NS * 32, landed)) {
+            if (tid == 0) atomicOr(&st->error, kErrTimeout);
+            break;
+        }
+        const unsigned t = ctrl->b_tile[b];
+        if (t >= num_tiles) break;
+        const unsigned r = ctrl->b_rec[b];
+        ConsumeTile<S> ct;
+        ct.tile = t;
+        ct.prefix = from_bits<S>(ctrl->rec_prefix[r]);
+        ct.aggregate = from_bits<S>(ctrl->rec_agg[r]);
+        ct.buf = bbuf + static_cast<size_t>(b) * P::kBBytes;
+        ct.round = round;
+        // release(): the B buffer and the record are no longer needed
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ctrl->b_empty[b]);
+                mbar_arrive(&ctrl->rec_free[r]);
+            }
+        };
+        round += P::consume(args, ct, ctrl->wtot[0], ctrl->wtot[1], warp, lane, release);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Scan policy: pass A reads the tile (4-byte elements) and folds it; pass B
+// re-reads it, scans it with the prefix and stores it.
+// ---------------------------------------------------------------------------
+template <class OpT, bool INCLUSIVE, int NS_, int NR_, int VECS_, int SA_, int SB_, int R_>
+struct ScanPolicy {
+    using Op = OpT;
+    using S = typename Op::S;
+    static constexpr int kConsumeWarps = NS_, kReduceWarps = NR_, kRecords = R_, kAStages = SA_, kBStages = SB_;
+    static constexpr int VECS = VECS_;
+    static constexpr int kWarpItems = 32 * 4 * VECS;
+    static constexpr int kTile = NS_ * 32 * 4 * VECS;
+    static constexpr size_t kABytes = static_cast<size_t>(kTile) * 4;
+    static constexpr size_t kBBytes = static_cast<size_t>(kTile) * 4;
+    static constexpr bool kHasExtra = false;
+    struct Args {
+        const S *in;
+        S *out;
+        size_t n;
+    };
+    __device__ static unsigned tile_len(const Args &a, unsigned t)
+    {
+        const size_t rem = a.n - static_cast<size_t>(t) * kTile;
+        return rem < static_cast<size_t>(kTile) ? static_cast<unsigned>(rem) : static_cast<unsigned>(kTile);
+    }
+    // elements a bulk copy delivers (a multiple of 16 bytes)
+    __device__ static unsigned copied(const Args &a, unsigned t) { return tile_len(a, t) & ~3u; }
+    __device__ static const void *a_src(const Args &a, unsigned t) { return a.in + static_cast<size_t>(t) * kTile; }
+    __device__ static unsigned a_bytes(const Args &a, unsigned t) { return copied(a, t) * 4u; }
+    __device__ static void b_copies(const Args &a, unsigned t, const void **src, unsigned *bytes, unsigned *off)
+    {
+        src[0] = a.in + static_cast<size_t>(t) * kTile;
+        bytes[0] = copied(a, t) * 4u;
+        off[0] = 0;
+    }
+    __device__ static void reduce(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int nthr, S &v,
+                                  unsigned &)
+    {
+        const Op op;
+        const S *buf = reinterpret_cast<const S *>(abuf);
+        const unsigned cp = copied(a, t);
+        S v0 = Op::identity(), v1 = Op::identity(), v2 = Op::identity(), v3 = Op::identity();
+        if (cp == static_cast<unsigned>(kTile)) {
+            const uint4 *b4 = reinterpret_cast<const uint4 *>(buf);
+#pragma unroll 4
+            for (int c = rtid; c < kTile / 4; c += nthr) {
+                const uint4 q = b4[c];
+                v0 = op(v0, from_bits<S>(q.x));
+                v1 = op(v1, from_bits<S>(q.y));
+                v2 = op(v2, from_bits<S>(q.z));
+                v3 = op(v3, from_bits<S>(q.w));
+            }
+        } else {
+            const size_t base = static_cast<size_t>(t) * kTile;
+            const unsigned len = tile_len(a, t);
+            for (unsigned e = rtid; e < len; e += nthr) v0 = op(v0, e < cp ? buf[e] : a.in[base + e]);
+        }
+        v = op(op(v0, v1), op(v2, v3));
+    }
+    __device__ static void after_reduce(const Args &, unsigned, unsigned) {}
+    template <class Release>
+    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
+                                       int warp, int lane, Release &release)
+    {
+        const Op op;
+        const unsigned t = ct.tile;
+        const size_t base = static_cast<size_t>(t) * kTile;
+        const int wbase = warp * kWarpItems;
+        const S *buf = reinterpret_cast<const S *>(ct.buf);
+        const unsigned cp = copied(a, t);
+        S x[VECS][4];
+        if (cp == static_cast<unsigned>(kTile)) {
+            const uint4 *b4 = reinterpret_cast<const uint4 *>(buf + wbase);
+#pragma unroll
+            for (int q = 0; q < VECS; ++q) {
+                const uint4 u = b4[q * 32 + lane];
+                x[q][0] = from_bits<S>(u.x);
+                x[q][1] = from_bits<S>(u.y);
+                x[q][2] = from_bits<S>(u.z);
+                x[q][3] = from_bits<S>(u.w);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < VECS; ++q)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const unsigned e = static_cast<unsigned>(wbase + (q * 32 + lane) * 4 + j);
+                    x[q][j] = (e < cp) ? buf[e] : ((base + e < a.n) ? a.in[base + e] : Op::identity());
+                }
+        }
+        release();   // the tile is in registers now
+        S tt[VECS];
+#pragma unroll
+        for (int q = 0; q < VECS; ++q) tt[q] = op(op(x[q][0], x[q][1]), op(x[q][2], x[q][3]));
+        S row_excl[VECS], warp_total;
+        warp_scan_rows<Op, VECS>(op, tt, lane, row_excl, warp_total);
+        S warp_excl, total;
+        group_scan<Op, NS_>(op, warp_total, (ct.round & 1) ? wbuf1 : wbuf0, warp, lane, warp_excl, total);
+        const S pfx = op(ct.prefix, warp_excl);
+#pragma unroll
+        for (int q = 0; q < VECS; ++q) {
+            S cur = op(pfx, row_excl[q]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const S v = x[q][j];
+                if (INCLUSIVE) {
+                    cur = op(cur, v);
+                    x[q][j] = cur;
+                } else {
+                    x[q][j] = cur;
+                    cur = op(cur, v);
+                }
+            }
+        }
+        if (base + kTile <= a.n) {
+            uint4 *o4 = reinterpret_cast<uint4 *>(a.out + base + wbase);
+#pragma unroll
+            for (int q = 0; q < VECS; ++q)
+                st_stream(o4 + q * 32 + lane,
+                          make_uint4(to_bits(x[q][0]), to_bits(x[q][1]), to_bits(x[q][2]), to_bits(x[q][3])));
+        } else {
+#pragma unroll
+            for (int q = 0; q < VECS; ++q)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const size_t e = base + wbase + static_cast<size_t>((q * 32 + lane) * 4 + j);
+                    if (e < a.n) a.out[e] = x[q][j];
+                }
+        }
+        return 1;   // one warp-totals buffer used
+    }
+};
+
+}  // namespace devscan

@@ -5,7 +5,7 @@
 //   * pipelined single pass (default for 16-byte-aligned data): persistent
 //     warp-specialised blocks; bulk copies, tile aggregates published as
 //     soon as a tile lands, two-level decoupled look-back, and L2 holding
-//     each tile while its prefix resolves (scan_l2.cuh); one launch, HBM
+//     each tile while its prefix resolves (pipeline_l2.cuh); one launch, HBM
 //     traffic about 2 * n * sizeof(T) bytes;
 //   * one tile per block with decoupled look-back (any 4-byte alignment):
 //     one launch, 2 * n * sizeof(T) bytes, but each block holds its tile in
@@ -16,7 +16,7 @@
 #include "core.cuh"
 #include "launch.h"
 #include "scan_kernel.cuh"
-#include "scan_l2.cuh"
+#include "pipeline_l2.cuh"
 
 #include <atomic>
 
@@ -177,10 +177,9 @@ cudaError_t launch_lookback(const void *in, void *out, size_t n, const Workspace
     return cudaGetLastError();
 }
 
-// Geometry of the pipelined kernel: 16 scan warps x 4 rows (8,192-element
+// Geometry of the pipelined scan: 16 consume warps x 4 rows (8,192-element
 // tiles), 2 reduce warps, 3 A buffers, 4 B buffers, 12 in-flight records
-// (1,024 threads, 224 KiB of shared memory: one block per SM).
-using PipeG = L2Geom<16, 2, 4, 3, 4, 12>;
+// (1,024 threads, about 224 KiB of shared memory: one block per SM).
 constexpr unsigned kWaitLimit = 1u << 18;   // bounded mbarrier polls (~1 us each at most)
 constexpr size_t kPipelineMinN = size_t(1) << 19;
 
@@ -189,23 +188,24 @@ cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspac
                              cudaStream_t s)
 {
     using S = typename Op::S;
-    auto kernel = scan_l2_kernel<Op, INCLUSIVE, 16, 2, 4, 3, 4, 12>;
+    using P = ScanPolicy<Op, INCLUSIVE, 16, 2, 4, 3, 4, 12>;
+    using G = PipeShape<P>;
+    auto kernel = pipeline_l2_kernel<P>;
     static std::atomic<unsigned long long> attribute_set{0};   // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if ((attribute_set.load() & bit) == 0) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(PipeG::kSmemBytes));
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(G::kSmemBytes));
         if (e != cudaSuccess) return e;
         attribute_set.fetch_or(bit);
     }
-    const unsigned tiles = tiles_for(n, PipeG::kTile);
+    const unsigned tiles = tiles_for(n, P::kTile);
     const unsigned grid = tiles < static_cast<unsigned>(ws.num_sms) ? tiles : static_cast<unsigned>(ws.num_sms);
-    kernel<<<grid, PipeG::kThreads, PipeG::kSmemBytes, s>>>(static_cast<const S *>(in), static_cast<S *>(out), n,
-                                                           tiles, ws.status, ws.state, ws.capacity, spin_limit,
-                                                           kWaitLimit);
+    typename P::Args args{static_cast<const S *>(in), static_cast<S *>(out), n};
+    kernel<<<grid, G::kThreads, G::kSmemBytes, s>>>(args, tiles, ws.status, ws.state, ws.capacity, spin_limit,
+                                                    kWaitLimit);
     return cudaGetLastError();
 }
 

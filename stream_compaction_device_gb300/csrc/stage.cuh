@@ -90,4 +90,38 @@ __device__ __forceinline__ void write_run_scalar(uint32_t *__restrict__ out, siz
         if (g0 + e < limit) out[g0 + e] = stage[s0 + static_cast<int>(e)];
 }
 
+// Copy a run staged in phase with its destination: element i of the run sits
+// at stage[(g0 & 3) + i] (stage 16-byte aligned) and goes to out[g0 + i], out
+// 16-byte aligned.  Shared chunk k then maps to output chunk g0 / 4 + k, so
+// every whole chunk is one 128-bit load and one 128-bit store; only the two
+// ragged end chunks are stored element by element.  Elements at or past
+// `limit` are never written.
+template <int THREADS>
+__device__ __forceinline__ void write_run_direct(uint32_t *__restrict__ out, size_t g0, unsigned cnt,
+                                                 const uint32_t *stage, int tid, size_t limit)
+{
+    if (cnt == 0 || g0 >= limit) return;   // (a start past the end only follows a timed-out wait)
+    const unsigned a = static_cast<unsigned>(g0 & 3);
+    const unsigned end = a + cnt;   // run occupies words [a, end) of the staged chunks
+    const unsigned chunks = (end + 3) >> 2;
+    uint4 *dst = reinterpret_cast<uint4 *>(out) + (g0 >> 2);
+    const uint4 *src = reinterpret_cast<const uint4 *>(stage);
+    const size_t room = limit - (g0 - a);   // words of out from the first chunk's start
+    for (unsigned k = tid; k < chunks; k += THREADS) {
+        const uint4 v = src[k];
+        const unsigned w0 = 4 * k;
+        if (w0 >= a && w0 + 4 <= end && w0 + 4 <= room) {
+            st_stream(dst + k, v);
+        } else {
+            uint32_t *o = reinterpret_cast<uint32_t *>(dst + k);
+            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const unsigned w = w0 + j;
+                if (w >= a && w < end && w < room) o[j] = vv[j];
+            }
+        }
+    }
+}
+
 }  // namespace devscan

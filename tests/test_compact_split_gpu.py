@@ -11,8 +11,8 @@ from gpu_util import from_dev, to_dev
 pytestmark = pytest.mark.gpu
 
 TILE = 4096
-SIZES = [1, 2, 3, 5, 31, 32, 33, 127, 128, 129, 1023, 1024, 1025, TILE - 1, TILE, TILE + 1,
-         3 * TILE + 5, 65_536, 65_537, 300_007]
+SIZES = [1, 2, 3, 5, 15, 16, 17, 31, 32, 33, 127, 128, 129, 1023, 1024, 1025, TILE - 1, TILE, TILE + 1,
+         8191, 8192, 8193, 3 * 8192 + 5, 65_536, 65_537, 300_007, 524_288, 524_291]
 
 
 @pytest.fixture(scope="module")
@@ -20,6 +20,15 @@ def ds():
     import stream_compaction_device_gb300 as m
     m.load()
     return m
+
+
+@pytest.fixture(params=["lookback", "pipelined"])
+def mode(request, ds):
+    """Run a test once on each kernel family (one tile per block; the
+    persistent two-pass pipeline)."""
+    ds.set_carry_mode(request.param)
+    yield request.param
+    ds.set_carry_mode("default")
 
 
 def gpu_compact(ds, v: np.ndarray, f: np.ndarray, voff=0, foff=0, ooff=0):
@@ -45,7 +54,7 @@ def check_compact(ds, v, f, **kw):
 
 
 @pytest.mark.parametrize("pattern", ["random", "none", "all", "alternate", "sparse", "runs"])
-def test_compact_sizes(ds, pattern):
+def test_compact_sizes(ds, mode, pattern):
     rng = np.random.default_rng(21)
     for n in SIZES:
         v = rng.integers(-2**31, 2**31, n, dtype=np.int32)
@@ -65,7 +74,7 @@ def test_compact_sizes(ds, pattern):
 
 
 @pytest.mark.parametrize("voff,foff,ooff", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (2, 3, 3), (0, 4, 2)])
-def test_compact_unaligned(ds, voff, foff, ooff):
+def test_compact_unaligned(ds, mode, voff, foff, ooff):
     rng = np.random.default_rng(voff * 100 + foff * 10 + ooff)
     for n in (1, 77, TILE + 3, 200_001):
         v = rng.integers(-2**31, 2**31, n, dtype=np.int32)
@@ -108,7 +117,7 @@ def gpu_split(ds, k: np.ndarray, bit: int, koff=0, ooff=0):
 
 
 @pytest.mark.parametrize("bit", [0, 1, 5, 16, 30, 31])
-def test_split_sizes(ds, bit):
+def test_split_sizes(ds, mode, bit):
     rng = np.random.default_rng(bit)
     for n in SIZES:
         k = rng.integers(0, 2**32, n, dtype=np.uint32)
@@ -117,7 +126,7 @@ def test_split_sizes(ds, bit):
         assert np.array_equal(got, ref), f"n={n} bit={bit}"
 
 
-def test_split_skewed(ds):
+def test_split_skewed(ds, mode):
     rng = np.random.default_rng(3)
     for n in (TILE + 1, 100_003):
         for frac in (0.0, 0.001, 0.999, 1.0):
@@ -127,7 +136,7 @@ def test_split_skewed(ds):
 
 
 @pytest.mark.parametrize("koff,ooff", [(1, 0), (0, 1), (3, 2)])
-def test_split_unaligned(ds, koff, ooff):
+def test_split_unaligned(ds, mode, koff, ooff):
     rng = np.random.default_rng(koff + 7 * ooff)
     for n in (1, 99, TILE + 5, 70_001):
         k = rng.integers(0, 2**32, n, dtype=np.uint32)
@@ -141,7 +150,7 @@ def gpu_sort(ds, k: np.ndarray):
     return from_dev(d, np.uint32)
 
 
-def test_sort_sizes(ds):
+def test_sort_sizes(ds, mode):
     rng = np.random.default_rng(5)
     for n in (1, 2, 3, 100, TILE, TILE + 1, 65_537, 1_000_003):
         k = rng.integers(0, 2**32, n, dtype=np.uint32)
