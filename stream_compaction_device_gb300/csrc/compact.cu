@@ -137,6 +137,7 @@ template <int NS_, int NR_, int VECS_, int SA_, int SB_, int R_>
 struct CompactPolicy {
     using Op = AddU32;
     using S = uint32_t;
+    static constexpr int kAHint = kL2EvictLast, kBHint = kL2EvictFirst, kPrefetch = 0;
     static constexpr int kConsumeWarps = NS_, kReduceWarps = NR_, kRecords = R_, kAStages = SA_, kBStages = SB_;
     static constexpr int VECS = VECS_;
     static constexpr int kWarpItems = 32 * 4 * VECS;
@@ -163,6 +164,13 @@ struct CompactPolicy {
     __device__ static unsigned values_copied(const Args &a, unsigned t) { return tile_len(a, t) & ~3u; }
     __device__ static const void *a_src(const Args &a, unsigned t) { return a.flags + static_cast<size_t>(t) * kTile; }
     __device__ static unsigned a_bytes(const Args &a, unsigned t) { return flags_copied(a, t); }
+    // both arrays: pass B then finds the values in L2 as well
+    __device__ static void prefetch_l2(const Args &a, unsigned t, uint64_t pol)
+    {
+        if (flags_copied(a, t) != 0) bulk_prefetch_l2(a_src(a, t), flags_copied(a, t), pol);
+        if (values_copied(a, t) != 0)
+            bulk_prefetch_l2(a.in + static_cast<size_t>(t) * kTile, values_copied(a, t) * 4u, pol);
+    }
     __device__ static void b_copies(const Args &a, unsigned t, const void **src, unsigned *bytes, unsigned *off)
     {
         src[0] = a.in + static_cast<size_t>(t) * kTile;

@@ -44,6 +44,22 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// L2 treatment of a bulk copy's lines.
+enum L2Hint : int { kL2None = 0, kL2EvictLast = 1, kL2EvictFirst = 2, kL2EvictNormal = 3 };
+
+__device__ __forceinline__ uint64_t l2_policy(int hint)
+{
+    return hint == kL2EvictLast ? l2_policy_evict_last()
+                                : (hint == kL2EvictFirst ? l2_policy_evict_first() : l2_policy_evict_normal());
+}
+
 __device__ __forceinline__ void bulk_load_hint(void *dst_smem, const void *src_global, unsigned bytes, uint64_t *bar,
                                                uint64_t policy)
 {
@@ -52,6 +68,14 @@ __device__ __forceinline__ void bulk_load_hint(void *dst_smem, const void *src_g
             "r"(smem_u32(dst_smem)),
         "l"(src_global), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Start moving `bytes` of global memory into L2 (no shared memory involved).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src_global, unsigned bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src_global), "r"(bytes),
+                 "l"(policy)
+                 : "memory");
 }
 
 // Named barrier ids of the pipeline (0 is __syncthreads).
@@ -162,8 +186,38 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
     if (warp == G::kProducerA) {
         // ------------------------------------------------------- A producer
         // One ticket >= num_tiles per block ends the tickets; then R end
-        // markers follow so that every look-back warp receives one.
-        const uint64_t pol = l2_policy_evict_last();
+        // markers follow so that every look-back warp receives one.  With
+        // D = P::kPrefetch > 0 the producer takes tickets D tiles ahead of
+        // their A buffer and starts moving those tiles into L2 at once, so an
+        // A buffer waits for an L2 hit rather than for HBM.  Lane j < D holds
+        // the j-th queued ticket.
+        constexpr int D = P::kPrefetch;
+        static_assert(D >= 0 && D < 32, "prefetch depth");
+        const uint64_t pol = l2_policy(P::kAHint);
+        const uint64_t pre_pol = l2_policy_evict_last();
+        bool tickets_done = false;
+        // takes the next ticket (num_tiles once they are done) and, for a real
+        // tile, starts its L2 prefetch
+        auto take = [&]() -> unsigned {
+            if (tickets_done) return num_tiles;
+            unsigned t = 0;
+            if (lane == 0) t = atomicAdd(&st->ticket, 1u);
+            t = __shfl_sync(kFullMask, t, 0);
+            if (t >= num_tiles) {
+                tickets_done = true;
+                // the block that takes the launch's last ticket closes the launch
+                if (t == num_tiles + gridDim.x - 1) finish_launch(st, status, num_tiles, capacity, lane);
+                return num_tiles;
+            }
+            if (D > 0 && lane == 0) P::prefetch_l2(args, t, pre_pol);
+            return t;
+        };
+        unsigned queued = num_tiles;
+#pragma unroll 1
+        for (int j = 0; j < D; ++j) {
+            const unsigned t = take();
+            if (lane == j) queued = t;
+        }
         unsigned ends = 0;
         for (unsigned i = 0; ends < static_cast<unsigned>(R); ++i) {
             const unsigned a = i % SA, ka = i / SA;
@@ -171,10 +225,14 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 if (lane == 0) atomicOr(&st->error, kErrTimeout);
                 break;
             }
-            unsigned t = num_tiles;
-            if (ends == 0) {
-                if (lane == 0) t = atomicAdd(&st->ticket, 1u);
-                t = __shfl_sync(kFullMask, t, 0);
+            unsigned t;
+            if (D > 0) {
+                t = __shfl_sync(kFullMask, queued, 0);
+                queued = __shfl_down_sync(kFullMask, queued, 1);
+                const unsigned nt = take();
+                if (lane == D - 1) queued = nt;
+            } else {
+                t = take();
             }
             if (t >= num_tiles) {
                 if (lane == 0) {
@@ -182,7 +240,6 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                     ctrl->a_last[a] = G::kNoCopy;
                     mbar_arrive(&ctrl->a_full[a]);
                 }
-                if (ends == 0 && t == num_tiles + gridDim.x - 1) finish_launch(st, status, num_tiles, capacity, lane);
                 ++ends;
                 continue;
             }
@@ -192,8 +249,12 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 if (bytes != 0) {
                     ctrl->a_last[a] = ka;
                     mbar_arrive_expect_tx(&ctrl->a_full[a], bytes);
-                    bulk_load_hint(abuf + static_cast<size_t>(a) * P::kABytes, P::a_src(args, t), bytes,
-                                   &ctrl->a_full[a], pol);
+                    if (P::kAHint == kL2None)
+                        bulk_load(abuf + static_cast<size_t>(a) * P::kABytes, P::a_src(args, t), bytes,
+                                  &ctrl->a_full[a]);
+                    else
+                        bulk_load_hint(abuf + static_cast<size_t>(a) * P::kABytes, P::a_src(args, t), bytes,
+                                       &ctrl->a_full[a], pol);
                 } else {
                     ctrl->a_last[a] = G::kNoCopy;
                     mbar_arrive(&ctrl->a_full[a]);
@@ -208,7 +269,9 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
 
     if (warp == G::kProducerB) {
         // ------------------------------------------------------- B producer
-        const uint64_t pol = l2_policy_evict_first();
+        // Records in order (measured: serving them as their prefixes resolve
+        // was slower -- the polling adds wake-up latency).
+        const uint64_t pol = l2_policy(P::kBHint);
         for (unsigned i = 0;; ++i) {
             const unsigned b = i % SB, kb = i / SB, r = i % R, kr = i / R;
             bool ok = mbar_wait(&ctrl->rec_ready[r], kr & 1u, wait_limit);
@@ -232,8 +295,13 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                     ctrl->b_last[b] = kb;
                     mbar_arrive_expect_tx(&ctrl->b_full[b], total);
                     unsigned char *dst = bbuf + static_cast<size_t>(b) * P::kBBytes;
-                    for (int j = 0; j < 2; ++j)
-                        if (bytes[j] != 0) bulk_load_hint(dst + off[j], src[j], bytes[j], &ctrl->b_full[b], pol);
+                    for (int j = 0; j < 2; ++j) {
+                        if (bytes[j] == 0) continue;
+                        if (P::kBHint == kL2None)
+                            bulk_load(dst + off[j], src[j], bytes[j], &ctrl->b_full[b]);
+                        else
+                            bulk_load_hint(dst + off[j], src[j], bytes[j], &ctrl->b_full[b], pol);
+                    }
                 } else {
                     ctrl->b_last[b] = G::kNoCopy;
                     mbar_arrive(&ctrl->b_full[b]);
@@ -375,9 +443,13 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
 // Scan policy: pass A reads the tile (4-byte elements) and folds it; pass B
 // re-reads it, scans it with the prefix and stores it.
 // ---------------------------------------------------------------------------
-template <class OpT, bool INCLUSIVE, int NS_, int NR_, int VECS_, int SA_, int SB_, int R_>
+// AH / BH: L2 hints of the pass-A and pass-B copies; STREAM_OUT: evict-first
+// (.cs) output stores.
+template <class OpT, bool INCLUSIVE, int NS_, int NR_, int VECS_, int SA_, int SB_, int R_, int AH = kL2EvictLast,
+          int BH = kL2EvictFirst, bool STREAM_OUT = true, int PREFETCH = 0>
 struct ScanPolicy {
     using Op = OpT;
+    static constexpr int kAHint = AH, kBHint = BH, kPrefetch = PREFETCH;
     using S = typename Op::S;
     static constexpr int kConsumeWarps = NS_, kReduceWarps = NR_, kRecords = R_, kAStages = SA_, kBStages = SB_;
     static constexpr int VECS = VECS_;
@@ -400,6 +472,10 @@ struct ScanPolicy {
     __device__ static unsigned copied(const Args &a, unsigned t) { return tile_len(a, t) & ~3u; }
     __device__ static const void *a_src(const Args &a, unsigned t) { return a.in + static_cast<size_t>(t) * kTile; }
     __device__ static unsigned a_bytes(const Args &a, unsigned t) { return copied(a, t) * 4u; }
+    __device__ static void prefetch_l2(const Args &a, unsigned t, uint64_t pol)
+    {
+        if (a_bytes(a, t) != 0) bulk_prefetch_l2(a_src(a, t), a_bytes(a, t), pol);
+    }
     __device__ static void b_copies(const Args &a, unsigned t, const void **src, unsigned *bytes, unsigned *off)
     {
         src[0] = a.in + static_cast<size_t>(t) * kTile;
@@ -488,9 +564,13 @@ struct ScanPolicy {
         if (base + kTile <= a.n) {
             uint4 *o4 = reinterpret_cast<uint4 *>(a.out + base + wbase);
 #pragma unroll
-            for (int q = 0; q < VECS; ++q)
-                st_stream(o4 + q * 32 + lane,
-                          make_uint4(to_bits(x[q][0]), to_bits(x[q][1]), to_bits(x[q][2]), to_bits(x[q][3])));
+            for (int q = 0; q < VECS; ++q) {
+                const uint4 v = make_uint4(to_bits(x[q][0]), to_bits(x[q][1]), to_bits(x[q][2]), to_bits(x[q][3]));
+                if (STREAM_OUT)
+                    st_stream(o4 + q * 32 + lane, v);
+                else
+                    o4[q * 32 + lane] = v;
+            }
         } else {
 #pragma unroll
             for (int q = 0; q < VECS; ++q)

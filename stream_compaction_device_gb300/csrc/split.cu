@@ -181,6 +181,7 @@ template <int NS_, int NR_, int VECS_, int SA_, int SB_, int R_>
 struct SplitPolicy {
     using Op = AddU32;
     using S = uint32_t;
+    static constexpr int kAHint = kL2EvictLast, kBHint = kL2EvictFirst, kPrefetch = 0;
     static constexpr int kConsumeWarps = NS_, kReduceWarps = NR_, kRecords = R_, kAStages = SA_, kBStages = SB_;
     static constexpr int VECS = VECS_;
     static constexpr int kWarpItems = 32 * 4 * VECS;
@@ -206,6 +207,10 @@ struct SplitPolicy {
     __device__ static unsigned copied(const Args &a, unsigned t) { return tile_len(a, t) & ~3u; }
     __device__ static const void *a_src(const Args &a, unsigned t) { return a.keys + static_cast<size_t>(t) * kTile; }
     __device__ static unsigned a_bytes(const Args &a, unsigned t) { return copied(a, t) * 4u; }
+    __device__ static void prefetch_l2(const Args &a, unsigned t, uint64_t pol)
+    {
+        if (a_bytes(a, t) != 0) bulk_prefetch_l2(a_src(a, t), a_bytes(a, t), pol);
+    }
     __device__ static void b_copies(const Args &a, unsigned t, const void **src, unsigned *bytes, unsigned *off)
     {
         src[0] = a.keys + static_cast<size_t>(t) * kTile;
