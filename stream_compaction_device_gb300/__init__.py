@@ -14,7 +14,7 @@ import torch
 from . import _lib
 from ._lib import DevscanError, OPS, load
 
-__all__ = ["scan_inclusive", "scan_exclusive", "compact", "split_bit", "radix_sort", "scan_host",
+__all__ = ["scan_inclusive", "scan_exclusive", "compact", "split_bit", "radix_sort", "radix_sort_digits", "scan_host",
            "device_status", "set_carry_mode", "stream_release", "selftest_stalled_wait", "DevscanError",
            "load"]
 
@@ -111,6 +111,20 @@ def radix_sort(keys: torch.Tensor, tmp: torch.Tensor | None = None, stream=None)
     _check_cuda(tmp, "tmp")
     _lib.check(load().radix_sort_u32(keys.data_ptr(), tmp.data_ptr(), keys.numel(), _stream_handle(stream)),
                "radix_sort_u32")
+    return keys
+
+
+def radix_sort_digits(keys: torch.Tensor, tmp: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """In-place ascending sort of 32-bit keys (bits read as uint32) by 8
+    passes of 4-bit digits; ``tmp`` is a same-size scratch tensor."""
+    _check_cuda(keys, "keys")
+    if keys.element_size() != 4 or keys.is_floating_point():
+        raise TypeError("keys must be a 32-bit integer tensor (bits read as uint32)")
+    if tmp is None:
+        tmp = torch.empty_like(keys)
+    _check_cuda(tmp, "tmp")
+    _lib.check(load().radix_sort_digits_u32(keys.data_ptr(), tmp.data_ptr(), keys.numel(),
+                                            _stream_handle(stream)), "radix_sort_digits_u32")
     return keys
 
 

@@ -52,6 +52,8 @@ def load() -> ctypes.CDLL:
         lib.split_bit_u32.restype = i
         lib.radix_sort_u32.argtypes = [vp, vp, sz, vp]
         lib.radix_sort_u32.restype = i
+        lib.radix_sort_digits_u32.argtypes = [vp, vp, sz, vp]
+        lib.radix_sort_digits_u32.restype = i
         lib.devscan_device_status.argtypes = [vp]
         lib.devscan_device_status.restype = i
         lib.devscan_status_string.argtypes = [i]

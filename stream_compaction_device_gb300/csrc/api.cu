@@ -25,6 +25,8 @@ struct Slot {
     void *base = nullptr;
     size_t bytes = 0;
     Workspace ws;
+    void *extra = nullptr;   // per-stream scratch of the digit sort (its histograms)
+    size_t extra_bytes = 0;
 };
 
 std::mutex g_mutex;
@@ -87,6 +89,33 @@ devscan_status acquire(cudaStream_t stream, unsigned tiles, Workspace *out)
     }
     slot.ws.num_sms = sms->second;
     *out = slot.ws;
+    return DEVSCAN_OK;
+}
+
+// Per-stream scratch of at least `bytes`, grown stream-ordered like the
+// workspace (the slot must exist: call acquire() first).
+devscan_status acquire_extra(cudaStream_t stream, size_t bytes, void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_slots.find({dev, reinterpret_cast<uintptr_t>(stream)});
+    if (it == g_slots.end()) return DEVSCAN_ERR_CUDA;
+    Slot &slot = it->second;
+    if (slot.extra_bytes < bytes) {
+        if (slot.extra != nullptr && cudaFreeAsync(slot.extra, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+        slot.extra = nullptr;
+        slot.extra_bytes = 0;
+        void *p = nullptr;
+        const cudaError_t e = cudaMallocAsync(&p, bytes, stream);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return e == cudaErrorMemoryAllocation ? DEVSCAN_ERR_NOMEM : DEVSCAN_ERR_CUDA;
+        }
+        slot.extra = p;
+        slot.extra_bytes = bytes;
+    }
+    *out = slot.extra;
     return DEVSCAN_OK;
 }
 
@@ -219,6 +248,30 @@ devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStrea
     return DEVSCAN_OK;
 }
 
+devscan_status radix_sort_digits_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStream_t stream)
+{
+    if (n > static_cast<size_t>(INT32_MAX)) return DEVSCAN_ERR_INVALID;
+    if (n == 0) return DEVSCAN_OK;
+    if (keys == nullptr || tmp == nullptr) return DEVSCAN_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(keys) % 4 != 0 || reinterpret_cast<uintptr_t>(tmp) % 4 != 0)
+        return DEVSCAN_ERR_INVALID;
+    if (overlaps(keys, n * 4, tmp, n * 4)) return DEVSCAN_ERR_INVALID;
+    const size_t hist_words = radix_hist_words(n);
+    Workspace ws;
+    devscan_status st = acquire(stream, tiles_for(hist_words, kScanTile), &ws);
+    if (st != DEVSCAN_OK) return st;
+    void *hist = nullptr;
+    st = acquire_extra(stream, hist_words * sizeof(uint32_t), &hist);
+    if (st != DEVSCAN_OK) return st;
+    uint32_t *src = keys, *dst = tmp;
+    for (int pass = 0; pass < 8; ++pass) {
+        if (launch_radix_pass(src, dst, n, pass, static_cast<uint32_t *>(hist), ws, kSpinLimit, stream) != cudaSuccess)
+            return DEVSCAN_ERR_CUDA;
+        std::swap(src, dst);
+    }
+    return DEVSCAN_OK;
+}
+
 devscan_status devscan_device_status(cudaStream_t stream)
 {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
@@ -265,7 +318,9 @@ devscan_status devscan_stream_release(cudaStream_t stream)
     auto it = g_slots.find({dev, reinterpret_cast<uintptr_t>(stream)});
     if (it == g_slots.end()) return DEVSCAN_OK;
     void *base = it->second.base;
+    void *extra = it->second.extra;
     g_slots.erase(it);
+    if (extra != nullptr && cudaFreeAsync(extra, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
     return from_cuda(cudaFreeAsync(base, stream));
 }
 

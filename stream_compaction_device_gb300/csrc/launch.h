@@ -75,4 +75,10 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
 cudaError_t launch_split(const uint32_t *keys, uint32_t *out, size_t n, int bit, const unsigned *zeros,
                          unsigned *next_zeros, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
+// One 4-bit-digit LSD radix pass (digit `pass`, bits 4 pass .. 4 pass + 3)
+// from src to dst; `hist` holds radix_hist_words(n) words of scratch.
+cudaError_t launch_radix_pass(const uint32_t *src, uint32_t *dst, size_t n, int pass, uint32_t *hist,
+                              const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+size_t radix_hist_words(size_t n);
+
 }  // namespace devscan

@@ -174,3 +174,44 @@ def test_config_sort(ds):
     sample = k[: 1 << 20]
     assert np.array_equal(gpu_sort(ds, sample), oracle.sort_lsd(sample))
     assert ds.device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# 4-bit-digit radix sort
+# ---------------------------------------------------------------------------
+def gpu_sort_digits(ds, k: np.ndarray, koff=0):
+    d = to_dev(np.concatenate([np.zeros(koff, np.uint32), k]))[koff:]
+    ds.radix_sort_digits(d)
+    torch.cuda.synchronize()
+    return from_dev(d, np.uint32)
+
+
+def test_sort_digits_sizes(ds):
+    rng = np.random.default_rng(9)
+    for n in (1, 2, 3, 15, 16, 17, 100, 4095, 4096, 4097, 65_537, 1_000_003):
+        k = rng.integers(0, 2**32, n, dtype=np.uint32)
+        k[: min(n, 6)] = np.array([0, 2**32 - 1, 7, 7, 2**31, 2**31 - 1], dtype=np.uint32)[: min(n, 6)]
+        assert np.array_equal(gpu_sort_digits(ds, k), oracle.sort_lsd(k)), f"n={n}"
+
+
+def test_sort_digits_patterns(ds):
+    rng = np.random.default_rng(10)
+    n = 300_001
+    cases = {
+        "all equal": np.full(n, 0xDEADBEEF, np.uint32),
+        "one digit": (rng.integers(0, 16, n) << 12).astype(np.uint32),
+        "descending": np.arange(n, dtype=np.uint32)[::-1].copy(),
+        "few values": rng.choice(np.array([3, 2**31, 5, 2**32 - 1], dtype=np.uint32), n),
+    }
+    for name, k in cases.items():
+        assert np.array_equal(gpu_sort_digits(ds, k), np.sort(k)), name
+    # unaligned keys (scalar load path)
+    k = rng.integers(0, 2**32, 77_777, dtype=np.uint32)
+    assert np.array_equal(gpu_sort_digits(ds, k, koff=1), np.sort(k))
+
+
+def test_config_sort_digits(ds):
+    from stream_compaction_device_gb300 import workloads as wl
+    k = wl.radix_keys()
+    assert np.array_equal(gpu_sort_digits(ds, k), np.sort(k))
+    assert ds.device_status() == 0
