@@ -322,6 +322,13 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
     # inclusive add on the same array, and the max / xor sweep
     med, _ = time_events(lambda: ds.scan_inclusive(d_in, d_out), reps, 3)
     out["i32_add_inclusive_2^28"] = row(n, med, 8 * n)
+    # the bracket check on the same +1/-1 array: alone (reads 4 B per element)
+    # and fused into the stored inclusive scan
+    res = torch.empty(2, dtype=torch.int32, device="cuda")
+    med, _ = time_events(lambda: ds.bracket_scan(d_in, result=res, store=False), reps, 3)
+    out["bracket_check_2^28"] = row(n, med, 4 * n)
+    med, _ = time_events(lambda: ds.bracket_scan(d_in, out=d_out, result=res), reps, 3)
+    out["bracket_scan_2^28"] = row(n, med, 8 * n)
     del d_in
     xm = torch.from_numpy(wl.max_values(n)).cuda()
     med, _ = time_events(lambda: ds.scan_inclusive(xm, d_out, op="max"), reps, 3)
@@ -341,7 +348,7 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
     dv = torch.from_numpy(v).cuda()
     dout = torch.empty_like(dv)
     cnt = torch.empty(1, dtype=torch.int32, device="cuda")
-    comp = {}
+    comp, comp_gt = {}, {}
     for sel in wl.SELECTIVITIES:
         f = torch.from_numpy(wl.predicate_flags(v, wl.threshold_for(sel))).cuda()
         med, _ = time_events(lambda: ds.compact(dv, f, dout, cnt), reps, 3)
@@ -350,7 +357,14 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
         r["kept"] = k
         comp[f"{int(sel * 100)}%"] = r
         del f
+        t = wl.threshold_for(sel)
+        med, _ = time_events(lambda: ds.compact_greater(dv, t, dout, cnt), reps, 3)
+        k = int(cnt.item())
+        r = row(nc, med, 4 * nc + 4 * k + 4)
+        r["kept"] = k
+        comp_gt[f"{int(sel * 100)}%"] = r
     out["compaction_2^26"] = comp
+    out["compaction_gt_fused_2^26"] = comp_gt
 
     # split and radix sort at N = 2^26
     keys = torch.from_numpy(wl.radix_keys(nc).view(np.int32)).cuda()

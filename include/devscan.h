@@ -100,6 +100,35 @@ devscan_status scan_exclusive_f32(const float *in, float *out, size_t n,
 devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out,
                            int32_t *count, size_t n, cudaStream_t stream);
 
+/* Stream compaction with the predicate evaluated on the device (P3 section
+ * 3.3: each element contributes 1 when it is to be output, 0 otherwise; P2
+ * section 4.1, the predicate applied element by element): out[0 .. *count)
+ * receives, in input order, every in[i] with in[i] > threshold (signed
+ * compare).  No flag array is read, so the traffic is 4 bytes per element
+ * plus 4 per kept element.  Arguments, limits and errors as compact_i32,
+ * without flags. */
+devscan_status compact_gt_i32(const int32_t *in, int32_t threshold, int32_t *out,
+                              int32_t *count, size_t n, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Bracket check fused into the scan (P1 section 一: '(' counts +1 and ')'
+ * -1; a negative running sum means a surplus ')', a nonzero final sum means
+ * the brackets do not pair up, and one scan answers both).  One pass over
+ * in[0 .. n):
+ *   out       : the inclusive int32 add-scan (wrapping modulo 2^32), or NULL
+ *               to skip storing it (the check alone then only reads in);
+ *               may equal in; 4-byte aligned;
+ *   result[0] : 1 if some inclusive prefix is negative (as int32), else 0;
+ *   result[1] : the final inclusive prefix (0 when n == 0).
+ * result is a device int32[2], 4-byte aligned, overlapping neither in nor
+ * out (else DEVSCAN_ERR_INVALID); it is cleared on the stream first.  The
+ * brackets are balanced iff result[0] == 0 and result[1] == 0.  Any int32
+ * weights are accepted; the answers refer to the wrapped int32 prefixes.
+ * n limits and errors as the scans.
+ * ------------------------------------------------------------------------- */
+devscan_status bracket_scan_i32(const int32_t *in, int32_t *out, int32_t *result, size_t n,
+                                cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Radix-sort one-bit split (P1 section 一, radix sort; P2 section 4.2): a
  * stable partition of keys by bit `bit`.  With zerosBefore(i) the exclusive

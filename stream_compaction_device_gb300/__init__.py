@@ -15,6 +15,7 @@ from . import _lib
 from ._lib import DevscanError, OPS, load
 
 __all__ = ["scan_inclusive", "scan_exclusive", "compact", "split_bit", "radix_sort", "radix_sort_digits", "scan_host",
+           "compact_greater", "bracket_scan",
            "device_status", "set_carry_mode", "stream_release", "selftest_stalled_wait", "DevscanError",
            "load"]
 
@@ -85,6 +86,49 @@ def compact(values: torch.Tensor, flags: torch.Tensor, out: torch.Tensor | None 
     _lib.check(load().compact_i32(values.data_ptr(), flags.data_ptr(), out.data_ptr(), count.data_ptr(),
                                   values.numel(), _stream_handle(stream)), "compact_i32")
     return out, count
+
+
+def compact_greater(values: torch.Tensor, threshold: int, out: torch.Tensor | None = None,
+                    count: torch.Tensor | None = None, stream=None):
+    """Order-preserving compaction of the int32 values greater than
+    ``threshold`` (signed), the predicate evaluated on the device.  Returns
+    (out, count) as :func:`compact`."""
+    _check_cuda(values, "values")
+    if values.dtype != torch.int32:
+        raise TypeError("values must be int32")
+    if out is None:
+        out = torch.empty_like(values)
+    if count is None:
+        count = torch.empty(1, dtype=torch.int32, device=values.device)
+    _check_cuda(out, "out")
+    _check_cuda(count, "count")
+    _lib.check(load().compact_gt_i32(values.data_ptr(), int(threshold), out.data_ptr(), count.data_ptr(),
+                                     values.numel(), _stream_handle(stream)), "compact_gt_i32")
+    return out, count
+
+
+def bracket_scan(weights: torch.Tensor, out: torch.Tensor | None = None, result: torch.Tensor | None = None,
+                 store: bool = True, stream=None):
+    """Inclusive int32 add-scan of +1/-1 bracket weights with the bracket
+    check in the same pass.  Returns (out or None, result): result[0] is 1
+    when some running sum is negative, result[1] the final sum.  With
+    ``store=False`` the scan is not written (the check alone)."""
+    _check_cuda(weights, "weights")
+    if weights.dtype != torch.int32:
+        raise TypeError("weights must be int32")
+    if store and out is None:
+        out = torch.empty_like(weights)
+    if not store:
+        out = None
+    if result is None:
+        result = torch.empty(2, dtype=torch.int32, device=weights.device)
+    _check_cuda(result, "result")
+    if out is not None:
+        _check_cuda(out, "out")
+    _lib.check(load().bracket_scan_i32(weights.data_ptr(), None if out is None else out.data_ptr(),
+                                       result.data_ptr(), weights.numel(), _stream_handle(stream)),
+               "bracket_scan_i32")
+    return out, result
 
 
 def split_bit(keys: torch.Tensor, bit: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

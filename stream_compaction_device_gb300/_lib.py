@@ -52,6 +52,10 @@ def load() -> ctypes.CDLL:
         lib.split_bit_u32.restype = i
         lib.radix_sort_u32.argtypes = [vp, vp, sz, vp]
         lib.radix_sort_u32.restype = i
+        lib.compact_gt_i32.argtypes = [vp, ctypes.c_int32, vp, vp, sz, vp]
+        lib.compact_gt_i32.restype = i
+        lib.bracket_scan_i32.argtypes = [vp, vp, vp, sz, vp]
+        lib.bracket_scan_i32.restype = i
         lib.radix_sort_digits_u32.argtypes = [vp, vp, sz, vp]
         lib.radix_sort_digits_u32.restype = i
         lib.devscan_device_status.argtypes = [vp]

@@ -201,6 +201,45 @@ devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out
                                     kSpinLimit, stream));
 }
 
+devscan_status compact_gt_i32(const int32_t *in, int32_t threshold, int32_t *out, int32_t *count, size_t n,
+                              cudaStream_t stream)
+{
+    if (count == nullptr || reinterpret_cast<uintptr_t>(count) % 4 != 0) return DEVSCAN_ERR_INVALID;
+    if (n > static_cast<size_t>(INT32_MAX)) return DEVSCAN_ERR_INVALID;
+    if (n > 0) {
+        if (in == nullptr || out == nullptr) return DEVSCAN_ERR_INVALID;
+        if (reinterpret_cast<uintptr_t>(in) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+            return DEVSCAN_ERR_INVALID;
+        if (overlaps(out, n * 4, in, n * 4) || overlaps(count, 4, out, n * 4) || overlaps(count, 4, in, n * 4))
+            return DEVSCAN_ERR_INVALID;
+    }
+    if (n == 0) return from_cuda(cudaMemsetAsync(count, 0, sizeof(int32_t), stream));
+    Workspace ws;
+    const devscan_status st = acquire(stream, tiles_for(n, kCompactTile), &ws);
+    if (st != DEVSCAN_OK) return st;
+    return from_cuda(launch_compact_gt(in, threshold, out, count, n, g_carry_mode.load(std::memory_order_relaxed),
+                                       ws, kSpinLimit, stream));
+}
+
+devscan_status bracket_scan_i32(const int32_t *in, int32_t *out, int32_t *result, size_t n, cudaStream_t stream)
+{
+    if (result == nullptr || reinterpret_cast<uintptr_t>(result) % 4 != 0) return DEVSCAN_ERR_INVALID;
+    if (n > static_cast<size_t>(0xffffffffu) * kScanTile) return DEVSCAN_ERR_INVALID;
+    if (n > 0) {
+        if (in == nullptr || reinterpret_cast<uintptr_t>(in) % 4 != 0) return DEVSCAN_ERR_INVALID;
+        if (out != nullptr && reinterpret_cast<uintptr_t>(out) % 4 != 0) return DEVSCAN_ERR_INVALID;
+        if (overlaps(result, 8, in, n * 4) || (out != nullptr && overlaps(result, 8, out, n * 4)))
+            return DEVSCAN_ERR_INVALID;
+    }
+    Workspace ws;
+    if (n > 0) {
+        const devscan_status st = acquire(stream, tiles_for(n, kScanTile), &ws);
+        if (st != DEVSCAN_OK) return st;
+    }
+    return from_cuda(launch_bracket(in, out, result, n, g_carry_mode.load(std::memory_order_relaxed), ws,
+                                    kSpinLimit, stream));
+}
+
 devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_t n, cudaStream_t stream)
 {
     if (bit < 0 || bit > 31) return DEVSCAN_ERR_INVALID;

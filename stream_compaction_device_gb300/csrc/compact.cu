@@ -17,11 +17,13 @@
 
 namespace devscan {
 
-template <int THREADS, int VECS, bool ALIGNED, bool OUT_ALIGNED>
+// GT: keep in[i] when (int32) in[i] > threshold (flags unused); otherwise
+// keep it when flags[i] != 0.
+template <int THREADS, int VECS, bool ALIGNED, bool OUT_ALIGNED, bool GT = false>
 __global__ void __launch_bounds__(THREADS)
 compact_kernel(const uint32_t *__restrict__ in, const uint8_t *__restrict__ flags, uint32_t *__restrict__ out,
                int32_t *__restrict__ count, size_t n, unsigned num_tiles, unsigned long long *status,
-               DevState *st, unsigned capacity, unsigned spin_limit)
+               DevState *st, unsigned capacity, unsigned spin_limit, int32_t threshold = 0)
 {
     constexpr int NWARPS = THREADS / 32;
     constexpr int WARP_ITEMS = 32 * 4 * VECS;
@@ -46,7 +48,17 @@ compact_kernel(const uint32_t *__restrict__ in, const uint8_t *__restrict__ flag
     uint32_t x[VECS][4];
     load_rows<uint32_t, VECS, ALIGNED>(in, warp_base, n, lane, full, x, 0u);
     uint32_t keep[VECS];
-    if (ALIGNED && full) {
+    if (GT) {
+#pragma unroll
+        for (int r = 0; r < VECS; ++r) {
+            const size_t e = warp_base + static_cast<size_t>(r * 32 + lane) * 4;
+            uint32_t m = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if ((full || e + k < n) && static_cast<int32_t>(x[r][k]) > threshold) m |= 1u << k;
+            keep[r] = m;
+        }
+    } else if (ALIGNED && full) {
         uint32_t f[VECS];
 #pragma unroll
         for (int r = 0; r < VECS; ++r)
@@ -116,6 +128,7 @@ compact_kernel(const uint32_t *__restrict__ in, const uint8_t *__restrict__ flag
 
 
 using CompactPipe = CompactPolicy<16, 2, 4, 2, 3, 12, 1>;
+using CompactGtPipe = CompactGtPolicy<16, 2, 4, 2, 4, 12, 1>;
 constexpr unsigned kCompactWaitLimit = 1u << 18;
 constexpr size_t kCompactPipelineMinN = size_t(1) << 19;
 
@@ -163,6 +176,63 @@ cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out
     else
         compact_kernel<THREADS, VECS, false, false><<<tiles, THREADS, 0, s>>>(
             vin, flags, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit);
+    return cudaGetLastError();
+}
+
+template <class P>
+cudaError_t set_pipeline_smem(void (*kernel)(typename P::Args, unsigned, unsigned long long *, DevState *, unsigned,
+                                             unsigned, unsigned),
+                              std::atomic<unsigned long long> &attribute_set)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if ((attribute_set.load() & bit) == 0) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(PipeShape<P>::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attribute_set.fetch_or(bit);
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_compact_gt(const int32_t *in, int32_t threshold, int32_t *out, int32_t *count, size_t n,
+                              int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+{
+    const bool out_aligned = reinterpret_cast<uintptr_t>(out) % 16 == 0;
+    const bool in_aligned = reinterpret_cast<uintptr_t>(in) % 16 == 0;
+    const uint32_t *vin = reinterpret_cast<const uint32_t *>(in);
+    uint32_t *vout = reinterpret_cast<uint32_t *>(out);
+    const bool pipelined =
+        in_aligned && (carry == kCarryPipelined || (carry != kCarryLookback && n >= kCompactPipelineMinN));
+    if (pipelined) {
+        using G = PipeShape<CompactGtPipe>;
+        auto kernel = pipeline_l2_kernel<CompactGtPipe>;
+        static std::atomic<unsigned long long> attribute_set{0};
+        cudaError_t e = set_pipeline_smem<CompactGtPipe>(kernel, attribute_set);
+        if (e != cudaSuccess) return e;
+        const unsigned tiles = tiles_for(n, CompactGtPipe::kTile);
+        const unsigned grid = tiles < static_cast<unsigned>(ws.num_sms) ? tiles : static_cast<unsigned>(ws.num_sms);
+        CompactGtPipe::Args args{vin, threshold, vout, count, n, tiles, out_aligned};
+        kernel<<<grid, G::kThreads, G::kSmemBytes, s>>>(args, tiles, ws.status, ws.state, ws.capacity, spin_limit,
+                                                        kCompactWaitLimit);
+        return cudaGetLastError();
+    }
+    constexpr int THREADS = kCompactThreads, VECS = kCompactVecs;
+    const unsigned tiles = tiles_for(n, kCompactTile);
+    if (in_aligned && out_aligned)
+        compact_kernel<THREADS, VECS, true, true, true><<<tiles, THREADS, 0, s>>>(
+            vin, nullptr, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit, threshold);
+    else if (in_aligned)
+        compact_kernel<THREADS, VECS, true, false, true><<<tiles, THREADS, 0, s>>>(
+            vin, nullptr, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit, threshold);
+    else if (out_aligned)
+        compact_kernel<THREADS, VECS, false, true, true><<<tiles, THREADS, 0, s>>>(
+            vin, nullptr, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit, threshold);
+    else
+        compact_kernel<THREADS, VECS, false, false, true><<<tiles, THREADS, 0, s>>>(
+            vin, nullptr, vout, count, n, tiles, ws.status, ws.state, ws.capacity, spin_limit, threshold);
     return cudaGetLastError();
 }
 

@@ -75,6 +75,15 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
 cudaError_t launch_split(const uint32_t *keys, uint32_t *out, size_t n, int bit, const unsigned *zeros,
                          unsigned *next_zeros, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
+// Compaction keeping in[i] when in[i] > threshold (signed), predicate
+// evaluated in the kernel.
+cudaError_t launch_compact_gt(const int32_t *in, int32_t threshold, int32_t *out, int32_t *count, size_t n,
+                              int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+// Inclusive int32 add-scan (stored when out != nullptr) with the bracket
+// answers in result[0..1]; clears result first (stream-ordered).
+cudaError_t launch_bracket(const int32_t *in, int32_t *out, int32_t *result, size_t n, int carry,
+                           const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
 // One 4-bit-digit LSD radix pass (digit `pass`, bits 4 pass .. 4 pass + 3)
 // from src to dst; `hist` holds radix_hist_words(n) words of scratch.
 cudaError_t launch_radix_pass(const uint32_t *src, uint32_t *dst, size_t n, int pass, uint32_t *hist,

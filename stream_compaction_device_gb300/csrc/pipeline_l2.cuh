@@ -507,17 +507,15 @@ struct ScanPolicy {
         v = op(op(v0, v1), op(v2, v3));
     }
     __device__ static void after_reduce(const Args &, unsigned, unsigned) {}
-    template <class Release>
-    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
-                                       int warp, int lane, Release &release)
+    // This warp's rows of the consumed tile, from the B buffer (elements past
+    // the bulk copy from global memory; past n the identity).
+    __device__ static void load_x(const Args &a, const ConsumeTile<S> &ct, int warp, int lane, S (&x)[VECS][4])
     {
-        const Op op;
         const unsigned t = ct.tile;
         const size_t base = static_cast<size_t>(t) * kTile;
         const int wbase = warp * kWarpItems;
         const S *buf = reinterpret_cast<const S *>(ct.buf);
         const unsigned cp = copied(a, t);
-        S x[VECS][4];
         if (cp == static_cast<unsigned>(kTile)) {
             const uint4 *b4 = reinterpret_cast<const uint4 *>(buf + wbase);
 #pragma unroll
@@ -537,7 +535,14 @@ struct ScanPolicy {
                     x[q][j] = (e < cp) ? buf[e] : ((base + e < a.n) ? a.in[base + e] : Op::identity());
                 }
         }
-        release();   // the tile is in registers now
+    }
+    // Scans the rows in place (inclusive or exclusive, the tile's prefix
+    // applied); returns the tile's own total.  Contains the consume group's
+    // barrier.
+    __device__ static S scan_x(const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1, int warp, int lane,
+                               S (&x)[VECS][4])
+    {
+        const Op op;
         S tt[VECS];
 #pragma unroll
         for (int q = 0; q < VECS; ++q) tt[q] = op(op(x[q][0], x[q][1]), op(x[q][2], x[q][3]));
@@ -561,8 +566,14 @@ struct ScanPolicy {
                 }
             }
         }
-        if (base + kTile <= a.n) {
-            uint4 *o4 = reinterpret_cast<uint4 *>(a.out + base + wbase);
+        return total;
+    }
+    __device__ static void store_x(S *out, size_t n, unsigned t, int warp, int lane, const S (&x)[VECS][4])
+    {
+        const size_t base = static_cast<size_t>(t) * kTile;
+        const int wbase = warp * kWarpItems;
+        if (base + kTile <= n) {
+            uint4 *o4 = reinterpret_cast<uint4 *>(out + base + wbase);
 #pragma unroll
             for (int q = 0; q < VECS; ++q) {
                 const uint4 v = make_uint4(to_bits(x[q][0]), to_bits(x[q][1]), to_bits(x[q][2]), to_bits(x[q][3]));
@@ -577,9 +588,19 @@ struct ScanPolicy {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const size_t e = base + wbase + static_cast<size_t>((q * 32 + lane) * 4 + j);
-                    if (e < a.n) a.out[e] = x[q][j];
+                    if (e < n) out[e] = x[q][j];
                 }
         }
+    }
+    template <class Release>
+    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
+                                       int warp, int lane, Release &release)
+    {
+        S x[VECS][4];
+        load_x(a, ct, warp, lane, x);
+        release();   // the tile is in registers now
+        scan_x(ct, wbuf0, wbuf1, warp, lane, x);
+        store_x(a.out, a.n, ct.tile, warp, lane, x);
         return 1;   // one warp-totals buffer used
     }
 };

@@ -6,17 +6,29 @@
 
 namespace devscan {
 
+// Work a scan kernel may do on each finished tile besides storing it.
+struct NoEpilogue {
+    struct Args {};
+    static constexpr bool kActive = false;
+    template <class S, int VECS>
+    __device__ static void tile(const Args &, const S (&)[VECS][4], bool, S, int, int)
+    {
+    }
+};
+
 // ---------------------------------------------------------------------------
 // Single-pass scan: one tile per block.
 // ---------------------------------------------------------------------------
 // LB: status words per lane of a look-back round trip; MINB: resident blocks
-// per SM the register allocation must allow.
+// per SM the register allocation must allow; EPI: per-tile epilogue (it sees
+// the scanned rows, whether the tile is the last one, and the tile's
+// inclusive prefix).  With an active epilogue a null `out` skips the store.
 template <class Op, int THREADS, int VECS, bool INCLUSIVE, bool ALIGNED, bool TICKETS,
-          int LB = kLookbackPerLane, int MINB = 1, bool TWO_LEVEL = false>
+          int LB = kLookbackPerLane, int MINB = 1, bool TWO_LEVEL = false, class EPI = NoEpilogue>
 __global__ void __launch_bounds__(THREADS, MINB)
 scan_lookback_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,
                      unsigned num_tiles, unsigned long long *status, DevState *st, unsigned capacity,
-                     unsigned spin_limit)
+                     unsigned spin_limit, typename EPI::Args epi = typename EPI::Args{})
 {
     using S = typename Op::S;
     constexpr int NWARPS = THREADS / 32;
@@ -91,6 +103,10 @@ scan_lookback_kernel(const typename Op::S *__restrict__ in, typename Op::S *__re
                 cur = op(cur, v);
             }
         }
+    }
+    if (EPI::kActive) {
+        EPI::template tile<S, VECS>(epi, x, tile == num_tiles - 1, op(s_prefix, tile_total), tid, lane);
+        if (out == nullptr) return;
     }
     store_rows<S, VECS, ALIGNED>(out, warp_base, n, lane, full, x);
 }

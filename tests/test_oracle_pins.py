@@ -195,6 +195,15 @@ def pin_brackets(o, golden):
     for s, want in cases.items():
         x = np.array([1 if c == "(" else -1 for c in s], dtype=np.int32)
         assert o.bracket_flags(o.scan(x, "add", True)) == want, s
+    # exhaustive: among the 2^L sequences of L brackets exactly the Catalan
+    # number C_{L/2} are balanced (Dyck words), and none when L is odd
+    catalan = {0: 1, 2: 1, 4: 2, 6: 5, 8: 14, 10: 42, 12: 132}
+    for length in range(13):
+        balanced = 0
+        for code in range(1 << length):
+            x = np.array([1 if (code >> i) & 1 else -1 for i in range(length)], dtype=np.int32)
+            balanced += o.bracket_flags(o.scan(x, "add", True)) == (False, False)
+        assert balanced == catalan.get(length, 0), length
 
 
 PINS = [pin_worked_example, pin_brute_force, pin_relation, pin_closed_forms,
