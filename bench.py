@@ -329,6 +329,12 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
     out["bracket_check_2^28"] = row(n, med, 4 * n)
     med, _ = time_events(lambda: ds.bracket_scan(d_in, out=d_out, result=res), reps, 3)
     out["bracket_scan_2^28"] = row(n, med, 8 * n)
+    # the same array negated: 98% of its running sums are negative, so most
+    # warps find a negative value (the flag store must not queue up)
+    d_in.neg_()
+    med, _ = time_events(lambda: ds.bracket_scan(d_in, out=d_out, result=res), reps, 3)
+    out["bracket_scan_2^28_mostly_negative"] = row(n, med, 8 * n)
+    d_in.neg_()
     del d_in
     xm = torch.from_numpy(wl.max_values(n)).cuda()
     med, _ = time_events(lambda: ds.scan_inclusive(xm, d_out, op="max"), reps, 3)

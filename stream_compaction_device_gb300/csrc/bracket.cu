@@ -4,8 +4,9 @@
 // one scan answers two questions -- a negative running sum means a surplus
 // ')', a nonzero final sum means the brackets do not pair up.  Here both
 // answers come out of the scan's own pass: every consumed tile tests its
-// scanned values for a negative one (a warp vote, then one plain store of 1
-// into result[0]) and the last tile writes the final sum into result[1].  The
+// scanned values for a negative one (a warp vote; a warp that finds one
+// stores 1 into result[0], at most once per launch) and the last tile writes
+// the final sum into result[1].  The
 // scanned array itself is stored only when the caller asks for it, so the
 // check alone reads the input once (4 bytes per element) and writes nothing
 // else.
@@ -22,16 +23,22 @@ namespace {
 // result[0] = 1 when any value of these scanned rows is negative (int32);
 // the thread holding tid 0 of the last tile writes result[1].  Rows padded
 // past n repeat the last inclusive value, so padding changes neither answer.
+// `marked` (warp-uniform) remembers that this warp has stored the flag
+// already: all warps storing to one word on every tile would queue up at its
+// L2 slice.
 template <int VECS>
 __device__ __forceinline__ void bracket_mark(int32_t *result, const uint32_t (&x)[VECS][4], bool last_tile,
-                                             uint32_t incl_end, int tid, int lane)
+                                             uint32_t incl_end, int tid, int lane, unsigned &marked)
 {
     int32_t lo = 0;
 #pragma unroll
     for (int q = 0; q < VECS; ++q)
 #pragma unroll
         for (int j = 0; j < 4; ++j) lo = min(lo, static_cast<int32_t>(x[q][j]));
-    if (__any_sync(kFullMask, lo < 0) && lane == 0) result[0] = 1;
+    if (marked == 0 && __any_sync(kFullMask, lo < 0)) {
+        if (lane == 0) result[0] = 1;
+        marked = 1;
+    }
     if (last_tile && tid == 0) result[1] = static_cast<int32_t>(incl_end);
 }
 
@@ -44,7 +51,8 @@ struct BracketEpilogue {
     template <class S, int VECS>
     __device__ static void tile(const Args &e, const S (&x)[VECS][4], bool last_tile, S incl_end, int tid, int lane)
     {
-        bracket_mark<VECS>(e.result, x, last_tile, incl_end, tid, lane);
+        unsigned marked = 0;   // one tile per block: nothing to remember
+        bracket_mark<VECS>(e.result, x, last_tile, incl_end, tid, lane, marked);
     }
 };
 
@@ -64,7 +72,8 @@ struct BracketPolicy : BracketBase {
         load_x(a, ct, warp, lane, x);
         release();   // the tile is in registers now
         const uint32_t total = scan_x(ct, wbuf0, wbuf1, warp, lane, x);
-        bracket_mark<VECS>(a.result, x, ct.tile == a.num_tiles - 1, ct.prefix + total, warp * 32 + lane, lane);
+        bracket_mark<VECS>(a.result, x, ct.tile == a.num_tiles - 1, ct.prefix + total, warp * 32 + lane, lane,
+                           *ct.warp_state);
         if (a.out != nullptr) store_x(a.out, a.n, ct.tile, warp, lane, x);
         return 1;
     }

@@ -111,6 +111,7 @@ struct ConsumeTile {
     S aggregate;        // the tile's own aggregate (from pass A)
     unsigned char *buf; // the B buffer (P::kBBytes bytes)
     unsigned round;     // alternates the warp-totals buffers
+    unsigned *warp_state;   // per-warp word kept across the block's tiles (0 at start)
 };
 
 template <class P>
@@ -411,6 +412,7 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
 
     // ----------------------------------------------------------- consume group
     unsigned round = 0;
+    unsigned warp_state = 0;
     for (unsigned i = 0;; ++i) {
         const unsigned b = i % SB, kb = i / SB;
         const bool landed = mbar_wait(&ctrl->b_full[b], kb & 1u, wait_limit);
@@ -427,6 +429,7 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
         ct.aggregate = from_bits<S>(ctrl->rec_agg[r]);
         ct.buf = bbuf + static_cast<size_t>(b) * P::kBBytes;
         ct.round = round;
+        ct.warp_state = &warp_state;
         // release(): the B buffer and the record are no longer needed
         auto release = [&]() {
             __syncwarp();
