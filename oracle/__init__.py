@@ -11,7 +11,8 @@ Pages followed (cited per routine in ``oracle.c``):
 
 * geek-doc.cn "并行前缀和 scan: Hillis-Steele、Blelloch 与 warp shuffle 三种写法",
   section 一 -- inclusive/exclusive scan, compaction, radix split, brackets;
-* lpnh.cn/news/2866224 "并行扫描 Scan/Prefix Sum", sections 2.1, 2.2, 3.3, 4.1;
+* lpnh.cn/news/2866224 "并行扫描 Scan/Prefix Sum", sections 2.1, 2.2, 3.3, 4.1,
+  7.2 (segmented scan);
 * pgsm.cn/news/414823 "SIMT数据依赖与并行前缀和", sections 4.1-4.2.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against the
@@ -63,8 +64,14 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, sz, i, i]
             fn.restype = i
+        for name in ("oracle_segscan_i32", "oracle_segscan_u32", "oracle_segscan_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, sz, i, i]
+            fn.restype = i
         lib.oracle_abs_prefix_f32.argtypes = [vp, vp, sz]
         lib.oracle_abs_prefix_f32.restype = None
+        lib.oracle_seg_abs_prefix_f32.argtypes = [vp, vp, vp, sz]
+        lib.oracle_seg_abs_prefix_f32.restype = None
         lib.oracle_compact_i32.argtypes = [vp, vp, vp, sz]
         lib.oracle_compact_i32.restype = ctypes.c_int64
         lib.oracle_split_bit_u32.argtypes = [vp, vp, i, sz]
@@ -115,6 +122,42 @@ def scan(x, op: str = "add", inclusive: bool = True) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"operator {op!r} is not defined for {x.dtype}")
     return y
+
+
+def segscan(x, heads, op: str = "add", inclusive: bool = True) -> np.ndarray:
+    """Serial segmented scan: a nonzero ``heads[i]`` starts a new segment at
+    i (element 0 always starts one) and the accumulator restarts from the
+    operator's identity there.  Types and precision as :func:`scan`."""
+    x = np.ascontiguousarray(np.asarray(x))
+    heads = np.ascontiguousarray(np.asarray(heads, dtype=np.uint8))
+    if heads.size != x.size:
+        raise ValueError("x and heads differ in length")
+    code = OPS[op]
+    lib = _load()
+    if x.dtype == np.int32:
+        y = np.empty_like(x)
+        rc = lib.oracle_segscan_i32(_ptr(x), _ptr(heads), _ptr(y), x.size, code, int(inclusive))
+    elif x.dtype == np.uint32:
+        y = np.empty_like(x)
+        rc = lib.oracle_segscan_u32(_ptr(x), _ptr(heads), _ptr(y), x.size, code, int(inclusive))
+    elif x.dtype == np.float32:
+        y = np.empty(x.shape, dtype=np.float64)
+        rc = lib.oracle_segscan_f32(_ptr(x), _ptr(heads), _ptr(y), x.size, code, int(inclusive))
+    else:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    if rc != 0:
+        raise ValueError(f"operator {op!r} is not defined for {x.dtype}")
+    return y
+
+
+def seg_abs_prefix(x, heads) -> np.ndarray:
+    """fp64 running sum of |x_j| over the segment of i, j <= i: the fp32
+    tolerance scale of the segmented scan."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    heads = np.ascontiguousarray(heads, dtype=np.uint8)
+    s = np.empty(x.shape, dtype=np.float64)
+    _load().oracle_seg_abs_prefix_f32(_ptr(x), _ptr(heads), _ptr(s), x.size)
+    return s
 
 
 def abs_prefix(x) -> np.ndarray:

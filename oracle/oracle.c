@@ -143,6 +143,93 @@ void oracle_abs_prefix_f32(const float *x, double *s, size_t n)
     }
 }
 
+/* ---- segmented scan --------------------------------------------------------
+ * P2 section 7.2 names the segmented scan as the building block for sparse
+ * data.  Its definition: a nonzero head flag heads[i] starts a new segment at
+ * i (element 0 always starts one), and each segment is scanned on its own --
+ * the accumulator returns to the operator's identity at every segment start.
+ * Operators, identities and fp32 precision as the plain scans above. */
+int oracle_segscan_i32(const int32_t *x, const uint8_t *heads, int32_t *y, size_t n, int op, int inclusive)
+{
+    if (op != ORACLE_ADD && op != ORACLE_MAX && op != ORACLE_XOR) return -1;
+    const uint32_t id = (op == ORACLE_MAX) ? (uint32_t)INT32_MIN : 0u;
+    uint32_t acc = id;
+    for (size_t i = 0; i < n; ++i) {
+        if (heads[i] != 0) acc = id;
+        uint32_t xi = (uint32_t)x[i];
+        if (inclusive) {
+            acc = op_i32(op, acc, xi);
+            y[i] = (int32_t)acc;
+        } else {
+            y[i] = (int32_t)acc;
+            acc = op_i32(op, acc, xi);
+        }
+    }
+    return 0;
+}
+
+int oracle_segscan_u32(const uint32_t *x, const uint8_t *heads, uint32_t *y, size_t n, int op, int inclusive)
+{
+    if (op != ORACLE_ADD && op != ORACLE_MAX && op != ORACLE_XOR) return -1;
+    uint32_t acc = 0u;
+    for (size_t i = 0; i < n; ++i) {
+        if (heads[i] != 0) acc = 0u;
+        if (inclusive) {
+            acc = op_u32(op, acc, x[i]);
+            y[i] = acc;
+        } else {
+            y[i] = acc;
+            acc = op_u32(op, acc, x[i]);
+        }
+    }
+    return 0;
+}
+
+int oracle_segscan_f32(const float *x, const uint8_t *heads, double *y, size_t n, int op, int inclusive)
+{
+    if (op == ORACLE_ADD) {
+        double acc = 0.0;
+        for (size_t i = 0; i < n; ++i) {
+            if (heads[i] != 0) acc = 0.0;
+            if (inclusive) {
+                acc += (double)x[i];
+                y[i] = acc;
+            } else {
+                y[i] = acc;
+                acc += (double)x[i];
+            }
+        }
+        return 0;
+    }
+    if (op == ORACLE_MAX) {
+        float acc = -INFINITY;
+        for (size_t i = 0; i < n; ++i) {
+            if (heads[i] != 0) acc = -INFINITY;
+            if (inclusive) {
+                acc = fmaxf(acc, x[i]);
+                y[i] = (double)acc;
+            } else {
+                y[i] = (double)acc;
+                acc = fmaxf(acc, x[i]);
+            }
+        }
+        return 0;
+    }
+    return -1;
+}
+
+/* Running sum of |x[j]| over the segment of i up to i, in double: the scale
+ * of the fp32 tolerance of the segmented scan. */
+void oracle_seg_abs_prefix_f32(const float *x, const uint8_t *heads, double *s, size_t n)
+{
+    double acc = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        if (heads[i] != 0) acc = 0.0;
+        acc += fabs((double)x[i]);
+        s[i] = acc;
+    }
+}
+
 /* ---- stream compaction -----------------------------------------------------
  * P2 section 4.1 and P3 section 4.1: keep in[i] when its flag is set, in
  * input order; the number kept is the count.  Returns the count. */

@@ -187,6 +187,79 @@ def pin_sort(o, golden):
         assert np.array_equal(o.sort_lsd(k), np.sort(k))
 
 
+def _fold_py(vals, op, dtype):
+    """Direct fold in Python integers / fractions (independent of the C
+    oracle): add wraps modulo 2^32 for the integer types."""
+    if dtype == np.float32:
+        if op == "add":
+            return float(sum(Fraction(float(v)) for v in vals))
+        return float(max((float(v) for v in vals), default=float("-inf")))
+    if op == "add":
+        r = sum(int(v) for v in vals) % 2**32
+    elif op == "xor":
+        r = reduce(lambda a, b: a ^ b, (int(v) % 2**32 for v in vals), 0)
+    else:
+        r = max((int(v) for v in vals), default=(-2**31 if dtype == np.int32 else 0))
+        r %= 2**32
+    if dtype == np.int32 and r >= 2**31:
+        r -= 2**32
+    return r
+
+
+def pin_segmented(o, golden):
+    """lpnh.cn section 7.2 (segmented scan): a head restarts the fold at the
+    identity.  Pinned by the hand-worked fixture, the two degenerate flag
+    patterns, brute-force folds of each element's own segment, and the
+    concatenation of plain scans of the segments."""
+    g = golden("segmented.txt")
+    x = np.array(g["x"], dtype=np.int32)
+    h = np.array(g["heads"], dtype=np.uint8)
+    assert o.segscan(x, h, "add", True).tolist() == g["inclusive"]
+    assert o.segscan(x, h, "add", False).tolist() == g["exclusive"]
+    assert o.segscan(x, h, "max", True).tolist() == g["max_inclusive"]
+    h0 = np.array(g["heads_no_first"], dtype=np.uint8)
+    assert o.segscan(x, h0, "add", True).tolist() == g["inclusive"]
+    rng = np.random.default_rng(17)
+    for dtype in (np.int32, np.uint32, np.float32):
+        for op in ("add", "max", "xor"):
+            if dtype == np.float32 and op == "xor":
+                continue
+            for n in (1, 2, 7, 33, 64):
+                if dtype == np.float32:
+                    xs = rng.integers(-50, 50, n).astype(np.float32)   # exact in fp64
+                elif dtype == np.int32:
+                    xs = rng.integers(-2**31, 2**31, n, dtype=np.int64).astype(np.int32)
+                else:
+                    xs = rng.integers(0, 2**32, n, dtype=np.uint64).astype(np.uint32)
+                hs = (rng.random(n) < 0.3).astype(np.uint8)
+                for inclusive in (True, False):
+                    got = o.segscan(xs, hs, op, inclusive)
+                    for i in range(n):
+                        start = max([j for j in range(i + 1) if hs[j]] + [0])
+                        seg = xs[start:i + 1] if inclusive else xs[start:i]
+                        assert got[i] == _fold_py(seg, op, dtype), (dtype, op, inclusive, n, i)
+                # no heads: the plain scan; a head everywhere: x itself / the identity
+                assert np.array_equal(o.segscan(xs, np.zeros(n, np.uint8), op, True), o.scan(xs, op, True))
+                ones = np.ones(n, np.uint8)
+                assert np.array_equal(o.segscan(xs, ones, op, True).astype(np.float64), xs.astype(np.float64))
+                ident = o.identity(op, dtype)
+                assert np.all(o.segscan(xs, ones, op, False) == ident)
+    # concatenation of independent plain scans, on a longer array
+    xs = rng.integers(-1000, 1000, 5000).astype(np.int32)
+    hs = (rng.random(5000) < 0.01).astype(np.uint8)
+    starts = [0] + [int(j) for j in np.nonzero(hs)[0] if j > 0] + [5000]
+    for inclusive in (True, False):
+        parts = [o.scan(xs[a:b], "add", inclusive) for a, b in zip(starts[:-1], starts[1:])]
+        assert np.array_equal(o.segscan(xs, hs, "add", inclusive), np.concatenate(parts))
+    # the fp32 tolerance scale restarts with the segments too
+    xf = rng.standard_normal(300).astype(np.float32)
+    hf = (rng.random(300) < 0.05).astype(np.uint8)
+    s = o.seg_abs_prefix(xf, hf)
+    for i in (0, 17, 150, 299):
+        start = max([j for j in range(i + 1) if hf[j]] + [0])
+        assert math.isclose(s[i], float(sum(Fraction(abs(float(v))) for v in xf[start:i + 1])), rel_tol=1e-15)
+
+
 def pin_brackets(o, golden):
     """geek-doc.cn section 一: '(' = +1, ')' = -1; a negative prefix means a
     surplus ')', a nonzero total means unbalanced."""
@@ -208,7 +281,7 @@ def pin_brackets(o, golden):
 
 PINS = [pin_worked_example, pin_brute_force, pin_relation, pin_closed_forms,
         pin_identities, pin_f32_exact, pin_compaction, pin_split, pin_sort,
-        pin_brackets]
+        pin_brackets, pin_segmented]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -306,7 +379,8 @@ def test_restatements_agree_on_random():
 # --------------------------------------------------------------------------
 def _mutant(**over):
     base = {name: getattr(oracle, name) for name in
-            ("scan", "compact", "split_bit", "sort_lsd", "bracket_flags", "abs_prefix")}
+            ("scan", "compact", "split_bit", "sort_lsd", "bracket_flags", "abs_prefix", "segscan",
+             "seg_abs_prefix", "identity")}
     base.update(over)
     return types.SimpleNamespace(**base)
 
@@ -383,6 +457,29 @@ def _brackets_final_only(incl):
     return False, unb
 
 
+def _seg_reset_after(x, heads, op="add", inclusive=True):
+    """Restarts one element late: the head element still joins the old
+    segment."""
+    h = np.asarray(heads, dtype=np.uint8)
+    shifted = np.concatenate([[1], h[:-1]]).astype(np.uint8) if h.size else h
+    return oracle.segscan(x, shifted, op, inclusive)
+
+
+def _seg_ignores_heads(x, heads, op="add", inclusive=True):
+    return oracle.scan(x, op, inclusive)
+
+
+def _seg_excl_carries_value(x, heads, op="add", inclusive=True):
+    """Exclusive form that leaves the previous segment's total at a head."""
+    y = oracle.segscan(x, heads, op, inclusive)
+    if not inclusive:
+        full = oracle.scan(x, op, False)
+        h = np.asarray(heads, dtype=np.uint8)
+        y = y.copy()
+        y[h != 0] = full[h != 0]
+    return y
+
+
 MUTANTS = {
     "inclusive/exclusive swapped": _mutant(scan=_swap_incl_excl),
     "exclusive starts at 0 for every op": _mutant(scan=_excl_zero_identity),
@@ -395,6 +492,9 @@ MUTANTS = {
     "split puts ones first": _mutant(split_bit=_split_ones_first),
     "sort misses the top bit": _mutant(sort_lsd=_sort_31_passes),
     "bracket check ignores negative prefixes": _mutant(bracket_flags=_brackets_final_only),
+    "segment restarts one element late": _mutant(segscan=_seg_reset_after),
+    "segmented scan ignores heads": _mutant(segscan=_seg_ignores_heads),
+    "exclusive segment start keeps the old total": _mutant(segscan=_seg_excl_carries_value),
 }
 
 
