@@ -346,7 +346,17 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
     med, _ = time_events(lambda: ds.scan_exclusive(xm, d_out), reps, 3)
     out["i32_add_exclusive_2^28_reduce_then_scan"] = row(n, med, 8 * n)
     ds.set_carry_mode(args.carry)
-    del xm, d_out
+    del xm
+    # segmented add at N = 2^28 (heads at rate 1/1024): 5 B read + 4 B written
+    sv, sh = wl.segmented(n)
+    dsv = torch.from_numpy(sv).cuda()
+    dsh = torch.from_numpy(sh).cuda()
+    del sv, sh
+    med, _ = time_events(lambda: ds.segmented_scan_inclusive(dsv, dsh, d_out), reps, 3)
+    out["segmented_i32_add_inclusive_2^28"] = row(n, med, 9 * n)
+    med, _ = time_events(lambda: ds.segmented_scan_exclusive(dsv, dsh, d_out), reps, 3)
+    out["segmented_i32_add_exclusive_2^28"] = row(n, med, 9 * n)
+    del dsv, dsh, d_out
 
     # compaction at N = 2^26
     nc = wl.N_COMPACT

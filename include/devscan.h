@@ -86,6 +86,35 @@ devscan_status scan_exclusive_f32(const float *in, float *out, size_t n,
                                   devscan_op op, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Segmented scans (P2 section 7.2 names the segmented scan for sparse data):
+ * heads[i] != 0 starts a new segment at i (element 0 always starts one) and
+ * every segment is scanned on its own, the running value returning to the
+ * operator's identity at each segment start:
+ *   inclusive  out[i] = in[s] (+) ... (+) in[i],
+ *   exclusive  out[i] = identity (+) in[s] (+) ... (+) in[i-1],
+ * with s the start of i's segment (exclusive: identity at every start).
+ *
+ *   in, out : device T[n], 4-byte aligned; out may equal in (in place),
+ *             otherwise the two must not overlap;
+ *   heads   : device uint8[n], nonzero = segment start; must not overlap out.
+ * Operators, identities, fp32 accuracy (per segment: |err_i| within
+ * 1e-5 * sum of |in[j]| over i's segment up to i), limits and errors as the
+ * scans above.  Traffic: 5 bytes read and 4 written per element.
+ * ------------------------------------------------------------------------- */
+devscan_status segmented_scan_inclusive_i32(const int32_t *in, const uint8_t *heads, int32_t *out,
+                                            size_t n, devscan_op op, cudaStream_t stream);
+devscan_status segmented_scan_inclusive_u32(const uint32_t *in, const uint8_t *heads, uint32_t *out,
+                                            size_t n, devscan_op op, cudaStream_t stream);
+devscan_status segmented_scan_inclusive_f32(const float *in, const uint8_t *heads, float *out,
+                                            size_t n, devscan_op op, cudaStream_t stream);
+devscan_status segmented_scan_exclusive_i32(const int32_t *in, const uint8_t *heads, int32_t *out,
+                                            size_t n, devscan_op op, cudaStream_t stream);
+devscan_status segmented_scan_exclusive_u32(const uint32_t *in, const uint8_t *heads, uint32_t *out,
+                                            size_t n, devscan_op op, cudaStream_t stream);
+devscan_status segmented_scan_exclusive_f32(const float *in, const uint8_t *heads, float *out,
+                                            size_t n, devscan_op op, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Stream compaction (P1 section 一; P2 section 4.1; P3 sections 4.1-4.2):
  * out[0 .. *count) receives, in input order, every in[i] whose flags[i] is
  * nonzero; *count is the number kept.  Each kept element's slot is the

@@ -15,7 +15,7 @@ from . import _lib
 from ._lib import DevscanError, OPS, load
 
 __all__ = ["scan_inclusive", "scan_exclusive", "compact", "split_bit", "radix_sort", "radix_sort_digits", "scan_host",
-           "compact_greater", "bracket_scan",
+           "compact_greater", "bracket_scan", "segmented_scan_inclusive", "segmented_scan_exclusive",
            "device_status", "set_carry_mode", "stream_release", "selftest_stalled_wait", "DevscanError",
            "load"]
 
@@ -64,6 +64,39 @@ def scan_exclusive(x: torch.Tensor, out: torch.Tensor | None = None, op: str = "
                    as_uint32: bool = False) -> torch.Tensor:
     """z[i] = x[0] op ... op x[i-1]; z[0] = identity of op."""
     return _scan("exclusive", x, out, op, stream, "u32" if as_uint32 else None)
+
+
+def _segscan(direction: str, x: torch.Tensor, heads: torch.Tensor, out, op: str, stream, dtype_override=None):
+    _check_cuda(x, "x")
+    _check_cuda(heads, "heads")
+    suffix = dtype_override or _SUFFIX.get(x.dtype)
+    if suffix is None:
+        raise TypeError(f"unsupported dtype {x.dtype} (int32, uint32, float32)")
+    if heads.dtype != torch.uint8 or heads.numel() != x.numel():
+        raise ValueError("heads must be a uint8 tensor of x's length")
+    if out is None:
+        out = torch.empty_like(x)
+    _check_cuda(out, "out")
+    if out.numel() != x.numel() or out.dtype != x.dtype:
+        raise ValueError("out must match x in size and dtype")
+    name = f"segmented_scan_{direction}_{suffix}"
+    _lib.check(getattr(load(), name)(x.data_ptr(), heads.data_ptr(), out.data_ptr(), x.numel(), OPS[op],
+                                     _stream_handle(stream)), name)
+    return out
+
+
+def segmented_scan_inclusive(x: torch.Tensor, heads: torch.Tensor, out: torch.Tensor | None = None,
+                             op: str = "add", stream=None, as_uint32: bool = False) -> torch.Tensor:
+    """Inclusive scan restarted at every nonzero ``heads[i]`` (element 0
+    always starts a segment)."""
+    return _segscan("inclusive", x, heads, out, op, stream, "u32" if as_uint32 else None)
+
+
+def segmented_scan_exclusive(x: torch.Tensor, heads: torch.Tensor, out: torch.Tensor | None = None,
+                             op: str = "add", stream=None, as_uint32: bool = False) -> torch.Tensor:
+    """Exclusive scan restarted at every nonzero ``heads[i]``: the identity
+    at each segment start."""
+    return _segscan("exclusive", x, heads, out, op, stream, "u32" if as_uint32 else None)
 
 
 def compact(values: torch.Tensor, flags: torch.Tensor, out: torch.Tensor | None = None,

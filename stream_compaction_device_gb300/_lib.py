@@ -19,6 +19,8 @@ STATUS = {0: "DEVSCAN_OK", 1: "DEVSCAN_ERR_INVALID", 2: "DEVSCAN_ERR_UNSUPPORTED
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NOMEM = range(6)
 
 SCAN_SYMBOLS = [f"scan_{d}_{t}" for d in ("inclusive", "exclusive") for t in ("i32", "u32", "f32")]
+SEGSCAN_SYMBOLS = tuple(f"segmented_scan_{d}_{t}" for d in ("inclusive", "exclusive")
+                        for t in ("i32", "u32", "f32"))
 
 
 class DevscanError(RuntimeError):
@@ -45,6 +47,10 @@ def load() -> ctypes.CDLL:
         for name in SCAN_SYMBOLS:
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, sz, i, vp]
+            fn.restype = i
+        for name in SEGSCAN_SYMBOLS:
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, sz, i, vp]
             fn.restype = i
         lib.compact_i32.argtypes = [vp, vp, vp, vp, sz, vp]
         lib.compact_i32.restype = i

@@ -146,6 +146,24 @@ devscan_status scan_common(ElemType type, bool inclusive, const void *in, void *
                                  kSpinLimit, stream));
 }
 
+devscan_status segscan_common(ElemType type, bool inclusive, const void *in, const uint8_t *heads, void *out,
+                              size_t n, devscan_op op, cudaStream_t stream)
+{
+    if (op != DEVSCAN_OP_ADD && op != DEVSCAN_OP_MAX && op != DEVSCAN_OP_XOR) return DEVSCAN_ERR_INVALID;
+    if (type == ElemType::F32 && op == DEVSCAN_OP_XOR) return DEVSCAN_ERR_UNSUPPORTED;
+    if (n == 0) return DEVSCAN_OK;
+    if (in == nullptr || heads == nullptr || out == nullptr) return DEVSCAN_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(in) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+        return DEVSCAN_ERR_INVALID;
+    if (n > static_cast<size_t>(0xffffffffu) * kScanTile) return DEVSCAN_ERR_INVALID;
+    if (overlaps(heads, n, out, n * 4) || (in != out && overlaps(in, n * 4, out, n * 4))) return DEVSCAN_ERR_INVALID;
+    Workspace ws;
+    const devscan_status st = acquire(stream, tiles_for(n, kScanTile), &ws);
+    if (st != DEVSCAN_OK) return st;
+    return from_cuda(launch_segscan(type, static_cast<int>(op), inclusive, in, heads, out, n,
+                                    g_carry_mode.load(std::memory_order_relaxed), ws, kSpinLimit, stream));
+}
+
 }  // namespace
 }  // namespace devscan
 
@@ -176,6 +194,37 @@ devscan_status scan_exclusive_u32(const uint32_t *in, uint32_t *out, size_t n, d
 devscan_status scan_exclusive_f32(const float *in, float *out, size_t n, devscan_op op, cudaStream_t stream)
 {
     return scan_common(ElemType::F32, false, in, out, n, op, stream);
+}
+
+devscan_status segmented_scan_inclusive_i32(const int32_t *in, const uint8_t *heads, int32_t *out, size_t n,
+                                            devscan_op op, cudaStream_t stream)
+{
+    return segscan_common(ElemType::I32, true, in, heads, out, n, op, stream);
+}
+devscan_status segmented_scan_inclusive_u32(const uint32_t *in, const uint8_t *heads, uint32_t *out, size_t n,
+                                            devscan_op op, cudaStream_t stream)
+{
+    return segscan_common(ElemType::U32, true, in, heads, out, n, op, stream);
+}
+devscan_status segmented_scan_inclusive_f32(const float *in, const uint8_t *heads, float *out, size_t n,
+                                            devscan_op op, cudaStream_t stream)
+{
+    return segscan_common(ElemType::F32, true, in, heads, out, n, op, stream);
+}
+devscan_status segmented_scan_exclusive_i32(const int32_t *in, const uint8_t *heads, int32_t *out, size_t n,
+                                            devscan_op op, cudaStream_t stream)
+{
+    return segscan_common(ElemType::I32, false, in, heads, out, n, op, stream);
+}
+devscan_status segmented_scan_exclusive_u32(const uint32_t *in, const uint8_t *heads, uint32_t *out, size_t n,
+                                            devscan_op op, cudaStream_t stream)
+{
+    return segscan_common(ElemType::U32, false, in, heads, out, n, op, stream);
+}
+devscan_status segmented_scan_exclusive_f32(const float *in, const uint8_t *heads, float *out, size_t n,
+                                            devscan_op op, cudaStream_t stream)
+{
+    return segscan_common(ElemType::F32, false, in, heads, out, n, op, stream);
 }
 
 devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out, int32_t *count, size_t n,

@@ -340,15 +340,21 @@ __device__ typename Op::S lookback(const Op &op, const unsigned long long *statu
 // Returns the tile's exclusive prefix; the caller publishes the tile's own
 // status words, this function the group word.
 // ---------------------------------------------------------------------------
+// agg_inclusive: the tile's own status is already inclusive with value agg
+// (a segmented scan's tile that contains a segment head): a group-closing
+// tile then publishes agg itself as the group's inclusive word.
 template <class Op>
 __device__ typename Op::S lookback2(const Op &op, const unsigned long long *status,
                                     unsigned long long *status2, unsigned tile, unsigned tag,
-                                    typename Op::S agg, unsigned *error, unsigned spin_limit, int lane)
+                                    typename Op::S agg, unsigned *error, unsigned spin_limit, int lane,
+                                    bool agg_inclusive = false)
 {
     using S = typename Op::S;
     const unsigned group = tile >> 5;
     const long long first = static_cast<long long>(group) << 5;
-    const bool closes_group = (tile & 31u) == 31u;
+    if (agg_inclusive && (tile & 31u) == 31u && lane == 0)
+        st_status(status2 + group, pack_status(tag, kFlagInclusive, to_bits(agg)));
+    const bool closes_group = !agg_inclusive && (tile & 31u) == 31u;
     bool gave_up = false;
 
     // level 1: this group's tiles first .. tile-1, lane j reading tile-1-j

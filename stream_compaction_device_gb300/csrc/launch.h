@@ -84,6 +84,10 @@ cudaError_t launch_compact_gt(const int32_t *in, int32_t threshold, int32_t *out
 cudaError_t launch_bracket(const int32_t *in, int32_t *out, int32_t *result, size_t n, int carry,
                            const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
+// Segmented scan: heads[i] != 0 starts a segment at i.
+cudaError_t launch_segscan(ElemType type, int op, bool inclusive, const void *in, const uint8_t *heads, void *out,
+                           size_t n, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
 // One 4-bit-digit LSD radix pass (digit `pass`, bits 4 pass .. 4 pass + 3)
 // from src to dst; `hist` holds radix_hist_words(n) words of scratch.
 cudaError_t launch_radix_pass(const uint32_t *src, uint32_t *dst, size_t n, int pass, uint32_t *hist,

@@ -103,6 +103,42 @@ __device__ __forceinline__ void group_scan(const Op &op, typename Op::S warp_tot
     group_total = __shfl_sync(kFullMask, v, NW - 1);
 }
 
+// A segmented policy (P::kSegmented) reports, per reduce warp, whether a
+// segment head lies in the warp's contiguous part of the tile (`extra`
+// nonzero) and folds only what follows the last head there; the kernel
+// combines the warps in order, and a tile with a head publishes its
+// aggregate as an inclusive prefix at once (nothing before the head can
+// change it).
+template <class P, class = void>
+struct IsSegmented {
+    static constexpr bool value = false;
+};
+template <class P>
+struct IsSegmented<P, decltype(void(P::kSegmented))> {
+    static constexpr bool value = P::kSegmented;
+};
+
+// Pass-A copies of tile t: P::a_copies when the policy has one (up to two
+// copies, as for pass B), else the single copy P::a_src / P::a_bytes.
+template <class P, class = void>
+struct PassACopies {
+    __device__ static void get(const typename P::Args &a, unsigned t, const void **src, unsigned *bytes,
+                               unsigned *off)
+    {
+        src[0] = P::a_src(a, t);
+        bytes[0] = P::a_bytes(a, t);
+        off[0] = 0;
+    }
+};
+template <class P>
+struct PassACopies<P, decltype(void(&P::a_copies))> {
+    __device__ static void get(const typename P::Args &a, unsigned t, const void **src, unsigned *bytes,
+                               unsigned *off)
+    {
+        P::a_copies(a, t, src, bytes, off);
+    }
+};
+
 // What the consume group gets for one tile.
 template <class S>
 struct ConsumeTile {
@@ -131,7 +167,7 @@ struct PipeShape {
         unsigned a_tile[SA], a_last[SA];
         unsigned b_tile[SB], b_rec[SB], b_last[SB];
         unsigned rec_tile[R];
-        uint32_t rec_agg[R], rec_prefix[R];
+        uint32_t rec_agg[R], rec_prefix[R], rec_head[R];
         uint32_t red[NR], red_extra[NR];
         uint32_t wtot[2][NS];
         unsigned tag;
@@ -155,6 +191,7 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
     using S = typename Op::S;
     using G = PipeShape<P>;
     constexpr int NS = G::NS, NR = G::NR, R = G::R, SA = G::SA, SB = G::SB;
+    constexpr bool SEG = IsSegmented<P>::value;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *abuf = smem + G::kABase;
     unsigned char *bbuf = smem + G::kBBase;
@@ -245,17 +282,22 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 continue;
             }
             if (lane == 0) {
-                const unsigned bytes = P::a_bytes(args, t);
+                const void *src[2] = {nullptr, nullptr};
+                unsigned bytes[2] = {0, 0}, off[2] = {0, 0};
+                PassACopies<P>::get(args, t, src, bytes, off);
+                const unsigned total = bytes[0] + bytes[1];
                 ctrl->a_tile[a] = t;
-                if (bytes != 0) {
+                if (total != 0) {
                     ctrl->a_last[a] = ka;
-                    mbar_arrive_expect_tx(&ctrl->a_full[a], bytes);
-                    if (P::kAHint == kL2None)
-                        bulk_load(abuf + static_cast<size_t>(a) * P::kABytes, P::a_src(args, t), bytes,
-                                  &ctrl->a_full[a]);
-                    else
-                        bulk_load_hint(abuf + static_cast<size_t>(a) * P::kABytes, P::a_src(args, t), bytes,
-                                       &ctrl->a_full[a], pol);
+                    mbar_arrive_expect_tx(&ctrl->a_full[a], total);
+                    unsigned char *dst = abuf + static_cast<size_t>(a) * P::kABytes;
+                    for (int j = 0; j < 2; ++j) {
+                        if (bytes[j] == 0) continue;
+                        if (P::kAHint == kL2None)
+                            bulk_load(dst + off[j], src[j], bytes[j], &ctrl->a_full[a]);
+                        else
+                            bulk_load_hint(dst + off[j], src[j], bytes[j], &ctrl->a_full[a], pol);
+                    }
                 } else {
                     ctrl->a_last[a] = G::kNoCopy;
                     mbar_arrive(&ctrl->a_full[a]);
@@ -330,11 +372,12 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 break;
             }
             const S agg = from_bits<S>(ctrl->rec_agg[r]);
+            const bool head = SEG && ctrl->rec_head[r] != 0;   // status already inclusive
             S prefix = Op::identity();
             if (t != 0) {
                 prefix = lookback2<Op>(op, status, group_status(status, capacity), t, tag, agg, &st->error,
-                                       spin_limit, lane);
-                publish<Op>(status, t, tag, kFlagInclusive, op(prefix, agg), lane);
+                                       spin_limit, lane, head);
+                if (!head) publish<Op>(status, t, tag, kFlagInclusive, op(prefix, agg), lane);
             }
             if (lane == 0) {
                 ctrl->rec_prefix[r] = to_bits(prefix);
@@ -379,7 +422,7 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
             if (lane == 0) mbar_arrive(&ctrl->a_empty[a]);   // buffer read: free it
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
-            if (P::kHasExtra) extra = __reduce_add_sync(kFullMask, extra);
+            if (P::kHasExtra || SEG) extra = __reduce_add_sync(kFullMask, extra);
             if (lane == 0) {
                 ctrl->red[rw] = to_bits(v);
                 ctrl->red_extra[rw] = extra;
@@ -389,19 +432,37 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
             if (rtid == 0) {
                 S agg = from_bits<S>(ctrl->red[0]);
                 unsigned ex = ctrl->red_extra[0];
+                unsigned head = 0;
+                if (SEG) {
+                    // in order: a warp whose part holds a head restarts the fold
+                    agg = Op::identity();
 #pragma unroll
-                for (int w = 1; w < NR; ++w) {
-                    agg = op(agg, from_bits<S>(ctrl->red[w]));
-                    ex += ctrl->red_extra[w];
+                    for (int w = 0; w < NR; ++w) {
+                        const S vw = from_bits<S>(ctrl->red[w]);
+                        if (ctrl->red_extra[w] != 0) {
+                            agg = vw;
+                            head = 1;
+                        } else {
+                            agg = op(agg, vw);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int w = 1; w < NR; ++w) {
+                        agg = op(agg, from_bits<S>(ctrl->red[w]));
+                        ex += ctrl->red_extra[w];
+                    }
                 }
                 // publish first; a record (and so a look-back warp) is only
                 // claimed for the time the prefix takes to resolve
-                st_status(status + t, pack_status(tag, t == 0 ? kFlagInclusive : kFlagAggregate, to_bits(agg)));
+                st_status(status + t, pack_status(tag, (t == 0 || head) ? kFlagInclusive : kFlagAggregate,
+                                                  to_bits(agg)));
                 if (P::kHasExtra) P::after_reduce(args, t, ex);
                 if (kr > 0) freed = mbar_wait(&ctrl->rec_free[r], (kr - 1) & 1u, wait_limit);
                 if (!freed) atomicOr(&st->error, kErrTimeout);
                 ctrl->rec_tile[r] = t;
                 ctrl->rec_agg[r] = to_bits(agg);
+                ctrl->rec_head[r] = head;
                 mbar_arrive(&ctrl->rec_pending[r]);
             }
             // red[] free for the next tile; a timed-out record wait ends the group

@@ -15,7 +15,11 @@ the pages fix no generator, so the seeds are this library's convention):
   (the bracket sequence of geek-doc.cn section 一);
 * ``radix_keys``    -- uint32 uniform over [0, 2^32), N = 2^26, seed 4;
 * ``max_values``    -- int32 uniform over the whole range, N = 2^28, seed 5;
-* ``xor_values``    -- uint32 uniform over [0, 2^32), N = 2^28, seed 6.
+* ``xor_values``    -- uint32 uniform over [0, 2^32), N = 2^28, seed 6;
+* ``segmented``     -- int32 uniform in [0, 9] with segment heads drawn
+  independently with p = 1/1024 (mean segment length 1,024; element 0 a
+  head), N = 2^28, seed 7 (the pages give no segmented workload: the size
+  follows the operator sweep, the values the 65,536-element case).
 """
 from __future__ import annotations
 
@@ -77,6 +81,16 @@ def max_values(n: int = N_SWEEP, seed: int = 5) -> np.ndarray:
 
 def xor_values(n: int = N_SWEEP, seed: int = 6) -> np.ndarray:
     return full_range_u32(n, seed)
+
+
+def segmented(n: int = N_SWEEP, seed: int = 7, mean_len: int = 1024) -> tuple[np.ndarray, np.ndarray]:
+    """(values, heads): int32 digits and uint8 segment heads."""
+    rng = np.random.default_rng(seed)
+    values = rng.integers(0, 10, n, dtype=np.int32)
+    heads = (rng.random(n, dtype=np.float32) < np.float32(1.0 / mean_len)).astype(np.uint8)
+    if n:
+        heads[0] = 1
+    return values, heads
 
 
 def random_input(dtype, n: int, seed: int, op: str = "add") -> np.ndarray:
