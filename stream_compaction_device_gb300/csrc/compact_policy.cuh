@@ -10,11 +10,23 @@ namespace devscan {
 
 __device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t *p) { return __ldcs(p); }
 
-// Bit k set when byte k of f is nonzero.
+// Bit 7 of every nonzero byte of f (the other bits clear): a byte's low
+// seven bits plus 0x7f reach bit 7 exactly when they are nonzero, without
+// carrying into the next byte.
+__device__ __forceinline__ uint32_t nonzero_byte_tops(uint32_t f)
+{
+    return (f | ((f & 0x7f7f7f7fu) + 0x7f7f7f7fu)) & 0x80808080u;
+}
+
+// Number of nonzero bytes of f.
+__device__ __forceinline__ unsigned nonzero_bytes(uint32_t f) { return __popc(nonzero_byte_tops(f)); }
+
+// Bit k set when byte k of f is nonzero: the four byte flags (bits 0, 8, 16,
+// 24) are gathered into bits 21..24 by one multiply with 1 + 2^7 + 2^14 +
+// 2^21 (no two partial products share a bit, so nothing carries).
 __device__ __forceinline__ uint32_t nonzero_byte_mask(uint32_t f)
 {
-    return ((f & 0x000000ffu) ? 1u : 0u) | ((f & 0x0000ff00u) ? 2u : 0u) | ((f & 0x00ff0000u) ? 4u : 0u) |
-           ((f & 0xff000000u) ? 8u : 0u);
+    return ((nonzero_byte_tops(f) >> 7) * 0x00204081u) >> 21 & 0xfu;
 }
 
 // ---------------------------------------------------------------------------
@@ -25,45 +37,70 @@ __device__ __forceinline__ uint32_t nonzero_byte_mask(uint32_t f)
 // writes one contiguous run at the tile's prefix.  HBM traffic is the
 // algorithmic 5 bytes per element plus 4 per kept element.
 // ---------------------------------------------------------------------------
-constexpr unsigned kBarCompactStage = 8;
-
-// Second half of a compaction consume step, shared by both predicate forms:
-// ranks the kept elements (bit j of keep[q] keeps x[q][j]), stages them in
-// `stage` in phase with their destination (so the copy out is straight
-// 128-bit chunks; `stage` must hold the tile plus 3 words and must be free to
-// overwrite once the group scan's barrier has passed) and writes them as one
-// contiguous run at the tile's prefix.  The last tile also writes the count.
-template <int NS, int VECS>
-__device__ __forceinline__ void compact_write_tile(const uint32_t (&x)[VECS][4], const uint32_t (&keep)[VECS],
-                                                   const ConsumeTile<uint32_t> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
-                                                   int warp, int lane, uint32_t *stage, uint32_t *out,
-                                                   bool out_aligned, size_t n, int32_t *count, bool last_tile)
+// Second half of a compaction consume step, shared by both predicate forms,
+// run by one warp on its own part of the tile (bit j of keep[q] keeps
+// x[q][j]).  The warp's kept elements form one contiguous run of the output
+// starting at g0 (the tile's prefix plus the kept counts of the earlier parts,
+// from pass A), so the warp needs no other warp: it ranks its elements with
+// one scan of the four rows' counts packed into the bytes of a word (a row
+// holds at most 128), stages them in its private `stage` area (kWarpItems + 4
+// words, 16-byte aligned) in phase with their destination and copies the run
+// out in whole 128-bit chunks, only the two ragged ends element by element.
+template <int VECS>
+__device__ __forceinline__ void compact_write_warp(const uint32_t (&x)[VECS][4], const uint32_t (&keep)[VECS],
+                                                   size_t g0, int lane, uint32_t *stage, uint32_t *out,
+                                                   bool out_aligned, size_t n)
 {
-    constexpr int THREADS = NS * 32;
-    const AddU32 op;
-    uint32_t cnt[VECS];
+    static_assert(VECS == 4, "the four rows' counts share one word");
+    uint32_t packed = 0;
 #pragma unroll
-    for (int q = 0; q < VECS; ++q) cnt[q] = __popc(keep[q]);
-    uint32_t row_excl[VECS], warp_total;
-    warp_scan_rows<AddU32, VECS>(op, cnt, lane, row_excl, warp_total);
-    uint32_t warp_excl, total;
-    // the barrier inside also means every thread has read the buffer
-    group_scan<AddU32, NS>(op, warp_total, (ct.round & 1) ? wbuf1 : wbuf0, warp, lane, warp_excl, total);
-    const unsigned phase = out_aligned ? (ct.prefix & 3u) : 0u;
+    for (int q = 0; q < VECS; ++q) packed |= static_cast<uint32_t>(__popc(keep[q])) << (8 * q);
+    uint32_t inc = packed;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
+        if (lane >= d) inc += u;
+    }
+    const uint32_t excl = inc - packed, tot = __shfl_sync(kFullMask, inc, 31);
+    const unsigned phase = out_aligned ? static_cast<unsigned>(g0 & 3) : 0u;
+    uint32_t row_base = phase, count = 0;
 #pragma unroll
     for (int q = 0; q < VECS; ++q) {
-        uint32_t rank = phase + warp_excl + row_excl[q];
+        uint32_t rank = row_base + ((excl >> (8 * q)) & 0xffu);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             if ((keep[q] >> j) & 1u) stage[rank++] = x[q][j];
+        const uint32_t row_total = (tot >> (8 * q)) & 0xffu;
+        row_base += row_total;
+        count += row_total;
     }
-    named_sync(kBarCompactStage, THREADS);
-    const unsigned tid = static_cast<unsigned>(warp * 32 + lane);
+    __syncwarp();
     if (out_aligned)
-        write_run_direct<THREADS>(out, ct.prefix, total, stage, static_cast<int>(tid), n);
+        write_run_direct<32>(out, g0, count, stage, lane, n);
     else
-        write_run_scalar<THREADS>(out, ct.prefix, total, stage, 0, static_cast<int>(tid), n);
-    if (last_tile && tid == 0) *count = static_cast<int32_t>(ct.prefix + total);
+        write_run_scalar<32>(out, g0, count, stage, 0, lane, n);
+    __syncwarp();   // the area is read before the warp stages its next part
+}
+
+// Finishes a reduce warp's part counts: c[i] is this lane's count of part
+// rw + i * NR (each part's total is at most 2^15, so two parts share one
+// word's 16-bit halves and one warp reduction); lane 0 stores the parts and
+// returns their sum.
+template <int PPW, int NR>
+__device__ __forceinline__ unsigned store_part_counts(const unsigned (&c)[PPW], int rw, int lane, uint32_t *part)
+{
+    unsigned mine = 0;
+#pragma unroll
+    for (int i = 0; i < PPW; i += 2) {
+        uint32_t w = c[i] | ((i + 1 < PPW) ? (c[i + 1] << 16) : 0u);
+        w = __reduce_add_sync(kFullMask, w);
+        if (lane == 0) {
+            part[rw + i * NR] = w & 0xffffu;
+            if (i + 1 < PPW) part[rw + (i + 1) * NR] = w >> 16;
+        }
+        mine += (w & 0xffffu) + (w >> 16);
+    }
+    return mine;
 }
 
 template <int NS_, int NR_, int VECS_, int SA_, int SB_, int R_, int PREFETCH = 0>
@@ -79,6 +116,9 @@ struct CompactPolicy {
     static constexpr size_t kABytes = static_cast<size_t>(kTile);                // flags
     static constexpr size_t kBBytes = kValueBytes + static_cast<size_t>(kTile);  // values, then flags
     static constexpr bool kHasExtra = false;
+    static constexpr int kParts = NS_;                                          // one part per consume warp
+    static constexpr int kWarpStage = kWarpItems + 4;                           // words, 16-byte multiple
+    static constexpr size_t kScratchBytes = static_cast<size_t>(NS_) * kWarpStage * 4;
     struct Args {
         const uint32_t *in;
         const uint8_t *flags;
@@ -113,31 +153,53 @@ struct CompactPolicy {
         bytes[1] = flags_copied(a, t);
         off[1] = static_cast<unsigned>(kValueBytes);
     }
-    __device__ static void reduce(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int nthr, S &v,
-                                  unsigned &)
+    // pass A: the kept count of each consume warp's part (kWarpItems flags),
+    // one warp reduction per part; lane 0 of each reduce warp returns the
+    // sum of its parts (the kernel adds the lanes and the warps)
+    __device__ static void reduce_parts(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int,
+                                        S &v, uint32_t *part)
     {
-        const unsigned cp = flags_copied(a, t);
-        unsigned c = 0;
-        const uint4 *f4 = reinterpret_cast<const uint4 *>(abuf);
-        for (unsigned k = rtid; k < cp / 16; k += nthr) {
-            const uint4 q = f4[k];
-            c += __popc(nonzero_byte_mask(q.x)) + __popc(nonzero_byte_mask(q.y)) + __popc(nonzero_byte_mask(q.z)) +
-                 __popc(nonzero_byte_mask(q.w));
-        }
+        static_assert(NS_ % NR_ == 0 && kWarpItems / 16 % 32 == 0, "whole parts per reduce warp");
+        constexpr int PPW = NS_ / NR_, CH = kWarpItems / 16 / 32;   // parts per warp, 16-flag chunks per lane
+        const int lane = rtid & 31, rw = rtid >> 5;
+        const unsigned cp = flags_copied(a, t), len = tile_len(a, t);
         const size_t base = static_cast<size_t>(t) * kTile;
-        const unsigned len = tile_len(a, t);
-        for (unsigned e = cp + rtid; e < len; e += nthr) c += a.flags[base + e] != 0 ? 1u : 0u;
-        v = c;
+        const uint4 *f4 = reinterpret_cast<const uint4 *>(abuf);
+        unsigned c[PPW];
+        if (len == static_cast<unsigned>(kTile)) {
+#pragma unroll
+            for (int i = 0; i < PPW; ++i) {
+                c[i] = 0;
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    const uint4 q = f4[(rw + i * NR_) * (kWarpItems / 16) + k * 32 + lane];
+                    c[i] += nonzero_bytes(q.x) + nonzero_bytes(q.y) + nonzero_bytes(q.z) + nonzero_bytes(q.w);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < PPW; ++i) {
+                c[i] = 0;
+                for (int k = 0; k < CH; ++k) {
+                    const unsigned e = static_cast<unsigned>((rw + i * NR_) * kWarpItems + 16 * (k * 32 + lane));
+                    for (unsigned j = 0; j < 16; ++j)
+                        if (e + j < len)
+                            c[i] += ((e + j < cp ? abuf[e + j] : a.flags[base + e + j]) != 0) ? 1u : 0u;
+                }
+            }
+        }
+        const unsigned mine = store_part_counts<PPW, NR_>(c, rw, lane, part);
+        v = (lane == 0) ? mine : 0u;
     }
     __device__ static void after_reduce(const Args &, unsigned, unsigned) {}
     template <class Release>
-    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
-                                       int warp, int lane, Release &release)
+    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *, uint32_t *, int warp,
+                                       int lane, Release &release)
     {
         const unsigned t = ct.tile;
         const size_t base = static_cast<size_t>(t) * kTile;
         const int wbase = warp * kWarpItems;
-        uint32_t *vals = reinterpret_cast<uint32_t *>(ct.buf);
+        const uint32_t *vals = reinterpret_cast<const uint32_t *>(ct.buf);
         const uint8_t *fl = ct.buf + kValueBytes;
         const unsigned len = tile_len(a, t);
         const unsigned vcp = values_copied(a, t), fcp = flags_copied(a, t);
@@ -168,12 +230,12 @@ struct CompactPolicy {
                 keep[q] = m;
             }
         }
-        // the staged run may run three words into the flags area, which is
-        // read already
-        compact_write_tile<NS_, VECS>(x, keep, ct, wbuf0, wbuf1, warp, lane, vals, a.out, a.out_aligned, a.n, a.count,
-                                      t == a.num_tiles - 1);
-        release();
-        return 1;
+        const size_t g0 = static_cast<size_t>(ct.prefix) + ct.part_excl[warp];
+        release();   // values in registers, offset read: the B buffer and the record are free
+        uint32_t *stage = reinterpret_cast<uint32_t *>(ct.scratch) + warp * kWarpStage;
+        compact_write_warp<VECS>(x, keep, g0, lane, stage, a.out, a.out_aligned, a.n);
+        if (t == a.num_tiles - 1 && warp == 0 && lane == 0) *a.count = static_cast<int32_t>(ct.prefix + ct.aggregate);
+        return 0;   // no warp-totals buffer used
     }
 };
 
@@ -203,8 +265,11 @@ struct CompactGtPolicy {
     static constexpr int kTile = NS_ * 32 * 4 * VECS;
     static constexpr size_t kValueBytes = static_cast<size_t>(kTile) * 4;
     static constexpr size_t kABytes = kValueBytes;
-    static constexpr size_t kBBytes = kValueBytes + 16;   // + room for the staging phase (3 words)
+    static constexpr size_t kBBytes = kValueBytes;
     static constexpr bool kHasExtra = false;
+    static constexpr int kParts = NS_;                  // one part per consume warp
+    static constexpr int kWarpStage = kWarpItems + 4;   // words, 16-byte multiple
+    static constexpr size_t kScratchBytes = static_cast<size_t>(NS_) * kWarpStage * 4;
     struct Args {
         const uint32_t *in;
         int32_t threshold;
@@ -232,32 +297,54 @@ struct CompactGtPolicy {
         bytes[0] = a_bytes(a, t);
         off[0] = 0;
     }
-    __device__ static void reduce(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int nthr, S &v,
-                                  unsigned &)
+    // pass A: the kept count of each consume warp's part, one warp reduction
+    // per part (see CompactPolicy::reduce_parts)
+    __device__ static void reduce_parts(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int,
+                                        S &v, uint32_t *part)
     {
-        const unsigned cp = copied(a, t);
-        const int32_t thr = a.threshold;
-        unsigned c = 0;
-        const uint4 *b4 = reinterpret_cast<const uint4 *>(abuf);
-#pragma unroll 4
-        for (unsigned k = rtid; k < cp / 4; k += nthr) {
-            const uint4 q = b4[k];
-            c += __popc(greater_mask(q.x, q.y, q.z, q.w, thr));
-        }
+        static_assert(NS_ % NR_ == 0 && kWarpItems / 4 % 32 == 0, "whole parts per reduce warp");
+        constexpr int PPW = NS_ / NR_, CH = kWarpItems / 4 / 32;   // parts per warp, 4-value chunks per lane
+        const int lane = rtid & 31, rw = rtid >> 5;
+        const unsigned cp = copied(a, t), len = tile_len(a, t);
         const size_t base = static_cast<size_t>(t) * kTile;
-        const unsigned len = tile_len(a, t);
-        for (unsigned e = cp + rtid; e < len; e += nthr) c += static_cast<int32_t>(a.in[base + e]) > thr ? 1u : 0u;
-        v = c;
+        const int32_t thr = a.threshold;
+        const uint4 *b4 = reinterpret_cast<const uint4 *>(abuf);
+        const uint32_t *b1 = reinterpret_cast<const uint32_t *>(abuf);
+        unsigned c[PPW];
+        if (len == static_cast<unsigned>(kTile)) {
+#pragma unroll
+            for (int i = 0; i < PPW; ++i) {
+                c[i] = 0;
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    const uint4 q = b4[(rw + i * NR_) * (kWarpItems / 4) + k * 32 + lane];
+                    c[i] += __popc(greater_mask(q.x, q.y, q.z, q.w, thr));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < PPW; ++i) {
+                c[i] = 0;
+                for (int k = 0; k < CH; ++k) {
+                    const unsigned e = static_cast<unsigned>((rw + i * NR_) * kWarpItems + 4 * (k * 32 + lane));
+                    for (unsigned j = 0; j < 4; ++j)
+                        if (e + j < len)
+                            c[i] += (static_cast<int32_t>(e + j < cp ? b1[e + j] : a.in[base + e + j]) > thr) ? 1u : 0u;
+                }
+            }
+        }
+        const unsigned mine = store_part_counts<PPW, NR_>(c, rw, lane, part);
+        v = (lane == 0) ? mine : 0u;
     }
     __device__ static void after_reduce(const Args &, unsigned, unsigned) {}
     template <class Release>
-    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
-                                       int warp, int lane, Release &release)
+    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *, uint32_t *, int warp,
+                                       int lane, Release &release)
     {
         const unsigned t = ct.tile;
         const size_t base = static_cast<size_t>(t) * kTile;
         const int wbase = warp * kWarpItems;
-        uint32_t *vals = reinterpret_cast<uint32_t *>(ct.buf);
+        const uint32_t *vals = reinterpret_cast<const uint32_t *>(ct.buf);
         const unsigned len = tile_len(a, t);
         const unsigned cp = copied(a, t);
         const int32_t thr = a.threshold;
@@ -286,10 +373,12 @@ struct CompactGtPolicy {
                 keep[q] = m;
             }
         }
-        compact_write_tile<NS_, VECS>(x, keep, ct, wbuf0, wbuf1, warp, lane, vals, a.out, a.out_aligned, a.n, a.count,
-                                      t == a.num_tiles - 1);
-        release();
-        return 1;
+        const size_t g0 = static_cast<size_t>(ct.prefix) + ct.part_excl[warp];
+        release();   // values in registers, offset read: the B buffer and the record are free
+        uint32_t *stage = reinterpret_cast<uint32_t *>(ct.scratch) + warp * kWarpStage;
+        compact_write_warp<VECS>(x, keep, g0, lane, stage, a.out, a.out_aligned, a.n);
+        if (t == a.num_tiles - 1 && warp == 0 && lane == 0) *a.count = static_cast<int32_t>(ct.prefix + ct.aggregate);
+        return 0;   // no warp-totals buffer used
     }
 };
 

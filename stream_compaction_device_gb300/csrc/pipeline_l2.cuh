@@ -118,6 +118,30 @@ struct IsSegmented<P, decltype(void(P::kSegmented))> {
     static constexpr bool value = P::kSegmented;
 };
 
+// Optional policy members, detected:
+//   kParts        the reduce step also reports the aggregates of kParts equal
+//                 parts of the tile (P::reduce_parts instead of P::reduce);
+//                 the consume step gets their exclusive prefixes, so each
+//                 consume warp knows its offset inside the tile without a
+//                 group-wide scan;
+//   kScratchBytes shared memory for the consume group beyond the B buffers.
+template <class P, class = void>
+struct PolicyParts {
+    static constexpr int value = 0;
+};
+template <class P>
+struct PolicyParts<P, decltype(void(P::kParts))> {
+    static constexpr int value = P::kParts;
+};
+template <class P, class = void>
+struct PolicyScratch {
+    static constexpr size_t value = 0;
+};
+template <class P>
+struct PolicyScratch<P, decltype(void(P::kScratchBytes))> {
+    static constexpr size_t value = P::kScratchBytes;
+};
+
 // Pass-A copies of tile t: P::a_copies when the policy has one (up to two
 // copies, as for pass B), else the single copy P::a_src / P::a_bytes.
 template <class P, class = void>
@@ -148,6 +172,8 @@ struct ConsumeTile {
     unsigned char *buf; // the B buffer (P::kBBytes bytes)
     unsigned round;     // alternates the warp-totals buffers
     unsigned *warp_state;   // per-warp word kept across the block's tiles (0 at start)
+    const uint32_t *part_excl;   // exclusive prefixes of the parts' aggregates (P::kParts > 0; until release)
+    unsigned char *scratch;      // P::kScratchBytes of shared memory for the consume group
 };
 
 template <class P>
@@ -160,6 +186,8 @@ struct PipeShape {
     static constexpr int kProducerB = NS + NR + R + 1;
     static constexpr int kThreads = (NS + NR + R + 2) * 32;
     static constexpr unsigned kNoCopy = 0xffffffffu;
+    static constexpr int kParts = PolicyParts<P>::value;
+    static constexpr int kPartSlots = kParts > 0 ? kParts : 1;
     struct Ctrl {
         uint64_t a_full[SA], a_empty[SA];
         uint64_t b_full[SB], b_empty[SB];
@@ -169,6 +197,7 @@ struct PipeShape {
         unsigned rec_tile[R];
         uint32_t rec_agg[R], rec_prefix[R], rec_head[R];
         uint32_t red[NR], red_extra[NR];
+        uint32_t red_part[kPartSlots], rec_part[R][kPartSlots];
         uint32_t wtot[2][NS];
         unsigned tag;
     };
@@ -176,7 +205,8 @@ struct PipeShape {
     static constexpr size_t kLead = 16;
     static constexpr size_t kABase = kLead;
     static constexpr size_t kBBase = kABase + static_cast<size_t>(SA) * P::kABytes;
-    static constexpr size_t kCtrlBase = kBBase + static_cast<size_t>(SB) * P::kBBytes;
+    static constexpr size_t kScratchBase = kBBase + static_cast<size_t>(SB) * P::kBBytes;
+    static constexpr size_t kCtrlBase = kScratchBase + ((PolicyScratch<P>::value + 15) & ~static_cast<size_t>(15));
     static constexpr size_t kSmemBytes = kCtrlBase + sizeof(Ctrl) + 64;
     static_assert(P::kABytes % 16 == 0 && P::kBBytes % 16 == 0, "16-byte aligned buffers");
     static_assert(kThreads <= 1024, "one block of at most 1024 threads");
@@ -417,7 +447,10 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
             }
             S v = Op::identity();
             unsigned extra = 0;
-            P::reduce(args, abuf + static_cast<size_t>(a) * P::kABytes, t, rtid, NR * 32, v, extra);
+            if constexpr (G::kParts > 0)
+                P::reduce_parts(args, abuf + static_cast<size_t>(a) * P::kABytes, t, rtid, NR * 32, v, ctrl->red_part);
+            else
+                P::reduce(args, abuf + static_cast<size_t>(a) * P::kABytes, t, rtid, NR * 32, v, extra);
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->a_empty[a]);   // buffer read: free it
 #pragma unroll
@@ -463,6 +496,13 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 ctrl->rec_tile[r] = t;
                 ctrl->rec_agg[r] = to_bits(agg);
                 ctrl->rec_head[r] = head;
+                if constexpr (G::kParts > 0) {
+                    S acc = Op::identity();
+                    for (int q = 0; q < G::kParts; ++q) {
+                        ctrl->rec_part[r][q] = to_bits(acc);
+                        acc = op(acc, from_bits<S>(ctrl->red_part[q]));
+                    }
+                }
                 mbar_arrive(&ctrl->rec_pending[r]);
             }
             // red[] free for the next tile; a timed-out record wait ends the group
@@ -491,6 +531,8 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
         ct.buf = bbuf + static_cast<size_t>(b) * P::kBBytes;
         ct.round = round;
         ct.warp_state = &warp_state;
+        ct.part_excl = ctrl->rec_part[r];
+        ct.scratch = smem + G::kScratchBase;
         // release(): the B buffer and the record are no longer needed
         auto release = [&]() {
             __syncwarp();
