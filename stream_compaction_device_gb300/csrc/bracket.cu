@@ -57,7 +57,7 @@ struct BracketEpilogue {
 };
 
 // Pipelined scan policy with the same epilogue (geometry of the int32 scan).
-using BracketBase = ScanPolicy<AddU32, true, 16, 2, 4, 2, 4, 12, kL2EvictLast, kL2EvictFirst, true, 1>;
+using BracketBase = ScanPolicy<AddU32, true, 16, 4, 4, 2, 4, 10, kL2EvictLast, kL2EvictFirst, true, 1>;
 
 struct BracketPolicy : BracketBase {
     struct Args : BracketBase::Args {

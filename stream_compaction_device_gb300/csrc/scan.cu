@@ -178,10 +178,12 @@ cudaError_t launch_lookback(const void *in, void *out, size_t n, const Workspace
 }
 
 // Geometry of the pipelined scan: 16 consume warps x 4 rows (8,192-element
-// tiles), 2 reduce warps, 2 A buffers, 4 B buffers, 12 in-flight records
+// tiles), 4 reduce warps, 2 A buffers, 4 B buffers, 10 in-flight records
 // (1,024 threads, about 193 KiB of shared memory: one block per SM); tickets
-// are taken one tile ahead and prefetched into L2.  Chosen by a sweep on
-// GB300 (deeper prefetch and more records overflow what L2 keeps).
+// are taken one tile ahead and prefetched into L2.  Chosen by sweeps on
+// GB300: the reduce step sits on the A ring's turnaround, so four reduce
+// warps beat two (by 3-4%); deeper prefetch and more records overflow what
+// L2 keeps.
 constexpr unsigned kWaitLimit = 1u << 18;   // bounded mbarrier polls (~1 us each at most)
 constexpr size_t kPipelineMinN = size_t(1) << 19;
 
@@ -190,7 +192,7 @@ cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspac
                              cudaStream_t s)
 {
     using S = typename Op::S;
-    using P = ScanPolicy<Op, INCLUSIVE, 16, 2, 4, 2, 4, 12, kL2EvictLast, kL2EvictFirst, true, 1>;
+    using P = ScanPolicy<Op, INCLUSIVE, 16, 4, 4, 2, 4, 10, kL2EvictLast, kL2EvictFirst, true, 1>;
     using G = PipeShape<P>;
     auto kernel = pipeline_l2_kernel<P>;
     static std::atomic<unsigned long long> attribute_set{0};   // one bit per device

@@ -453,7 +453,7 @@ cudaError_t launch_seg_pipelined(const void *in, const uint8_t *heads, void *out
                                  unsigned spin_limit, cudaStream_t s)
 {
     using S = typename Op::S;
-    using P = SegScanPolicy<Op, INCLUSIVE, 16, 2, 4, 2, 3, 12, 1>;
+    using P = SegScanPolicy<Op, INCLUSIVE, 16, 4, 4, 3, 2, 10, 1>;
     using G = PipeShape<P>;
     auto kernel = pipeline_l2_kernel<P>;
     static std::atomic<unsigned long long> attribute_set{0};   // one bit per device

@@ -163,7 +163,7 @@ split_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size
 }
 
 
-using SplitPipe = SplitPolicy<16, 2, 4, 3, 3, 12, 1>;
+using SplitPipe = SplitPolicy<16, 4, 4, 2, 3, 10, 1>;
 constexpr unsigned kSplitWaitLimit = 1u << 18;
 constexpr size_t kSplitPipelineMinN = size_t(1) << 19;
 
