@@ -117,6 +117,7 @@ struct CompactPolicy {
     static constexpr size_t kBBytes = kValueBytes + static_cast<size_t>(kTile);  // values, then flags
     static constexpr bool kHasExtra = false;
     static constexpr int kParts = NS_;                                          // one part per consume warp
+    static constexpr bool kWarpIndependent = true;                              // no barrier in consume()
     static constexpr int kWarpStage = kWarpItems + 4;                           // words, 16-byte multiple
     static constexpr size_t kScratchBytes = static_cast<size_t>(NS_) * kWarpStage * 4;
     struct Args {
@@ -268,6 +269,7 @@ struct CompactGtPolicy {
     static constexpr size_t kBBytes = kValueBytes;
     static constexpr bool kHasExtra = false;
     static constexpr int kParts = NS_;                  // one part per consume warp
+    static constexpr bool kWarpIndependent = true;      // no barrier in consume()
     static constexpr int kWarpStage = kWarpItems + 4;   // words, 16-byte multiple
     static constexpr size_t kScratchBytes = static_cast<size_t>(NS_) * kWarpStage * 4;
     struct Args {

@@ -133,6 +133,17 @@ template <class P>
 struct PolicyParts<P, decltype(void(P::kParts))> {
     static constexpr int value = P::kParts;
 };
+//   kWarpIndependent  the consume step has no group-wide barrier: each
+//                 consume warp waits for its B buffer on its own and may run
+//                 ahead of the others by up to the ring's depth.
+template <class P, class = void>
+struct PolicyWarpIndependent {
+    static constexpr bool value = false;
+};
+template <class P>
+struct PolicyWarpIndependent<P, decltype(void(P::kWarpIndependent))> {
+    static constexpr bool value = P::kWarpIndependent;
+};
 template <class P, class = void>
 struct PolicyScratch {
     static constexpr size_t value = 0;
@@ -517,7 +528,14 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
     for (unsigned i = 0;; ++i) {
         const unsigned b = i % SB, kb = i / SB;
         const bool landed = mbar_wait(&ctrl->b_full[b], kb & 1u, wait_limit);
-        if (!named_sync_and(kBarConsumeDecide, NS * 32, landed)) {
+        if constexpr (PolicyWarpIndependent<P>::value) {
+            // no barrier inside the consume step: a warp that gives up leaves
+            // alone, and every wait of the others stays bounded
+            if (!landed) {
+                if (lane == 0) atomicOr(&st->error, kErrTimeout);
+                break;
+            }
+        } else if (!named_sync_and(kBarConsumeDecide, NS * 32, landed)) {
             if (tid == 0) atomicOr(&st->error, kErrTimeout);
             break;
         }
