@@ -151,16 +151,30 @@ class ClockSampler:
 # timing helpers
 # ---------------------------------------------------------------------------
 def time_events(fn, reps, warmup, flush=None):
-    """Median and mean per-call milliseconds of fn() with CUDA events on the
-    current stream; ``flush`` (if any) runs between calls outside the events."""
+    """Per-call milliseconds of fn() with CUDA events on the current stream,
+    as (median, mean).  Without ``flush`` the calls run back to back between
+    one pair of events, as the headline steps do, so the host's launch
+    overhead overlaps the device work and the result is the device time per
+    call (median and mean are then the same number).  With ``flush`` (run
+    between calls, outside the events) every call is timed on its own, which
+    includes whatever launch latency the device waits for."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    if flush is None:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        b.synchronize()
+        per = a.elapsed_time(b) / reps
+        return per, per
     times = []
     for _ in range(reps):
-        if flush is not None:
-            flush()
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
@@ -304,7 +318,9 @@ def run_ours(args):
 
 
 def run_extras(args, ds, wl, d_in, d_out, peak):
-    """Secondary rows: each timed with CUDA events (median of reps)."""
+    """Secondary rows, timed with CUDA events: back-to-back calls between one
+    event pair (device time per call), except the rows that flush L2 between
+    calls, which are timed call by call."""
     import torch
     out = {}
     reps = args.extra_reps

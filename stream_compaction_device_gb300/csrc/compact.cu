@@ -127,7 +127,7 @@ compact_kernel(const uint32_t *__restrict__ in, const uint8_t *__restrict__ flag
 }
 
 
-using CompactPipe = CompactPolicy<16, 4, 4, 2, 3, 8, 1>;
+using CompactPipe = CompactPolicy<16, 4, 4, 3, 3, 8, 1>;
 using CompactGtPipe = CompactGtPolicy<16, 4, 4, 3, 2, 10, 1>;
 constexpr unsigned kCompactWaitLimit = 1u << 18;
 constexpr size_t kCompactPipelineMinN = size_t(1) << 19;

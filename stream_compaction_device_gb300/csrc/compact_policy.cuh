@@ -103,6 +103,12 @@ __device__ __forceinline__ unsigned store_part_counts(const unsigned (&c)[PPW], 
     return mine;
 }
 
+// Pass A copies only the flags, so the values need not reach L2 before a
+// tile is counted: they are moved there once pass A has counted the tile,
+// while its prefix resolves.  That keeps L2's footprint smaller than moving
+// them with the flags at ticket time (measured 9-10% faster at 50-99% kept;
+// loading only the kept values of sparse tiles instead of the bulk copy
+// measured slower).
 template <int NS_, int NR_, int VECS_, int SA_, int SB_, int R_, int PREFETCH = 0>
 struct CompactPolicy {
     using Op = AddU32;
@@ -118,6 +124,7 @@ struct CompactPolicy {
     static constexpr bool kHasExtra = false;
     static constexpr int kParts = NS_;                                          // one part per consume warp
     static constexpr bool kWarpIndependent = true;                              // no barrier in consume()
+    static constexpr bool kAggregateAware = true;                               // on_aggregate moves the values
     static constexpr int kWarpStage = kWarpItems + 4;                           // words, 16-byte multiple
     static constexpr size_t kScratchBytes = static_cast<size_t>(NS_) * kWarpStage * 4;
     struct Args {
@@ -138,12 +145,22 @@ struct CompactPolicy {
     __device__ static unsigned values_copied(const Args &a, unsigned t) { return tile_len(a, t) & ~3u; }
     __device__ static const void *a_src(const Args &a, unsigned t) { return a.flags + static_cast<size_t>(t) * kTile; }
     __device__ static unsigned a_bytes(const Args &a, unsigned t) { return flags_copied(a, t); }
-    // both arrays: pass B then finds the values in L2 as well
+    // the flags, for pass A (the values follow in on_aggregate)
     __device__ static void prefetch_l2(const Args &a, unsigned t, uint64_t pol)
     {
         if (flags_copied(a, t) != 0) bulk_prefetch_l2(a_src(a, t), flags_copied(a, t), pol);
+    }
+    // after pass A: the tile's values start moving into L2 while its prefix
+    // resolves
+    __device__ static void on_aggregate(const Args &a, unsigned t, uint32_t)
+    {
         if (values_copied(a, t) != 0)
-            bulk_prefetch_l2(a.in + static_cast<size_t>(t) * kTile, values_copied(a, t) * 4u, pol);
+            bulk_prefetch_l2(a.in + static_cast<size_t>(t) * kTile, values_copied(a, t) * 4u, l2_policy_evict_last());
+    }
+    __device__ static void b_copies_for(const Args &a, unsigned t, uint32_t, const void **src, unsigned *bytes,
+                                        unsigned *off)
+    {
+        b_copies(a, t, src, bytes, off);
     }
     __device__ static void b_copies(const Args &a, unsigned t, const void **src, unsigned *bytes, unsigned *off)
     {

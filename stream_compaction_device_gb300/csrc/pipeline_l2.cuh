@@ -144,6 +144,18 @@ template <class P>
 struct PolicyWarpIndependent<P, decltype(void(P::kWarpIndependent))> {
     static constexpr bool value = P::kWarpIndependent;
 };
+//   kAggregateAware  the policy sees each tile's aggregate: P::on_aggregate
+//                 runs right after the reduce step publishes it, and pass B
+//                 takes its copies from P::b_copies_for (given the
+//                 aggregate) instead of P::b_copies.
+template <class P, class = void>
+struct PolicyAggregateAware {
+    static constexpr bool value = false;
+};
+template <class P>
+struct PolicyAggregateAware<P, decltype(void(P::kAggregateAware))> {
+    static constexpr bool value = P::kAggregateAware;
+};
 template <class P, class = void>
 struct PolicyScratch {
     static constexpr size_t value = 0;
@@ -372,7 +384,10 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 const void *src[2] = {nullptr, nullptr};
                 unsigned bytes[2] = {0, 0}, off[2] = {0, 0};
                 if (t < num_tiles) {
-                    P::b_copies(args, t, src, bytes, off);
+                    if constexpr (PolicyAggregateAware<P>::value)
+                        P::b_copies_for(args, t, from_bits<S>(ctrl->rec_agg[r]), src, bytes, off);
+                    else
+                        P::b_copies(args, t, src, bytes, off);
                     total = bytes[0] + bytes[1];
                 }
                 if (total != 0) {
@@ -502,6 +517,7 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 st_status(status + t, pack_status(tag, (t == 0 || head) ? kFlagInclusive : kFlagAggregate,
                                                   to_bits(agg)));
                 if (P::kHasExtra) P::after_reduce(args, t, ex);
+                if constexpr (PolicyAggregateAware<P>::value) P::on_aggregate(args, t, agg);
                 if (kr > 0) freed = mbar_wait(&ctrl->rec_free[r], (kr - 1) & 1u, wait_limit);
                 if (!freed) atomicOr(&st->error, kErrTimeout);
                 ctrl->rec_tile[r] = t;
