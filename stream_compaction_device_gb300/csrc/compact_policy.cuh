@@ -82,27 +82,6 @@ __device__ __forceinline__ void compact_write_warp(const uint32_t (&x)[VECS][4],
     __syncwarp();   // the area is read before the warp stages its next part
 }
 
-// Finishes a reduce warp's part counts: c[i] is this lane's count of part
-// rw + i * NR (each part's total is at most 2^15, so two parts share one
-// word's 16-bit halves and one warp reduction); lane 0 stores the parts and
-// returns their sum.
-template <int PPW, int NR>
-__device__ __forceinline__ unsigned store_part_counts(const unsigned (&c)[PPW], int rw, int lane, uint32_t *part)
-{
-    unsigned mine = 0;
-#pragma unroll
-    for (int i = 0; i < PPW; i += 2) {
-        uint32_t w = c[i] | ((i + 1 < PPW) ? (c[i + 1] << 16) : 0u);
-        w = __reduce_add_sync(kFullMask, w);
-        if (lane == 0) {
-            part[rw + i * NR] = w & 0xffffu;
-            if (i + 1 < PPW) part[rw + (i + 1) * NR] = w >> 16;
-        }
-        mine += (w & 0xffffu) + (w >> 16);
-    }
-    return mine;
-}
-
 // Pass A copies only the flags, so the values need not reach L2 before a
 // tile is counted: they are moved there once pass A has counted the tile,
 // while its prefix resolves.  That keeps L2's footprint smaller than moving
@@ -175,7 +154,7 @@ struct CompactPolicy {
     // one warp reduction per part; lane 0 of each reduce warp returns the
     // sum of its parts (the kernel adds the lanes and the warps)
     __device__ static void reduce_parts(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int,
-                                        S &v, uint32_t *part)
+                                        S &v, unsigned &, uint32_t *part)
     {
         static_assert(NS_ % NR_ == 0 && kWarpItems / 16 % 32 == 0, "whole parts per reduce warp");
         constexpr int PPW = NS_ / NR_, CH = kWarpItems / 16 / 32;   // parts per warp, 16-flag chunks per lane
@@ -319,7 +298,7 @@ struct CompactGtPolicy {
     // pass A: the kept count of each consume warp's part, one warp reduction
     // per part (see CompactPolicy::reduce_parts)
     __device__ static void reduce_parts(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int,
-                                        S &v, uint32_t *part)
+                                        S &v, unsigned &, uint32_t *part)
     {
         static_assert(NS_ % NR_ == 0 && kWarpItems / 4 % 32 == 0, "whole parts per reduce warp");
         constexpr int PPW = NS_ / NR_, CH = kWarpItems / 4 / 32;   // parts per warp, 4-value chunks per lane

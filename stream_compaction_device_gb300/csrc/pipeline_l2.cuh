@@ -186,6 +186,27 @@ struct PassACopies<P, decltype(void(&P::a_copies))> {
     }
 };
 
+// Finishes a reduce warp's part counts: c[i] is this lane's count of part
+// rw + i * NR (each part's total is at most 2^15, so two parts share one
+// word's 16-bit halves and one warp reduction); lane 0 stores the parts and
+// returns their sum.
+template <int PPW, int NR>
+__device__ __forceinline__ unsigned store_part_counts(const unsigned (&c)[PPW], int rw, int lane, uint32_t *part)
+{
+    unsigned mine = 0;
+#pragma unroll
+    for (int i = 0; i < PPW; i += 2) {
+        uint32_t w = c[i] | ((i + 1 < PPW) ? (c[i + 1] << 16) : 0u);
+        w = __reduce_add_sync(kFullMask, w);
+        if (lane == 0) {
+            part[rw + i * NR] = w & 0xffffu;
+            if (i + 1 < PPW) part[rw + (i + 1) * NR] = w >> 16;
+        }
+        mine += (w & 0xffffu) + (w >> 16);
+    }
+    return mine;
+}
+
 // What the consume group gets for one tile.
 template <class S>
 struct ConsumeTile {
@@ -474,7 +495,8 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
             S v = Op::identity();
             unsigned extra = 0;
             if constexpr (G::kParts > 0)
-                P::reduce_parts(args, abuf + static_cast<size_t>(a) * P::kABytes, t, rtid, NR * 32, v, ctrl->red_part);
+                P::reduce_parts(args, abuf + static_cast<size_t>(a) * P::kABytes, t, rtid, NR * 32, v, extra,
+                                ctrl->red_part);
             else
                 P::reduce(args, abuf + static_cast<size_t>(a) * P::kABytes, t, rtid, NR * 32, v, extra);
             __syncwarp();

@@ -15,13 +15,69 @@ __device__ __forceinline__ unsigned zeros_of(uint4 q, int bit)
 
 // ---------------------------------------------------------------------------
 // Pipelined split (see pipeline_l2.cuh): pass A reads the tile's keys and
-// counts the keys whose bit is 0 -- the aggregate the look-back carries --
-// and, inside a sort, the zeros of the next bit; pass B re-reads the keys
-// (from L2), ranks them, stages the zeros and then the ones in the B buffer
-// and writes two contiguous runs: zeros at the tile's prefix, ones at
-// Z + (tile start - prefix).  HBM traffic: 8 bytes per key.
+// counts, for each consume warp's 512-key part, the keys whose bit is 0 (the
+// tile's sum is the aggregate the look-back carries) and, inside a sort, the
+// zeros of the next bit.  Pass B re-reads the keys (from L2); every consume
+// warp, on its own, ranks its part, stages its zeros and its ones in a
+// private shared-memory area and writes two contiguous runs: zeros at the
+// tile's prefix plus the zeros of the earlier parts, ones at
+// Z + (keys before the part - zeros before the part).  HBM traffic: 8 bytes
+// per key.
 // ---------------------------------------------------------------------------
-constexpr unsigned kBarSplitStage = 8;
+
+// One consume warp's part of a split (bit j of zmask[q] marks key x[q][j] as
+// a zero; part_len keys are real): ranks the zeros with one scan of the four
+// rows' counts packed into the bytes of a word, stages the zeros from word
+// zeros_at % 4 and the ones from the next 16-byte boundary after them (plus
+// ones_at % 4) in its private `stage` area (kWarpItems + 12 words), and
+// writes both runs out in whole 128-bit chunks where they line up.
+template <int VECS>
+__device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], const uint32_t (&zmask)[VECS],
+                                                 unsigned part_len, size_t zeros_at, size_t ones_at, int lane,
+                                                 uint32_t *stage, uint32_t *out, bool out_aligned, size_t n)
+{
+    static_assert(VECS == 4, "the four rows' counts share one word");
+    uint32_t packed = 0;
+#pragma unroll
+    for (int q = 0; q < VECS; ++q) packed |= static_cast<uint32_t>(__popc(zmask[q])) << (8 * q);
+    uint32_t inc = packed;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
+        if (lane >= d) inc += u;
+    }
+    const uint32_t excl = inc - packed, tot = __shfl_sync(kFullMask, inc, 31);
+    const uint32_t zeros = (tot & 0xffu) + ((tot >> 8) & 0xffu) + ((tot >> 16) & 0xffu) + (tot >> 24);
+    const unsigned z_phase = out_aligned ? static_cast<unsigned>(zeros_at & 3) : 0u;
+    const unsigned o_phase = out_aligned ? static_cast<unsigned>(ones_at & 3) : 0u;
+    const unsigned o_base = out_aligned ? ((z_phase + zeros + 3u) & ~3u) : zeros;
+    uint32_t row_base = 0;
+#pragma unroll
+    for (int q = 0; q < VECS; ++q) {
+        uint32_t zr = row_base + ((excl >> (8 * q)) & 0xffu);
+        const uint32_t li0 = static_cast<uint32_t>((q * 32 + lane) * 4);   // index inside the part
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t li = li0 + j;
+            if (li < part_len) {
+                if ((zmask[q] >> j) & 1u)
+                    stage[z_phase + zr++] = x[q][j];
+                else
+                    stage[o_base + o_phase + (li - zr)] = x[q][j];
+            }
+        }
+        row_base += (tot >> (8 * q)) & 0xffu;
+    }
+    __syncwarp();
+    if (out_aligned) {
+        write_run_direct<32>(out, zeros_at, zeros, stage, lane, n);
+        write_run_direct<32>(out, ones_at, part_len - zeros, stage + o_base, lane, n);
+    } else {
+        write_run_scalar<32>(out, zeros_at, zeros, stage, 0, lane, n);
+        write_run_scalar<32>(out, ones_at, part_len - zeros, stage, static_cast<int>(zeros), lane, n);
+    }
+    __syncwarp();   // the area is read before the warp stages its next part
+}
 
 template <int NS_, int NR_, int VECS_, int SA_, int SB_, int R_, int PREFETCH = 0>
 struct SplitPolicy {
@@ -33,7 +89,13 @@ struct SplitPolicy {
     static constexpr int kWarpItems = 32 * 4 * VECS;
     static constexpr int kTile = NS_ * 32 * 4 * VECS;
     static constexpr size_t kABytes = static_cast<size_t>(kTile) * 4;
-    static constexpr size_t kBBytes = static_cast<size_t>(kTile) * 4 + 64;   // keys, margin for the run copy
+    static constexpr size_t kBBytes = static_cast<size_t>(kTile) * 4;
+    static constexpr int kParts = NS_;                   // one part per consume warp
+    static constexpr bool kWarpIndependent = true;       // no barrier in consume()
+    // words: the zeros from word 0..3, the ones from the next 16-byte boundary
+    // plus 0..3, and the copy-out's last whole chunk: at most kWarpItems + 12
+    static constexpr int kWarpStage = kWarpItems + 12;
+    static constexpr size_t kScratchBytes = static_cast<size_t>(NS_) * kWarpStage * 4;
     static constexpr bool kHasExtra = true;
     struct Args {
         const uint32_t *keys;
@@ -63,24 +125,45 @@ struct SplitPolicy {
         bytes[0] = copied(a, t) * 4u;
         off[0] = 0;
     }
-    __device__ static void reduce(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int nthr, S &v,
-                                  unsigned &extra)
+    __device__ static void reduce_parts(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int, S &v,
+                                        unsigned &extra, uint32_t *part)
     {
+        static_assert(NS_ % NR_ == 0 && kWarpItems / 4 % 32 == 0, "whole parts per reduce warp");
+        constexpr int PPW = NS_ / NR_, CH = kWarpItems / 4 / 32;   // parts per warp, 4-key chunks per lane
+        const int lane = rtid & 31, rw = rtid >> 5;
         const unsigned cp = copied(a, t), len = tile_len(a, t);
-        const uint4 *k4 = reinterpret_cast<const uint4 *>(abuf);
-        unsigned z = 0, nz = 0;
-        for (unsigned c = rtid; c < cp / 4; c += nthr) {
-            const uint4 q = k4[c];
-            z += zeros_of(q, a.bit);
-            nz += zeros_of(q, a.next_bit);
-        }
         const size_t base = static_cast<size_t>(t) * kTile;
-        for (unsigned e = cp + rtid; e < len; e += nthr) {
-            const uint32_t k = a.keys[base + e];
-            z += ((k >> a.bit) & 1u) ? 0u : 1u;
-            nz += ((k >> a.next_bit) & 1u) ? 0u : 1u;
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(abuf);
+        const uint32_t *k1 = reinterpret_cast<const uint32_t *>(abuf);
+        unsigned c[PPW], nz = 0;
+        if (len == static_cast<unsigned>(kTile)) {
+#pragma unroll
+            for (int i = 0; i < PPW; ++i) {
+                c[i] = 0;
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    const uint4 q = k4[(rw + i * NR_) * (kWarpItems / 4) + k * 32 + lane];
+                    c[i] += zeros_of(q, a.bit);
+                    nz += zeros_of(q, a.next_bit);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < PPW; ++i) {
+                c[i] = 0;
+                for (int k = 0; k < CH; ++k) {
+                    const unsigned e = static_cast<unsigned>((rw + i * NR_) * kWarpItems + 4 * (k * 32 + lane));
+                    for (unsigned j = 0; j < 4; ++j)
+                        if (e + j < len) {
+                            const uint32_t key = (e + j < cp) ? k1[e + j] : a.keys[base + e + j];
+                            c[i] += ((key >> a.bit) & 1u) ? 0u : 1u;
+                            nz += ((key >> a.next_bit) & 1u) ? 0u : 1u;
+                        }
+                }
+            }
         }
-        v = z;
+        const unsigned mine = store_part_counts<PPW, NR_>(c, rw, lane, part);
+        v = (lane == 0) ? mine : 0u;
         extra = nz;
     }
     __device__ static void after_reduce(const Args &a, unsigned, unsigned next_zero_count)
@@ -88,17 +171,15 @@ struct SplitPolicy {
         if (a.next_zeros != nullptr && next_zero_count != 0) atomicAdd(a.next_zeros, next_zero_count);
     }
     template <class Release>
-    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
-                                       int warp, int lane, Release &release)
+    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *, uint32_t *, int warp,
+                                       int lane, Release &release)
     {
-        constexpr int THREADS = NS_ * 32;
-        const AddU32 op;
         const unsigned t = ct.tile;
         const size_t base = static_cast<size_t>(t) * kTile;
         const int wbase = warp * kWarpItems;
-        uint32_t *buf = reinterpret_cast<uint32_t *>(ct.buf);
+        const uint32_t *buf = reinterpret_cast<const uint32_t *>(ct.buf);
         const unsigned len = tile_len(a, t), cp = copied(a, t);
-        uint32_t x[VECS][4], zmask[VECS], cnt[VECS];
+        uint32_t x[VECS][4], zmask[VECS];
 #pragma unroll
         for (int q = 0; q < VECS; ++q) {
             if (len == static_cast<unsigned>(kTile)) {
@@ -121,47 +202,17 @@ struct SplitPolicy {
                 if (e < len && !((x[q][j] >> a.bit) & 1u)) m |= 1u << j;
             }
             zmask[q] = m;
-            cnt[q] = __popc(m);
         }
-        uint32_t row_excl[VECS], warp_total;
-        warp_scan_rows<AddU32, VECS>(op, cnt, lane, row_excl, warp_total);
-        uint32_t warp_excl, tile_zeros;
-        // the barrier inside also means every thread has read the buffer
-        group_scan<AddU32, NS_>(op, warp_total, (ct.round & 1) ? wbuf1 : wbuf0, warp, lane, warp_excl, tile_zeros);
-        // stage both runs in phase with their destinations (both offsets are
-        // known here): zeros from word z_phase, ones from the next 16-byte
-        // boundary after the zeros plus o_phase
-        const size_t zeros_before = ct.prefix;
-        const size_t ones_at = static_cast<size_t>(*a.zeros_total) + (base - zeros_before);
-        const unsigned z_phase = a.out_aligned ? static_cast<unsigned>(zeros_before & 3) : 0u;
-        const unsigned o_phase = a.out_aligned ? static_cast<unsigned>(ones_at & 3) : 0u;
-        const unsigned o_base = a.out_aligned ? ((z_phase + tile_zeros + 3u) & ~3u) : tile_zeros;
-#pragma unroll
-        for (int q = 0; q < VECS; ++q) {
-            uint32_t zr = warp_excl + row_excl[q];
-            const uint32_t li0 = static_cast<uint32_t>(wbase + (q * 32 + lane) * 4);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t li = li0 + j;
-                if (li < len) {
-                    if ((zmask[q] >> j) & 1u)
-                        buf[z_phase + zr++] = x[q][j];
-                    else
-                        buf[o_base + o_phase + (li - zr)] = x[q][j];
-                }
-            }
-        }
-        named_sync(kBarSplitStage, THREADS);
-        const int tid = warp * 32 + lane;
-        if (a.out_aligned) {
-            write_run_direct<THREADS>(a.out, zeros_before, tile_zeros, buf, tid, a.n);
-            write_run_direct<THREADS>(a.out, ones_at, len - tile_zeros, buf + o_base, tid, a.n);
-        } else {
-            write_run_scalar<THREADS>(a.out, zeros_before, tile_zeros, buf, 0, tid, a.n);
-            write_run_scalar<THREADS>(a.out, ones_at, len - tile_zeros, buf, static_cast<int>(tile_zeros), tid, a.n);
-        }
-        release();
-        return 1;
+        const size_t zeros_at = static_cast<size_t>(ct.prefix) + ct.part_excl[warp];
+        const size_t ones_at = static_cast<size_t>(*a.zeros_total) + (base + wbase - zeros_at);
+        const unsigned part_len = len > static_cast<unsigned>(wbase)
+                                      ? (len - wbase < static_cast<unsigned>(kWarpItems) ? len - wbase
+                                                                                          : static_cast<unsigned>(kWarpItems))
+                                      : 0u;
+        release();   // keys in registers, offsets read: the B buffer and the record are free
+        uint32_t *stage = reinterpret_cast<uint32_t *>(ct.scratch) + warp * kWarpStage;
+        split_write_warp<VECS>(x, zmask, part_len, zeros_at, ones_at, lane, stage, a.out, a.out_aligned, a.n);
+        return 0;   // no warp-totals buffer used
     }
 };
 
