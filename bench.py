@@ -156,8 +156,9 @@ def time_events(fn, reps, warmup, flush=None):
     one pair of events, as the headline steps do, so the host's launch
     overhead overlaps the device work and the result is the device time per
     call (median and mean are then the same number).  With ``flush`` (run
-    between calls, outside the events) every call is timed on its own, which
-    includes whatever launch latency the device waits for."""
+    between calls, outside the events) every call gets its own pair of events;
+    everything is enqueued before the one synchronize at the end, so the
+    device never waits on the host inside a pair."""
     import torch
     for _ in range(warmup):
         fn()
@@ -172,7 +173,7 @@ def time_events(fn, reps, warmup, flush=None):
         b.synchronize()
         per = a.elapsed_time(b) / reps
         return per, per
-    times = []
+    pairs = []
     for _ in range(reps):
         flush()
         a = torch.cuda.Event(enable_timing=True)
@@ -180,8 +181,9 @@ def time_events(fn, reps, warmup, flush=None):
         a.record()
         fn()
         b.record()
-        b.synchronize()
-        times.append(a.elapsed_time(b))
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in pairs]
     return statistics.median(times), statistics.fmean(times)
 
 

@@ -217,12 +217,19 @@ devscan_status devscan_stream_release(cudaStream_t stream);
 /* Inter-block carry strategy for the scans (P1 section 四 describes the
  * three-phase "reduce, scan the block totals, add the offsets" scheme and
  * mentions chaining blocks inside one launch):
- *   0 = default (3 for 16-byte-aligned in/out and n >= 2^19, else 1);
+ *   0 = default: for 16-byte-aligned in/out the scans take 4 for
+ *       2^17 <= n <= 3 * 2^22 and 3 above; compaction, the split, the
+ *       bracket scan and the segmented scan take 3 from n = 2^19; everything
+ *       else takes 1;
  *   1 = one tile per block, single-pass decoupled look-back;
  *   2 = reduce-then-scan (three launches, one extra read of the input);
  *   3 = pipelined single pass: persistent warp-specialised blocks with bulk
  *       copies and a two-level look-back (16-byte-aligned in/out; others
- *       use 1).
+ *       use 1);
+ *   4 = L2-resident scan (scans only): one cooperative launch of one block
+ *       per SM, a grid barrier between the chunk totals and the chunk scans,
+ *       the second read served by L2 (16-byte-aligned in/out; others use 1;
+ *       compaction, split and the segmented scan use 3).
  * Compaction and the split follow the same choice between 1 and 3 (their
  * pipelined kernels need 16-byte-aligned inputs, and flags too for
  * compaction).  Process-wide; meant for measurement.  Returns

@@ -235,9 +235,10 @@ def device_status(stream=None) -> int:
 
 
 def set_carry_mode(mode: str) -> None:
-    """'default', 'lookback' (one tile per block), 'rts' (reduce-then-scan)
-    or 'pipelined' (persistent warp-specialised single pass), process-wide."""
-    code = {"default": 0, "lookback": 1, "rts": 2, "pipelined": 3}[mode]
+    """'default', 'lookback' (one tile per block), 'rts' (reduce-then-scan),
+    'pipelined' (persistent warp-specialised single pass) or 'l2' (the
+    L2-resident cooperative scan, scans only), process-wide."""
+    code = {"default": 0, "lookback": 1, "rts": 2, "pipelined": 3, "l2": 4}[mode]
     _lib.check(load().devscan_set_carry_mode(code), "devscan_set_carry_mode")
 
 

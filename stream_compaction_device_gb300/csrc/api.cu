@@ -414,7 +414,8 @@ devscan_status devscan_stream_release(cudaStream_t stream)
 
 devscan_status devscan_set_carry_mode(int mode)
 {
-    if (mode != kCarryDefault && mode != kCarryLookback && mode != kCarryReduceThenScan && mode != kCarryPipelined)
+    if (mode != kCarryDefault && mode != kCarryLookback && mode != kCarryReduceThenScan && mode != kCarryPipelined &&
+        mode != kCarryL2Resident)
         return DEVSCAN_ERR_INVALID;
     g_carry_mode.store(mode, std::memory_order_relaxed);
     return DEVSCAN_OK;

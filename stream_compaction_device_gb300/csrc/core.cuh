@@ -89,9 +89,12 @@ struct DevState {
     unsigned ticket;
     unsigned error;
     unsigned cursor;
-    unsigned pad[12];
+    unsigned grid_arrive;   // blocks that reached the grid barrier (L2-resident scan)
+    unsigned grid_depart;   // blocks that left it; the last one resets both
+    unsigned pad[10];
     unsigned zeros[48];
 };
+static_assert(sizeof(DevState) == 256, "DevState is 256 bytes in every workspace layout");
 
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kEpochTags = (1u << 30) - 1u;   // tags 1 .. 2^30 - 1

@@ -29,7 +29,8 @@ constexpr int kMaxTile = 4096;   // largest of the three (workspace sizing)
 constexpr bool kUseTickets = true;
 
 constexpr int kOpAdd = 0, kOpMax = 1, kOpXor = 2;
-constexpr int kCarryDefault = 0, kCarryLookback = 1, kCarryReduceThenScan = 2, kCarryPipelined = 3;
+constexpr int kCarryDefault = 0, kCarryLookback = 1, kCarryReduceThenScan = 2, kCarryPipelined = 3,
+              kCarryL2Resident = 4;
 
 enum class ElemType { I32, U32, F32 };
 
@@ -83,6 +84,11 @@ cudaError_t launch_compact_gt(const int32_t *in, int32_t threshold, int32_t *out
 // answers in result[0..1]; clears result first (stream-ordered).
 cudaError_t launch_bracket(const int32_t *in, int32_t *out, int32_t *result, size_t n, int carry,
                            const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
+// Scan of an input that fits in L2: one cooperative launch, one block per SM
+// (16-byte-aligned in/out).
+cudaError_t launch_scan_l2_resident(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
+                                   const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
 // Segmented scan: heads[i] != 0 starts a segment at i.
 cudaError_t launch_segscan(ElemType type, int op, bool inclusive, const void *in, const uint8_t *heads, void *out,

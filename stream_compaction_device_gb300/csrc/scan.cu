@@ -185,7 +185,12 @@ cudaError_t launch_lookback(const void *in, void *out, size_t n, const Workspace
 // warps beat two (by 3-4%); deeper prefetch and more records overflow what
 // L2 keeps.
 constexpr unsigned kWaitLimit = 1u << 18;   // bounded mbarrier polls (~1 us each at most)
-constexpr size_t kPipelineMinN = size_t(1) << 19;
+constexpr size_t kPipelineMinN = size_t(1) << 20;
+// Sizes the L2-resident scan takes by default: measured on GB300 (L2 flushed
+// between calls) it beats the one-tile kernel from 2^17 and the pipeline up
+// to 2^23 by 10-20%, ties at 2^24 and loses above, once the input no longer
+// stays in L2 between its two reads.
+constexpr size_t kL2ResidentMinN = size_t(1) << 17, kL2ResidentMaxN = size_t(3) << 22;
 
 template <class Op, bool INCLUSIVE>
 cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,
@@ -232,7 +237,7 @@ cudaError_t dispatch_op(const void *in, void *out, size_t n, bool aligned, int c
                         unsigned spin_limit, cudaStream_t s)
 {
     if (carry == kCarryReduceThenScan && aligned) return launch_rts<Op, INCLUSIVE>(in, out, n, ws, s);
-    // below ~2^19 elements the pipeline's fill latency outweighs its
+    // up to 2^19 elements the pipeline's fill latency outweighs its
     // bandwidth: one tile per block is faster there (measured on GB300)
     const bool pipelined = aligned && (carry == kCarryPipelined || (carry == kCarryDefault && n >= kPipelineMinN));
     if (pipelined) return launch_pipelined<Op, INCLUSIVE>(in, out, n, ws, spin_limit, s);
@@ -253,6 +258,10 @@ cudaError_t dispatch_dir(const void *in, void *out, size_t n, bool inclusive, bo
 cudaError_t launch_scan(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
                         bool aligned, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
 {
+    // inputs that fit in L2: one cooperative launch (scan_l2res.cu)
+    if (aligned && (carry == kCarryL2Resident ||
+                    (carry == kCarryDefault && n >= kL2ResidentMinN && n <= kL2ResidentMaxN)))
+        return launch_scan_l2_resident(type, op, inclusive, in, out, n, ws, spin_limit, s);
     switch (type) {
     case ElemType::I32:
         if (op == kOpAdd) return dispatch_dir<AddU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);

@@ -1,0 +1,234 @@
+// L2-resident scan for inputs that fit in L2 (sm_103a): one cooperative
+// launch, one block per SM, two phases around one grid barrier.
+//
+// geek-doc.cn "并行前缀和 scan ..." section 四: reduce the blocks, scan the
+// block totals, add the offsets -- here in a single launch.  GB300's L2
+// (about 126 MB) holds the whole input of a mid-size scan (2^24 four-byte
+// elements are 64 MB), so the second read of the classic reduce-then-scan is
+// an L2 hit and HBM still moves 2 * n * sizeof(T) bytes:
+//   phase 1  block b folds its contiguous chunk (loads marked evict_last, so
+//            the chunk stays in L2) and stores its total in block_sums[b];
+//   barrier  every block arrives at a grid-wide counter (a bounded wait that
+//            records a timeout in the error word);
+//   phase 2  block b folds block_sums[0 .. b) in a fixed order (its offset),
+//            re-reads its chunk from L2 and scans it tile by tile, carrying
+//            the running prefix, with streaming stores.
+// There is no per-tile look-back chain, so a launch costs one barrier and
+// two streams over the data instead of a pipeline's fill and drain; the fp32
+// result does not depend on timing.
+#include "core.cuh"
+#include "launch.h"
+
+namespace devscan {
+namespace {
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 128-bit load whose lines L2 keeps (evict_last).
+__device__ __forceinline__ uint4 ld_keep(const uint4 *p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// All `blocks` blocks meet here.  Returns false (and records a timeout) when
+// the wait runs out.
+__device__ bool grid_barrier(DevState *st, unsigned blocks, unsigned spin_limit)
+{
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();   // this block's total before its arrival
+        atomicAdd(&st->grid_arrive, 1u);
+        int ok = 1;
+        unsigned spins = 0;
+        while (ld_acquire(&st->grid_arrive) < blocks) {
+            if (++spins >= spin_limit) {
+                atomicOr(&st->error, kErrTimeout);
+                ok = 0;
+                break;
+            }
+            __nanosleep(spins < 64 ? 32 : 256);
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+// The last block to leave resets the counters for the next launch on the
+// stream (which cannot start before this one has ended).
+__device__ void grid_depart(DevState *st, unsigned blocks)
+{
+    if (threadIdx.x == 0 && atomicAdd(&st->grid_depart, 1u) == blocks - 1) {
+        st->grid_arrive = 0;
+        st->grid_depart = 0;
+    }
+}
+
+template <class Op, bool INCLUSIVE, int THREADS, int VECS>
+__global__ void __launch_bounds__(THREADS, 1)
+l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,
+                        size_t chunk, typename Op::S *__restrict__ block_sums, DevState *st, unsigned spin_limit)
+{
+    using S = typename Op::S;
+    constexpr int NWARPS = THREADS / 32;
+    constexpr int WARP_ITEMS = 32 * 4 * VECS;
+    constexpr int TILE = THREADS * 4 * VECS;
+    __shared__ S s_warp[2][NWARPS];
+    __shared__ S s_carry;
+    const Op op;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned blocks = gridDim.x;
+    const size_t begin = static_cast<size_t>(blockIdx.x) * chunk;
+    const size_t end = begin + chunk < n ? begin + chunk : n;
+
+    // ---- phase 1: the chunk's total; its lines stay in L2
+    const uint64_t keep = policy_evict_last();
+    S acc = Op::identity();
+    for (size_t t0 = begin; t0 < end; t0 += TILE) {
+        const size_t wb = t0 + static_cast<size_t>(warp) * WARP_ITEMS;
+        if (t0 + TILE <= end) {
+#pragma unroll
+            for (int r = 0; r < VECS; ++r) {
+                const uint4 q = ld_keep(reinterpret_cast<const uint4 *>(in + wb) + r * 32 + lane, keep);
+                acc = op(acc, op(op(from_bits<S>(q.x), from_bits<S>(q.y)), op(from_bits<S>(q.z), from_bits<S>(q.w))));
+            }
+        } else {
+            for (int r = 0; r < VECS; ++r)
+                for (int j = 0; j < 4; ++j) {
+                    const size_t e = wb + static_cast<size_t>((r * 32 + lane) * 4 + j);
+                    if (e < end) acc = op(acc, in[e]);
+                }
+        }
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) acc = op(acc, __shfl_xor_sync(kFullMask, acc, d));
+    if (lane == 0) s_warp[0][warp] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        S v = lane < NWARPS ? s_warp[0][lane] : Op::identity();
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
+        if (lane == 0) block_sums[blockIdx.x] = v;
+    }
+
+    const bool ok = grid_barrier(st, blocks, spin_limit);
+
+    // ---- phase 2: this block's offset, then its chunk scanned tile by tile
+    if (warp == 0) {
+        S v = Op::identity();
+        if (ok)
+            for (unsigned b = lane; b < blockIdx.x; b += 32) v = op(v, __ldcg(block_sums + b));   // through L2
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
+        if (lane == 0) s_carry = v;
+    }
+    __syncthreads();
+    S carry = s_carry;
+    unsigned parity = 0;
+    for (size_t t0 = begin; t0 < end; t0 += TILE, parity ^= 1u) {
+        const size_t wb = t0 + static_cast<size_t>(warp) * WARP_ITEMS;
+        const bool full = t0 + TILE <= end;
+        S x[VECS][4];
+        load_rows<S, VECS, true>(in, wb, end, lane, full, x, Op::identity());
+        S tt[VECS];
+#pragma unroll
+        for (int r = 0; r < VECS; ++r) tt[r] = op(op(x[r][0], x[r][1]), op(x[r][2], x[r][3]));
+        S row_excl[VECS], warp_total;
+        warp_scan_rows<Op, VECS>(op, tt, lane, row_excl, warp_total);
+        if (lane == 0) s_warp[parity][warp] = warp_total;
+        __syncthreads();   // two buffers: the next tile writes the other one
+        S warp_excl, tile_total;
+        block_scan_warps<Op, NWARPS>(op, s_warp[parity], warp, lane, warp_excl, tile_total);
+        const S pfx = op(carry, warp_excl);
+#pragma unroll
+        for (int r = 0; r < VECS; ++r) {
+            S cur = op(pfx, row_excl[r]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const S v = x[r][k];
+                if (INCLUSIVE) {
+                    cur = op(cur, v);
+                    x[r][k] = cur;
+                } else {
+                    x[r][k] = cur;
+                    cur = op(cur, v);
+                }
+            }
+        }
+        store_rows<S, VECS, true>(out, wb, end, lane, full, x);
+        carry = op(carry, tile_total);
+    }
+    grid_depart(st, blocks);
+}
+
+template <class Op, bool INCLUSIVE, int VECS>
+cudaError_t launch_l2res(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,
+                         cudaStream_t s)
+{
+    using S = typename Op::S;
+    constexpr int THREADS = 1024;
+    constexpr size_t TILE = static_cast<size_t>(THREADS) * 4 * VECS;
+    const size_t tiles = (n + TILE - 1) / TILE;
+    size_t blocks = tiles < static_cast<size_t>(ws.num_sms) ? tiles : static_cast<size_t>(ws.num_sms);
+    const size_t chunk = ((tiles + blocks - 1) / blocks) * TILE;
+    blocks = (n + chunk - 1) / chunk;   // no block without work
+    const S *sin = static_cast<const S *>(in);
+    S *sout = static_cast<S *>(out);
+    S *sums = reinterpret_cast<S *>(ws.tile_sums);
+    DevState *st = ws.state;
+    void *args[] = {&sin, &sout, &n, const_cast<size_t *>(&chunk), &sums, &st, &spin_limit};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(&l2_resident_scan_kernel<Op, INCLUSIVE, THREADS, VECS>),
+                                       dim3(static_cast<unsigned>(blocks)), dim3(THREADS), args, 0, s);
+}
+
+template <class Op>
+cudaError_t launch_l2res_dir(bool inclusive, const void *in, void *out, size_t n, const Workspace &ws,
+                             unsigned spin_limit, cudaStream_t s)
+{
+    // small inputs take 4,096-element tiles so that more blocks share them
+    if (n >= (size_t(1) << 21))
+        return inclusive ? launch_l2res<Op, true, 4>(in, out, n, ws, spin_limit, s)
+                         : launch_l2res<Op, false, 4>(in, out, n, ws, spin_limit, s);
+    return inclusive ? launch_l2res<Op, true, 1>(in, out, n, ws, spin_limit, s)
+                     : launch_l2res<Op, false, 1>(in, out, n, ws, spin_limit, s);
+}
+
+}  // namespace
+
+cudaError_t launch_scan_l2_resident(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
+                                   const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+{
+    switch (type) {
+    case ElemType::I32:
+        if (op == kOpAdd) return launch_l2res_dir<AddU32>(inclusive, in, out, n, ws, spin_limit, s);
+        if (op == kOpMax) return launch_l2res_dir<MaxI32>(inclusive, in, out, n, ws, spin_limit, s);
+        return launch_l2res_dir<XorU32>(inclusive, in, out, n, ws, spin_limit, s);
+    case ElemType::U32:
+        if (op == kOpAdd) return launch_l2res_dir<AddU32>(inclusive, in, out, n, ws, spin_limit, s);
+        if (op == kOpMax) return launch_l2res_dir<MaxU32>(inclusive, in, out, n, ws, spin_limit, s);
+        return launch_l2res_dir<XorU32>(inclusive, in, out, n, ws, spin_limit, s);
+    case ElemType::F32:
+        if (op == kOpAdd) return launch_l2res_dir<AddF32>(inclusive, in, out, n, ws, spin_limit, s);
+        return launch_l2res_dir<MaxF32>(inclusive, in, out, n, ws, spin_limit, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace devscan

@@ -94,21 +94,21 @@ def test_int32_wraps(ds):
     check(ds, x, "add", False)
 
 
-@pytest.mark.parametrize("mode", ["lookback", "rts", "pipelined"])
+@pytest.mark.parametrize("mode", ["lookback", "rts", "pipelined", "l2"])
 def test_carry_modes(ds, mode):
     """Every inter-block carry path gives the oracle's results."""
     from stream_compaction_device_gb300 import workloads as wl
     ds.set_carry_mode(mode)
     try:
         for dtype, op in CASES:
-            for n in (1, 5, TILE, 2 * TILE + 1, 8192 * 3 + 7, 1_000_003):
+            for n in (1, 5, TILE, 2 * TILE + 1, 8192 * 3 + 7, 16384 * 152 + 9, 1_000_003, (1 << 21) + 17):
                 for inclusive in (True, False):
                     check(ds, wl.random_input(dtype, n, n + 1, op), op, inclusive)
     finally:
         ds.set_carry_mode("default")
 
 
-@pytest.mark.parametrize("mode", ["default", "lookback"])
+@pytest.mark.parametrize("mode", ["default", "lookback", "l2"])
 def test_repeated_runs_identical(ds, mode):
     """Integer results do not depend on block timing: 50 launches, one answer."""
     from stream_compaction_device_gb300 import workloads as wl
