@@ -185,14 +185,15 @@ devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_
  * ------------------------------------------------------------------------- */
 devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStream_t stream);
 
-/* LSD radix sort of uint32 keys by 4-bit digits: 8 passes (P1 section 一:
+/* LSD radix sort of uint32 keys by 8-bit digits: 4 passes (P1 section 一:
  * a round may take "one or several bits"; P2 section 4.2: per-digit counts,
- * a prefix over them, then the scatter).  Each pass counts the 16 digit
- * values of every 4,096-key tile, scans the digit-major count array with the
+ * a prefix over them, then the scatter).  Each pass counts the 256 digit
+ * values of every 8,192-key tile, scans the digit-major count array with the
  * library's exclusive add-scan (giving every (digit, tile) run its output
- * position), and scatters each tile's keys stably as 16 contiguous runs.
- * Same arguments and result as radix_sort_u32; a per-stream scratch of
- * n / 256 words holds the counts (allocated stream-ordered on first use). */
+ * position), and scatters each tile's keys stably as one contiguous run per
+ * digit.  Same arguments and result as radix_sort_u32 (the result is in
+ * keys; n at most INT32_MAX); a per-stream scratch of n / 32 words holds the
+ * counts (allocated stream-ordered on first use). */
 devscan_status radix_sort_digits_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------

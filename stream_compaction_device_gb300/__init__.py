@@ -192,8 +192,8 @@ def radix_sort(keys: torch.Tensor, tmp: torch.Tensor | None = None, stream=None)
 
 
 def radix_sort_digits(keys: torch.Tensor, tmp: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """In-place ascending sort of 32-bit keys (bits read as uint32) by 8
-    passes of 4-bit digits; ``tmp`` is a same-size scratch tensor."""
+    """In-place ascending sort of 32-bit keys (bits read as uint32) by 4
+    passes of 8-bit digits; ``tmp`` is a same-size scratch tensor."""
     _check_cuda(keys, "keys")
     if keys.element_size() != 4 or keys.is_floating_point():
         raise TypeError("keys must be a 32-bit integer tensor (bits read as uint32)")

@@ -352,7 +352,7 @@ devscan_status radix_sort_digits_u32(uint32_t *keys, uint32_t *tmp, size_t n, cu
     st = acquire_extra(stream, hist_words * sizeof(uint32_t), &hist);
     if (st != DEVSCAN_OK) return st;
     uint32_t *src = keys, *dst = tmp;
-    for (int pass = 0; pass < 8; ++pass) {
+    for (int pass = 0; pass < kRadixPasses; ++pass) {
         if (launch_radix_pass(src, dst, n, pass, static_cast<uint32_t *>(hist), ws, kSpinLimit, stream) != cudaSuccess)
             return DEVSCAN_ERR_CUDA;
         std::swap(src, dst);

@@ -94,8 +94,11 @@ cudaError_t launch_scan_l2_resident(ElemType type, int op, bool inclusive, const
 cudaError_t launch_segscan(ElemType type, int op, bool inclusive, const void *in, const uint8_t *heads, void *out,
                            size_t n, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
-// One 4-bit-digit LSD radix pass (digit `pass`, bits 4 pass .. 4 pass + 3)
-// from src to dst; `hist` holds radix_hist_words(n) words of scratch.
+// Digit width and passes of the multi-bit LSD radix sort.
+constexpr int kRadixDigitBits = 8, kRadixPasses = 32 / kRadixDigitBits;
+
+// One LSD radix pass (digit `pass`, bits kRadixDigitBits * pass and up) from
+// src to dst; `hist` holds radix_hist_words(n) words of scratch.
 cudaError_t launch_radix_pass(const uint32_t *src, uint32_t *dst, size_t n, int pass, uint32_t *hist,
                               const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 size_t radix_hist_words(size_t n);

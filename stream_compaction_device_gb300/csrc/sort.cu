@@ -1,181 +1,204 @@
-// Multi-bit LSD radix sort of uint32 keys, 4-bit digits, 8 passes (sm_103a).
+// Multi-bit LSD radix sort of uint32 keys: 8-bit digits, 4 passes (sm_103a).
 //
 // geek-doc.cn "并行前缀和 scan ..." section 一: radix sort rounds take "one or
 // several bits", and the core of each round is a scan; lpnh.cn "并行扫描"
 // section 4.2: per-digit counts, a prefix over them, then the scatter.
 //
-// One pass over digit p (bits 4p .. 4p+3):
-//   1. radix_hist_kernel: every tile of 4,096 keys counts its 16 digit
+// One pass over digit p (bits 8p .. 8p+7):
+//   1. radix_hist_kernel: every tile of 8,192 keys counts its 256 digit
 //      values and stores them digit-major: hist[d * tiles + tile];
-//   2. an exclusive add-scan of that array (the library's own scan) turns it
-//      into every (digit, tile) run's first output position: all keys of
-//      smaller digits, plus the keys of digit d in earlier tiles;
-//   3. radix_scatter_kernel: every tile ranks its keys stably by digit
-//      (private per-thread digit counters in shared memory, then one block
-//      scan over them in digit-major order), stages the tile sorted by digit
-//      and writes its 16 runs, each contiguous in the output.
-// Traffic: 12 bytes per key per pass (read, read, write) instead of the
-// 8 bytes x 32 passes of the one-bit split sort.
+//   2. an exclusive add-scan of that array (the library's own scan; at 2^26
+//      keys it is 2M counts, which the L2-resident scan takes) turns it into
+//      every (digit, tile) run's first output position: all keys of smaller
+//      digits, plus the keys of digit d in earlier tiles;
+//   3. radix_scatter_kernel: every tile ranks its keys stably by digit -- rows
+//      of 32 consecutive keys in input order, eight ballots grouping the
+//      lanes with equal digits, one counter row per warp in shared memory --
+//      stages the tile sorted by digit and writes each digit's keys as one
+//      contiguous run.
+// Traffic: 12 bytes per key per pass (count read, scatter read and write),
+// 48 per key for the sort, against 260 for the 32 one-bit splits.
 #include "core.cuh"
 #include "launch.h"
 
 namespace devscan {
 
-constexpr int kSortThreads = 256;
-constexpr int kSortItems = 16;   // keys per thread, contiguous (blocked layout)
-constexpr int kSortTile = kSortThreads * kSortItems;   // 4,096
-constexpr int kDigits = 16;
+constexpr int kSortThreads = 512;
+constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortRows = 16;                          // rows of 32 keys per warp
+constexpr int kSortTile = kSortThreads * kSortRows;    // 8,192 keys
+constexpr int kSortBuckets = 1 << kRadixDigitBits;     // 256
 
-__device__ __forceinline__ unsigned digit_of(uint32_t key, int shift) { return (key >> shift) & 15u; }
+__device__ __forceinline__ unsigned digit_of(uint32_t key, int shift) { return (key >> shift) & (kSortBuckets - 1); }
 
-// Blocked load: thread t takes keys [16 t, 16 t + 16) of the tile.  Keys past
-// n are flagged invalid.
-__device__ __forceinline__ void load_blocked(const uint32_t *__restrict__ keys, size_t base, size_t n, int tid,
-                                             bool aligned, uint32_t (&k)[kSortItems])
+// Lanes whose 8-bit digit equals this lane's, built from one ballot per digit
+// bit (the hardware match instruction measured far slower here); `valid`:
+// this row's lanes that hold a key.
+__device__ __forceinline__ unsigned match_digit(unsigned d, unsigned valid)
 {
-    const size_t e0 = base + static_cast<size_t>(tid) * kSortItems;
-    if (aligned && e0 + kSortItems <= n) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(keys + e0);
+    unsigned eq = valid;
 #pragma unroll
-        for (int v = 0; v < kSortItems / 4; ++v) {
-            const uint4 q = ld_stream(p + v);
-            k[4 * v] = q.x;
-            k[4 * v + 1] = q.y;
-            k[4 * v + 2] = q.z;
-            k[4 * v + 3] = q.w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < kSortItems; ++j) k[j] = (e0 + j < n) ? keys[e0 + j] : 0u;
+    for (int b = 0; b < kRadixDigitBits; ++b) {
+        const unsigned bit = (d >> b) & 1u;
+        const unsigned set = __ballot_sync(kFullMask, bit);
+        eq &= bit ? set : ~set;
     }
+    return eq;
 }
 
-// hist[d * tiles + tile] = number of keys of the tile whose digit is d.
+__device__ __forceinline__ unsigned lanemask_lt()
+{
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// hist[d * tiles + tile] = number of keys of the tile whose digit is d.  The
+// count does not depend on the order, so each thread takes 16 consecutive
+// keys with 128-bit loads; one shared counter row per pair of warps.
 __global__ void __launch_bounds__(kSortThreads)
 radix_hist_kernel(const uint32_t *__restrict__ keys, size_t n, int shift, unsigned tiles, uint32_t *__restrict__ hist,
                   bool aligned)
 {
-    __shared__ unsigned s_count[kDigits];
-    const int tid = threadIdx.x;
+    constexpr int COPIES = kSortWarps / 2;
+    __shared__ uint32_t s_h[COPIES][kSortBuckets];   // 8 KB
+    const int tid = threadIdx.x, warp = tid >> 5;
     const unsigned tile = blockIdx.x;
-    if (tid < kDigits) s_count[tid] = 0;
-    const size_t base = static_cast<size_t>(tile) * kSortTile;
-    uint32_t k[kSortItems];
-    load_blocked(keys, base, n, tid, aligned, k);
-    // 16 digit counts packed as 16-bit fields of 8 words (a thread counts at
-    // most 16 keys, a warp at most 512)
-    uint32_t c[kDigits / 2];
-#pragma unroll
-    for (int w = 0; w < kDigits / 2; ++w) c[w] = 0;
-    const size_t e0 = base + static_cast<size_t>(tid) * kSortItems;
-#pragma unroll
-    for (int j = 0; j < kSortItems; ++j) {
-        if (e0 + j < n) {
-            const unsigned d = digit_of(k[j], shift);
-            const uint32_t inc = 1u << ((d & 1u) * 16);
-#pragma unroll
-            for (int w = 0; w < kDigits / 2; ++w) c[w] += (d >> 1 == static_cast<unsigned>(w)) ? inc : 0u;
-        }
-    }
-#pragma unroll
-    for (int w = 0; w < kDigits / 2; ++w)
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) c[w] += __shfl_xor_sync(kFullMask, c[w], o);
+    for (int i = tid; i < COPIES * kSortBuckets; i += kSortThreads) (&s_h[0][0])[i] = 0;
     __syncthreads();
-    if ((tid & 31) == 0) {
+    uint32_t *h = s_h[warp >> 1];
+    const size_t e0 = static_cast<size_t>(tile) * kSortTile + static_cast<size_t>(tid) * kSortRows;
+    if (aligned && e0 + kSortRows <= n) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(keys + e0);
 #pragma unroll
-        for (int w = 0; w < kDigits / 2; ++w) {
-            atomicAdd(&s_count[2 * w], c[w] & 0xffffu);
-            atomicAdd(&s_count[2 * w + 1], c[w] >> 16);
+        for (int v = 0; v < kSortRows / 4; ++v) {
+            const uint4 q = __ldcs(p + v);
+            atomicAdd(&h[digit_of(q.x, shift)], 1u);
+            atomicAdd(&h[digit_of(q.y, shift)], 1u);
+            atomicAdd(&h[digit_of(q.z, shift)], 1u);
+            atomicAdd(&h[digit_of(q.w, shift)], 1u);
         }
+    } else {
+        for (int j = 0; j < kSortRows; ++j)
+            if (e0 + j < n) atomicAdd(&h[digit_of(keys[e0 + j], shift)], 1u);
     }
     __syncthreads();
-    if (tid < kDigits) hist[static_cast<size_t>(tid) * tiles + tile] = s_count[tid];
+    if (tid < kSortBuckets) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int w = 0; w < COPIES; ++w) c += s_h[w][tid];
+        hist[static_cast<size_t>(tid) * tiles + tile] = c;
+    }
 }
 
-__global__ void __launch_bounds__(kSortThreads)
-radix_scatter_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size_t n, int shift,
-                     unsigned tiles, const uint32_t *__restrict__ run_start, bool aligned)
+// Exclusive scan of one value per thread over threads 0 .. 255 of the block
+// (every thread must call it; the others pass 0); uses s_tmp[8].
+__device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *s_tmp, int tid)
 {
-    constexpr int NWARPS = kSortThreads / 32;
-    // private digit counters: column tid of row d; scanned in place
-    __shared__ uint32_t s_cnt[kDigits * kSortThreads];
-    __shared__ uint32_t s_keys[kSortTile];
-    __shared__ uint32_t s_warp[NWARPS];
-    __shared__ uint32_t s_start[kDigits], s_tbase[kDigits + 1];
+    const int lane = tid & 31, warp = tid >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
+        if (lane >= d) inc += u;
+    }
+    if (warp < kSortBuckets / 32 && lane == 31) s_tmp[warp] = inc;
+    __syncthreads();
+    uint32_t base = 0;
+    if (warp < kSortBuckets / 32)
+        for (int w = 0; w < warp; ++w) base += s_tmp[w];
+    __syncthreads();
+    return base + inc - v;
+}
+
+// keys_in -> keys_out by the digit at `shift`; run_start[d * tiles + tile]:
+// the first output position of the tile's keys of digit d.
+__global__ void __launch_bounds__(kSortThreads, 2)
+radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict__ keys_out, size_t n, int shift,
+                     unsigned tiles, const uint32_t *__restrict__ run_start)
+{
+    // per-warp digit counters; then each (warp, digit)'s first staged position
+    __shared__ uint32_t s_wcount[kSortWarps][kSortBuckets];   // 16 KB
+    __shared__ uint32_t s_keys[kSortTile];                     // 32 KB: the tile sorted by digit
+    __shared__ uint32_t s_delta[kSortBuckets];                 // output position - staged position, per digit
+    __shared__ uint32_t s_tmp[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned tile = blockIdx.x;
     const size_t base = static_cast<size_t>(tile) * kSortTile;
+    const size_t wbase = base + static_cast<size_t>(warp) * (kSortRows * 32);
     const unsigned len = (n - base < static_cast<size_t>(kSortTile)) ? static_cast<unsigned>(n - base) : kSortTile;
 
+    for (int i = tid; i < kSortWarps * kSortBuckets; i += kSortThreads) (&s_wcount[0][0])[i] = 0;
+    if (tid < kSortBuckets) s_delta[tid] = run_start[static_cast<size_t>(tid) * tiles + tile];   // the run's start
+    // keys of this warp's 512 that exist (the last tile is ragged)
+    const unsigned wlen = n > wbase ? static_cast<unsigned>(n - wbase < 512 ? n - wbase : 512) : 0u;
+    uint32_t key[kSortRows];
 #pragma unroll
-    for (int d = 0; d < kDigits; ++d) s_cnt[d * kSortThreads + tid] = 0;
-    if (tid < kDigits) s_start[tid] = run_start[static_cast<size_t>(tid) * tiles + tile];
-    uint32_t k[kSortItems];
-    unsigned long long loc = 0;   // 16 x 4-bit local offsets (each < 16)
-    load_blocked(keys, base, n, tid, aligned, k);
-    // local offset of each key among this thread's earlier keys of its digit
-    // (a thread's own column: no other thread touches it)
+    for (int r = 0; r < kSortRows; ++r) {
+        const unsigned i = static_cast<unsigned>(r * 32 + lane);
+        key[r] = (i < wlen) ? __ldcs(keys_in + wbase + i) : 0u;
+    }
+    __syncthreads();
+
+    // rank within the warp: row by row (input order), equal digits grouped;
+    // two rows' ranks (below 512) share a register's 16-bit halves
+    uint32_t rank2[kSortRows / 2];
 #pragma unroll
-    for (int j = 0; j < kSortItems; ++j) {
-        if (static_cast<unsigned>(tid * kSortItems + j) < len) {
-            const unsigned d = digit_of(k[j], shift);
-            const uint32_t o = s_cnt[d * kSortThreads + tid];
-            s_cnt[d * kSortThreads + tid] = o + 1;
-            loc |= static_cast<unsigned long long>(o) << (4 * j);
+    for (int r = 0; r < kSortRows / 2; ++r) rank2[r] = 0;
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int r = 0; r < kSortRows; ++r) {
+        const bool has = static_cast<unsigned>(r * 32 + lane) < wlen;
+        const unsigned d = digit_of(key[r], shift);
+        const unsigned same = match_digit(d, __ballot_sync(kFullMask, has));
+        const int leader = has ? __ffs(same) - 1 : lane;
+        uint32_t before = 0;
+        if (has && lane == leader) {
+            before = s_wcount[warp][d];
+            s_wcount[warp][d] = before + __popc(same);
+        }
+        before = __shfl_sync(kFullMask, before, leader);
+        rank2[r / 2] |= (before + __popc(same & lt)) << (16 * (r & 1));
+    }
+    __syncthreads();
+
+    // per digit (thread d): the tile's count, the digit's first staged
+    // position, then every warp's first staged position for the digit (one
+    // lookup per key below) and the output shift of the digit's run
+    uint32_t count = 0;
+    if (tid < kSortBuckets) {
+#pragma unroll
+        for (int w = 0; w < kSortWarps; ++w) count += s_wcount[w][tid];
+    }
+    const uint32_t start = excl_scan_256(tid < kSortBuckets ? count : 0u, s_tmp, tid);
+    if (tid < kSortBuckets) {
+        uint32_t at = start;
+#pragma unroll
+        for (int w = 0; w < kSortWarps; ++w) {
+            const uint32_t c = s_wcount[w][tid];
+            s_wcount[w][tid] = at;
+            at += c;
+        }
+        s_delta[tid] -= start;   // output start - staged start (wraps as an unsigned offset)
+    }
+    __syncthreads();
+
+    // stage sorted by digit (stable: warp order, then row order, then lane)
+#pragma unroll
+    for (int r = 0; r < kSortRows; ++r) {
+        if (static_cast<unsigned>(r * 32 + lane) < wlen) {
+            const unsigned d = digit_of(key[r], shift);
+            s_keys[s_wcount[warp][d] + ((rank2[r / 2] >> (16 * (r & 1))) & 0xffffu)] = key[r];
         }
     }
     __syncthreads();
 
-    // exclusive scan of s_cnt in digit-major order: warp w scans words
-    // [512 w, 512 w + 512) row by row (lane l reads word 32 r + l: no bank
-    // conflicts), carrying the row totals; warp totals through shared memory
-    {
-        const int seg = warp * (kDigits * kSortThreads / NWARPS);
-        uint32_t carry = 0;
-#pragma unroll 4
-        for (int r = 0; r < kDigits * kSortThreads / NWARPS / 32; ++r) {
-            const uint32_t v = s_cnt[seg + 32 * r + lane];
-            uint32_t inc = v;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
-                if (lane >= d) inc += u;
-            }
-            s_cnt[seg + 32 * r + lane] = carry + inc - v;
-            carry += __shfl_sync(kFullMask, inc, 31);
-        }
-        if (lane == 0) s_warp[warp] = carry;
-    }
-    __syncthreads();
-    {
-        uint32_t wex = 0;
-#pragma unroll
-        for (int w = 0; w < NWARPS; ++w) wex += (w < warp) ? s_warp[w] : 0u;
-        const int seg = warp * (kDigits * kSortThreads / NWARPS);
-        for (int r = 0; r < kDigits * kSortThreads / NWARPS / 32; ++r) s_cnt[seg + 32 * r + lane] += wex;
-    }
-    __syncthreads();
-    if (tid <= kDigits) s_tbase[tid] = (tid < kDigits) ? s_cnt[tid * kSortThreads] : len;
-
-    // stage the tile sorted by digit (stable: digit-major, then thread,
-    // then a thread's own order)
-#pragma unroll
-    for (int j = 0; j < kSortItems; ++j) {
-        if (static_cast<unsigned>(tid * kSortItems + j) < len) {
-            const unsigned d = digit_of(k[j], shift);
-            s_keys[s_cnt[d * kSortThreads + tid] + static_cast<uint32_t>((loc >> (4 * j)) & 15u)] = k[j];
-        }
-    }
-    __syncthreads();
-
-    // write the 16 runs: staged key i of digit d goes to
-    // run_start[d, tile] + (i - first staged position of d)
+    // each digit's keys as one run: staged key i of digit d goes to
+    // i + (first output position - first staged position of d)
     for (unsigned i = tid; i < len; i += kSortThreads) {
-        const uint32_t key = s_keys[i];
-        const unsigned d = digit_of(key, shift);
-        const size_t dst = static_cast<size_t>(s_start[d]) + (i - s_tbase[d]);
-        if (dst < n) out[dst] = key;
+        const uint32_t k = s_keys[i];
+        const size_t dst = static_cast<uint32_t>(i + s_delta[digit_of(k, shift)]);
+        if (dst < n) __stcs(keys_out + dst, k);
     }
 }
 
@@ -183,18 +206,18 @@ cudaError_t launch_radix_pass(const uint32_t *src, uint32_t *dst, size_t n, int 
                               const Workspace &ws, unsigned spin_limit, cudaStream_t s)
 {
     const unsigned tiles = tiles_for(n, kSortTile);
-    const int shift = 4 * pass;
+    const int shift = kRadixDigitBits * pass;
     const bool aligned = reinterpret_cast<uintptr_t>(src) % 16 == 0;
     radix_hist_kernel<<<tiles, kSortThreads, 0, s>>>(src, n, shift, tiles, hist, aligned);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_scan(ElemType::U32, kOpAdd, false, hist, hist, static_cast<size_t>(tiles) * kDigits,
+    e = launch_scan(ElemType::U32, kOpAdd, false, hist, hist, static_cast<size_t>(tiles) * kSortBuckets,
                     reinterpret_cast<uintptr_t>(hist) % 16 == 0, kCarryDefault, ws, spin_limit, s);
     if (e != cudaSuccess) return e;
-    radix_scatter_kernel<<<tiles, kSortThreads, 0, s>>>(src, dst, n, shift, tiles, hist, aligned);
+    radix_scatter_kernel<<<tiles, kSortThreads, 0, s>>>(src, dst, n, shift, tiles, hist);
     return cudaGetLastError();
 }
 
-size_t radix_hist_words(size_t n) { return static_cast<size_t>(tiles_for(n, kSortTile)) * kDigits; }
+size_t radix_hist_words(size_t n) { return static_cast<size_t>(tiles_for(n, kSortTile)) * kSortBuckets; }
 
 }  // namespace devscan
