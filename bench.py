@@ -9,12 +9,17 @@ is needed between steps.  Prints one JSON line:
   value      whole-job Gelem/s (all ranks' elements / max-over-ranks time)
   roofline   the scan kernel's algorithmic bytes (2 * N * 4 per launch) over
              its CUDA-event duration, against the measured HBM copy peak
-  e2e        the same scan from pinned host memory: host-to-device copy,
-             scan, device-to-host copy of the result, every step
+  e2e        the same scan from pinned host memory through scan_host:
+             host-to-device copy, scan, device-to-host copy of the result,
+             every step; steps alternate between two streams, so one step's
+             download overlaps the next one's upload
   cpu_baseline  the serial CPU oracle on the host cores (1 thread)
-  extra      compaction at N = 2^26 (1/50/99 %), the max / xor sweep at
-             N = 2^28, fp32 add at N = 2^24, N = 65,536 latency, split and
-             the 32-pass radix sort at N = 2^26, and the reduce-then-scan carry
+  extra      the inclusive / max / xor sweep, the bracket check and bracket
+             scan and the segmented scan at N = 2^28; compaction (flags and
+             fused predicate), the split, the 32-pass and the 8-bit radix
+             sorts at N = 2^26; fp32 add at N = 2^24; N = 65,536 latency; the
+             reduce-then-scan carry.  Back-to-back calls between one pair of
+             events (device time per call), except the rows that flush L2
 
 ``--impl reference`` times the CPU oracle instead (the reference arm): each
 step is the oracle's serial exclusive scan of a 2^22-element sample of the
@@ -266,22 +271,30 @@ def run_ours(args):
     # end to end from pinned host memory through the public API
     e2e = None
     if not args.no_e2e:
+        # steps alternate between two streams (each with its own device and
+        # pinned output buffers), so one step's download overlaps the next
+        # step's upload, as a user streaming batches would run it; every step
+        # still moves its whole input up and its whole result down
         h_in = torch.from_numpy(x_host).pin_memory()
-        h_out = torch.empty_like(h_in).pin_memory()
-        e2e_steps = max(3, min(20, args.steps))
-        for _ in range(2):
-            ds.scan_host(h_in, inclusive=False, out_host=h_out, work=(d_in, d_out))
+        h_outs = [torch.empty_like(h_in).pin_memory() for _ in range(2)]
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        works = [(d_in, d_out), (torch.empty_like(d_in), torch.empty_like(d_out))]
+        e2e_steps = max(4, min(20, args.steps))
+        for j in range(2):
+            ds.scan_host(h_in, inclusive=False, out_host=h_outs[j], work=works[j], stream=streams[j])
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            ds.scan_host(h_in, inclusive=False, out_host=h_out, work=(d_in, d_out))
+        for i in range(e2e_steps):
+            j = i % 2
+            ds.scan_host(h_in, inclusive=False, out_host=h_outs[j], work=works[j], stream=streams[j],
+                         synchronize=False)
         torch.cuda.synchronize()
         el = time.perf_counter() - t0
         el, u = aggregate(el, float(n) * e2e_steps, world, torch.device("cuda", local))
         e2e = {"value": round(u / el / 1e9, 3), "unit": "Gelem/s", "h2d_bytes_per_step": n * 4,
                "d2h_bytes_per_step": n * 4, "steps": e2e_steps}
-        del h_in, h_out
+        del h_in, h_outs, works
 
     extra = None
     if not args.no_extras and rank == 0:

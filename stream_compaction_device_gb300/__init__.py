@@ -206,11 +206,15 @@ def radix_sort_digits(keys: torch.Tensor, tmp: torch.Tensor | None = None, strea
 
 
 def scan_host(x_host: torch.Tensor, inclusive: bool = False, op: str = "add", device="cuda",
-              stream=None, out_host: torch.Tensor | None = None, work=None) -> torch.Tensor:
+              stream=None, out_host: torch.Tensor | None = None, work=None,
+              synchronize: bool = True) -> torch.Tensor:
     """Scan a host array end to end: host-to-device copy, device scan,
-    device-to-host copy, all ordered on ``stream``; returns once the result
-    is in ``out_host``.  Pinned host tensors make the copies asynchronous.
-    ``work`` may pass preallocated (device input, device output) tensors."""
+    device-to-host copy, all ordered on ``stream``.  Pinned host tensors make
+    the copies asynchronous.  ``work`` may pass preallocated (device input,
+    device output) tensors.  With ``synchronize`` (the default) it returns
+    once the result is in ``out_host``; without, it returns at once and the
+    result is there when ``stream`` has reached this point, so calls on two
+    streams overlap one call's download with the next one's upload."""
     if x_host.is_cuda:
         raise ValueError("x_host must be a host tensor")
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -225,7 +229,8 @@ def scan_host(x_host: torch.Tensor, inclusive: bool = False, op: str = "add", de
         if out_host is None:
             out_host = torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=x_host.is_pinned())
         out_host.copy_(d_out, non_blocking=True)
-    s.synchronize()
+    if synchronize:
+        s.synchronize()
     return out_host
 
 
