@@ -219,7 +219,7 @@ devscan_status devscan_stream_release(cudaStream_t stream);
  * three-phase "reduce, scan the block totals, add the offsets" scheme and
  * mentions chaining blocks inside one launch):
  *   0 = default: for 16-byte-aligned in/out the scans take 4 for
- *       2^17 <= n <= 3 * 2^22 and 3 above; compaction, the split, the
+ *       2^17 <= n <= 2^24 and 3 above; compaction, the split, the
  *       bracket scan and the segmented scan take 3 from n = 2^19; everything
  *       else takes 1;
  *   1 = one tile per block, single-pass decoupled look-back;

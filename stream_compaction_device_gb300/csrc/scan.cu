@@ -188,9 +188,9 @@ constexpr unsigned kWaitLimit = 1u << 18;   // bounded mbarrier polls (~1 us eac
 constexpr size_t kPipelineMinN = size_t(1) << 20;
 // Sizes the L2-resident scan takes by default: measured on GB300 (L2 flushed
 // between calls) it beats the one-tile kernel from 2^17 and the pipeline up
-// to 2^23 by 10-20%, ties at 2^24 and loses above, once the input no longer
-// stays in L2 between its two reads.
-constexpr size_t kL2ResidentMinN = size_t(1) << 17, kL2ResidentMaxN = size_t(3) << 22;
+// to 2^24 by 10-40%, and loses above, once the input no longer stays in L2
+// between its two reads.
+constexpr size_t kL2ResidentMinN = size_t(1) << 17, kL2ResidentMaxN = size_t(1) << 24;
 
 template <class Op, bool INCLUSIVE>
 cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,

@@ -5,16 +5,20 @@
 // block totals, add the offsets -- here in a single launch.  GB300's L2
 // (about 126 MB) holds the whole input of a mid-size scan (2^24 four-byte
 // elements are 64 MB), so the second read of the classic reduce-then-scan is
-// an L2 hit and HBM still moves 2 * n * sizeof(T) bytes:
-//   phase 1  block b folds its contiguous chunk (loads marked evict_last, so
-//            the chunk stays in L2) and stores its total in block_sums[b];
+// an L2 hit and HBM still moves 2 * n * sizeof(T) bytes.  Every warp owns a
+// contiguous part of its block's chunk:
+//   phase 1  each warp folds its part (loads marked evict_last, so the part
+//            stays in L2); the block's total goes to block_sums[b] and the
+//            warp totals stay in shared memory;
 //   barrier  every block arrives at a grid-wide counter (a bounded wait that
 //            records a timeout in the error word);
-//   phase 2  block b folds block_sums[0 .. b) in a fixed order (its offset),
-//            re-reads its chunk from L2 and scans it tile by tile, carrying
-//            the running prefix, with streaming stores.
-// There is no per-tile look-back chain, so a launch costs one barrier and
-// two streams over the data instead of a pipeline's fill and drain; the fp32
+//   phase 2  block b folds block_sums[0 .. b) in a fixed order (its offset);
+//            each warp adds the totals of the block's earlier warps, then
+//            re-reads its part from L2 segment by segment (the next segment
+//            loaded while this one is scanned) and scans it with a running
+//            carry and streaming stores.
+// There is no per-tile look-back chain and no block barrier between segments,
+// so a launch costs one grid barrier and two streams over the data; the fp32
 // result does not depend on timing.
 #include "core.cuh"
 #include "launch.h"
@@ -88,41 +92,48 @@ l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *_
 {
     using S = typename Op::S;
     constexpr int NWARPS = THREADS / 32;
-    constexpr int WARP_ITEMS = 32 * 4 * VECS;
-    constexpr int TILE = THREADS * 4 * VECS;
-    __shared__ S s_warp[2][NWARPS];
+    constexpr int SEG = 32 * 4 * VECS;   // elements a warp moves per step (the chunk is a multiple of NWARPS * SEG)
+    __shared__ S s_wtot[NWARPS];
     __shared__ S s_carry;
     const Op op;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned blocks = gridDim.x;
     const size_t begin = static_cast<size_t>(blockIdx.x) * chunk;
     const size_t end = begin + chunk < n ? begin + chunk : n;
+    const size_t wpart = chunk / NWARPS;
+    const size_t wb = begin + static_cast<size_t>(warp) * wpart;   // this warp's part: [wb, we)
+    const size_t we = wb + wpart < end ? wb + wpart : end;
 
-    // ---- phase 1: the chunk's total; its lines stay in L2
+    // ---- phase 1: the part's total; its lines stay in L2
     const uint64_t keep = policy_evict_last();
     S acc = Op::identity();
-    for (size_t t0 = begin; t0 < end; t0 += TILE) {
-        const size_t wb = t0 + static_cast<size_t>(warp) * WARP_ITEMS;
-        if (t0 + TILE <= end) {
+    size_t s = wb;
+    for (; s + 2 * SEG <= we; s += 2 * SEG) {
+        uint4 q[2 * VECS];
 #pragma unroll
-            for (int r = 0; r < VECS; ++r) {
-                const uint4 q = ld_keep(reinterpret_cast<const uint4 *>(in + wb) + r * 32 + lane, keep);
+        for (int r = 0; r < 2 * VECS; ++r) q[r] = ld_keep(reinterpret_cast<const uint4 *>(in + s) + r * 32 + lane, keep);
+#pragma unroll
+        for (int r = 0; r < 2 * VECS; ++r)
+            acc = op(acc, op(op(from_bits<S>(q[r].x), from_bits<S>(q[r].y)), op(from_bits<S>(q[r].z), from_bits<S>(q[r].w))));
+    }
+    for (; s < we; s += SEG) {
+        for (int r = 0; r < VECS; ++r) {
+            const size_t e = s + static_cast<size_t>(r * 32 + lane) * 4;
+            if (e + 4 <= we) {
+                const uint4 q = ld_keep(reinterpret_cast<const uint4 *>(in + e), keep);
                 acc = op(acc, op(op(from_bits<S>(q.x), from_bits<S>(q.y)), op(from_bits<S>(q.z), from_bits<S>(q.w))));
+            } else {
+                for (int k = 0; k < 4; ++k)
+                    if (e + k < we) acc = op(acc, in[e + k]);
             }
-        } else {
-            for (int r = 0; r < VECS; ++r)
-                for (int j = 0; j < 4; ++j) {
-                    const size_t e = wb + static_cast<size_t>((r * 32 + lane) * 4 + j);
-                    if (e < end) acc = op(acc, in[e]);
-                }
         }
     }
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) acc = op(acc, __shfl_xor_sync(kFullMask, acc, d));
-    if (lane == 0) s_warp[0][warp] = acc;
+    if (lane == 0) s_wtot[warp] = acc;
     __syncthreads();
     if (warp == 0) {
-        S v = lane < NWARPS ? s_warp[0][lane] : Op::identity();
+        S v = lane < NWARPS ? s_wtot[lane] : Op::identity();
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
         if (lane == 0) block_sums[blockIdx.x] = v;
@@ -130,7 +141,7 @@ l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *_
 
     const bool ok = grid_barrier(st, blocks, spin_limit);
 
-    // ---- phase 2: this block's offset, then its chunk scanned tile by tile
+    // ---- phase 2: the block's offset, the warp's offset, then the part scanned
     if (warp == 0) {
         S v = Op::identity();
         if (ok)
@@ -140,26 +151,30 @@ l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *_
         if (lane == 0) s_carry = v;
     }
     __syncthreads();
-    S carry = s_carry;
-    unsigned parity = 0;
-    for (size_t t0 = begin; t0 < end; t0 += TILE, parity ^= 1u) {
-        const size_t wb = t0 + static_cast<size_t>(warp) * WARP_ITEMS;
-        const bool full = t0 + TILE <= end;
+    S carry;
+    {
+        S v = lane < warp ? s_wtot[lane] : Op::identity();
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
+        carry = op(s_carry, v);
+    }
+    S xn[VECS][4];
+    if (wb < we) load_rows<S, VECS, true>(in, wb, we, lane, wb + SEG <= we, xn, Op::identity());
+    for (s = wb; s < we; s += SEG) {
         S x[VECS][4];
-        load_rows<S, VECS, true>(in, wb, end, lane, full, x, Op::identity());
+#pragma unroll
+        for (int r = 0; r < VECS; ++r)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[r][k] = xn[r][k];
+        if (s + SEG < we) load_rows<S, VECS, true>(in, s + SEG, we, lane, s + 2 * SEG <= we, xn, Op::identity());
         S tt[VECS];
 #pragma unroll
         for (int r = 0; r < VECS; ++r) tt[r] = op(op(x[r][0], x[r][1]), op(x[r][2], x[r][3]));
         S row_excl[VECS], warp_total;
         warp_scan_rows<Op, VECS>(op, tt, lane, row_excl, warp_total);
-        if (lane == 0) s_warp[parity][warp] = warp_total;
-        __syncthreads();   // two buffers: the next tile writes the other one
-        S warp_excl, tile_total;
-        block_scan_warps<Op, NWARPS>(op, s_warp[parity], warp, lane, warp_excl, tile_total);
-        const S pfx = op(carry, warp_excl);
 #pragma unroll
         for (int r = 0; r < VECS; ++r) {
-            S cur = op(pfx, row_excl[r]);
+            S cur = op(carry, row_excl[r]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const S v = x[r][k];
@@ -172,8 +187,8 @@ l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *_
                 }
             }
         }
-        store_rows<S, VECS, true>(out, wb, end, lane, full, x);
-        carry = op(carry, tile_total);
+        store_rows<S, VECS, true>(out, s, we, lane, s + SEG <= we, x);
+        carry = op(carry, warp_total);
     }
     grid_depart(st, blocks);
 }
@@ -184,10 +199,10 @@ cudaError_t launch_l2res(const void *in, void *out, size_t n, const Workspace &w
 {
     using S = typename Op::S;
     constexpr int THREADS = 1024;
-    constexpr size_t TILE = static_cast<size_t>(THREADS) * 4 * VECS;
-    const size_t tiles = (n + TILE - 1) / TILE;
-    size_t blocks = tiles < static_cast<size_t>(ws.num_sms) ? tiles : static_cast<size_t>(ws.num_sms);
-    const size_t chunk = ((tiles + blocks - 1) / blocks) * TILE;
+    constexpr size_t UNIT = static_cast<size_t>(THREADS) * 4 * VECS;   // one segment per warp
+    const size_t units = (n + UNIT - 1) / UNIT;
+    size_t blocks = units < static_cast<size_t>(ws.num_sms) ? units : static_cast<size_t>(ws.num_sms);
+    const size_t chunk = ((units + blocks - 1) / blocks) * UNIT;
     blocks = (n + chunk - 1) / chunk;   // no block without work
     const S *sin = static_cast<const S *>(in);
     S *sout = static_cast<S *>(out);
@@ -202,10 +217,10 @@ template <class Op>
 cudaError_t launch_l2res_dir(bool inclusive, const void *in, void *out, size_t n, const Workspace &ws,
                              unsigned spin_limit, cudaStream_t s)
 {
-    // small inputs take 4,096-element tiles so that more blocks share them
+    // small inputs take 4,096-element chunk units so that more blocks share them
     if (n >= (size_t(1) << 21))
-        return inclusive ? launch_l2res<Op, true, 4>(in, out, n, ws, spin_limit, s)
-                         : launch_l2res<Op, false, 4>(in, out, n, ws, spin_limit, s);
+        return inclusive ? launch_l2res<Op, true, 2>(in, out, n, ws, spin_limit, s)
+                         : launch_l2res<Op, false, 2>(in, out, n, ws, spin_limit, s);
     return inclusive ? launch_l2res<Op, true, 1>(in, out, n, ws, spin_limit, s)
                      : launch_l2res<Op, false, 1>(in, out, n, ws, spin_limit, s);
 }

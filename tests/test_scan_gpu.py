@@ -108,6 +108,16 @@ def test_carry_modes(ds, mode):
         ds.set_carry_mode("default")
 
 
+def test_default_size_boundaries(ds):
+    """Sizes around the default's switches between the one-tile kernel, the
+    L2-resident scan and the pipeline (2^17 and 2^24), ragged chunks included."""
+    from stream_compaction_device_gb300 import workloads as wl
+    for n in ((1 << 17) - 1, 1 << 17, (1 << 17) + 4097, 3 * (1 << 20) + 1, (1 << 24) - 3, 1 << 24, (1 << 24) + 1):
+        check(ds, wl.random_input(np.int32, n, n, "add"), "add", False)
+        check(ds, wl.random_input(np.float32, n, n + 1, "add"), "add", True)
+        check(ds, wl.random_input(np.uint32, n, n + 2, "max"), "max", False)
+
+
 @pytest.mark.parametrize("mode", ["default", "lookback", "l2"])
 def test_repeated_runs_identical(ds, mode):
     """Integer results do not depend on block timing: 50 launches, one answer."""
