@@ -73,6 +73,29 @@ def test_compact_sizes(ds, mode, pattern):
         check_compact(ds, v, f)
 
 
+@pytest.mark.parametrize("pattern", ["random2pct", "clustered", "mixed", "at_limit", "over_limit"])
+def test_compact_sparse_tiles(ds, mode, pattern):
+    """Tiles of 8,192 with few kept elements (256 or 257 each), tiles whose
+    kept elements crowd one 512-element part, and sparse tiles next to dense
+    ones."""
+    rng = np.random.default_rng(sum(map(ord, pattern)))
+    for n in (64 * 8192, 64 * 8192 + 4101, 1 << 21):
+        v = rng.integers(-2**31, 2**31, n, dtype=np.int32)
+        i = np.arange(n)
+        if pattern == "random2pct":
+            f = (rng.random(n) < 0.02).astype(np.uint8)
+        elif pattern == "clustered":          # 200 kept, all in the tile's first part
+            f = ((i % 8192) < 200).astype(np.uint8)
+        elif pattern == "mixed":              # even tiles 1% kept, odd tiles 60%
+            p = np.where((i // 8192) % 2 == 0, 0.01, 0.60)
+            f = (rng.random(n) < p).astype(np.uint8)
+        elif pattern == "at_limit":           # exactly 256 kept per tile
+            f = ((i % 32) == 5).astype(np.uint8) * 9
+        else:                                 # 257 kept per tile
+            f = (((i % 32) == 5) | ((i % 8192) == 6)).astype(np.uint8)
+        check_compact(ds, v, f)
+
+
 @pytest.mark.parametrize("voff,foff,ooff", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (2, 3, 3), (0, 4, 2)])
 def test_compact_unaligned(ds, mode, voff, foff, ooff):
     rng = np.random.default_rng(voff * 100 + foff * 10 + ooff)
