@@ -12,8 +12,9 @@
 //      every (digit, tile) run's first output position: all keys of smaller
 //      digits, plus the keys of digit d in earlier tiles;
 //   3. radix_scatter_kernel: every tile ranks its keys stably by digit -- rows
-//      of 32 consecutive keys in input order, eight ballots grouping the
-//      lanes with equal digits, one counter row per warp in shared memory --
+//      of 32 consecutive keys in input order, the lanes with equal digits
+//      grouped by eight ballots (three rows in four) or the hardware match
+//      (every fourth row), one counter row per warp in shared memory --
 //      stages the tile sorted by digit and writes each digit's keys as one
 //      contiguous run.
 // Traffic: 12 bytes per key per pass (count read, scatter read and write),
@@ -32,8 +33,11 @@ constexpr int kSortBuckets = 1 << kRadixDigitBits;     // 256
 __device__ __forceinline__ unsigned digit_of(uint32_t key, int shift) { return (key >> shift) & (kSortBuckets - 1); }
 
 // Lanes whose 8-bit digit equals this lane's, built from one ballot per digit
-// bit (the hardware match instruction measured far slower here); `valid`:
-// this row's lanes that hold a key.
+// bit; `valid`: this row's lanes that hold a key.  The ballots keep the
+// integer pipe busy and the hardware match instruction the shared-memory
+// pipe, so the scatter ranks one row in four with the match and the rest with
+// ballots (measured: all ballots 288 us, all matches 496 us, one in four
+// matches 252 us for a 2^26-key pass).
 __device__ __forceinline__ unsigned match_digit(unsigned d, unsigned valid)
 {
     unsigned eq = valid;
@@ -111,11 +115,17 @@ __device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *s_tmp, i
     return base + inc - v;
 }
 
+// Rows ranked with the hardware match instead of ballots: every fourth.
+constexpr unsigned kMatchRows = 0x1111u;
+
 // keys_in -> keys_out by the digit at `shift`; run_start[d * tiles + tile]:
-// the first output position of the tile's keys of digit d.
+// the first output position of the tile's keys of digit d.  Block b sorts
+// tile tile0 + b; FULL: every tile of the launch holds kSortTile keys (the
+// ragged last tile gets a launch of its own), which drops the bounds checks.
+template <bool FULL>
 __global__ void __launch_bounds__(kSortThreads, 2)
 radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict__ keys_out, size_t n, int shift,
-                     unsigned tiles, const uint32_t *__restrict__ run_start)
+                     unsigned tiles, unsigned tile0, const uint32_t *__restrict__ run_start)
 {
     // per-warp digit counters; then each (warp, digit)'s first staged position
     __shared__ uint32_t s_wcount[kSortWarps][kSortBuckets];   // 16 KB
@@ -123,20 +133,20 @@ radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict_
     __shared__ uint32_t s_delta[kSortBuckets];                 // output position - staged position, per digit
     __shared__ uint32_t s_tmp[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned tile = blockIdx.x;
+    const unsigned tile = tile0 + blockIdx.x;
     const size_t base = static_cast<size_t>(tile) * kSortTile;
     const size_t wbase = base + static_cast<size_t>(warp) * (kSortRows * 32);
-    const unsigned len = (n - base < static_cast<size_t>(kSortTile)) ? static_cast<unsigned>(n - base) : kSortTile;
+    const unsigned len = FULL ? kSortTile : static_cast<unsigned>(n - base < kSortTile ? n - base : kSortTile);
 
     for (int i = tid; i < kSortWarps * kSortBuckets; i += kSortThreads) (&s_wcount[0][0])[i] = 0;
     if (tid < kSortBuckets) s_delta[tid] = run_start[static_cast<size_t>(tid) * tiles + tile];   // the run's start
     // keys of this warp's 512 that exist (the last tile is ragged)
-    const unsigned wlen = n > wbase ? static_cast<unsigned>(n - wbase < 512 ? n - wbase : 512) : 0u;
+    const unsigned wlen = FULL ? 512u : (n > wbase ? static_cast<unsigned>(n - wbase < 512 ? n - wbase : 512) : 0u);
     uint32_t key[kSortRows];
 #pragma unroll
     for (int r = 0; r < kSortRows; ++r) {
         const unsigned i = static_cast<unsigned>(r * 32 + lane);
-        key[r] = (i < wlen) ? __ldcs(keys_in + wbase + i) : 0u;
+        key[r] = (FULL || i < wlen) ? __ldcs(keys_in + wbase + i) : 0u;
     }
     __syncthreads();
 
@@ -148,9 +158,10 @@ radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict_
     const unsigned lt = lanemask_lt();
 #pragma unroll
     for (int r = 0; r < kSortRows; ++r) {
-        const bool has = static_cast<unsigned>(r * 32 + lane) < wlen;
+        const bool has = FULL || static_cast<unsigned>(r * 32 + lane) < wlen;
+        const unsigned valid = FULL ? kFullMask : __ballot_sync(kFullMask, has);
         const unsigned d = digit_of(key[r], shift);
-        const unsigned same = match_digit(d, __ballot_sync(kFullMask, has));
+        const unsigned same = ((kMatchRows >> r) & 1u) ? (__match_any_sync(kFullMask, d) & valid) : match_digit(d, valid);
         const int leader = has ? __ffs(same) - 1 : lane;
         uint32_t before = 0;
         if (has && lane == leader) {
@@ -186,7 +197,7 @@ radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict_
     // stage sorted by digit (stable: warp order, then row order, then lane)
 #pragma unroll
     for (int r = 0; r < kSortRows; ++r) {
-        if (static_cast<unsigned>(r * 32 + lane) < wlen) {
+        if (FULL || static_cast<unsigned>(r * 32 + lane) < wlen) {
             const unsigned d = digit_of(key[r], shift);
             s_keys[s_wcount[warp][d] + ((rank2[r / 2] >> (16 * (r & 1))) & 0xffffu)] = key[r];
         }
@@ -195,6 +206,7 @@ radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict_
 
     // each digit's keys as one run: staged key i of digit d goes to
     // i + (first output position - first staged position of d)
+#pragma unroll 4
     for (unsigned i = tid; i < len; i += kSortThreads) {
         const uint32_t k = s_keys[i];
         const size_t dst = static_cast<uint32_t>(i + s_delta[digit_of(k, shift)]);
@@ -214,7 +226,9 @@ cudaError_t launch_radix_pass(const uint32_t *src, uint32_t *dst, size_t n, int 
     e = launch_scan(ElemType::U32, kOpAdd, false, hist, hist, static_cast<size_t>(tiles) * kSortBuckets,
                     reinterpret_cast<uintptr_t>(hist) % 16 == 0, kCarryDefault, ws, spin_limit, s);
     if (e != cudaSuccess) return e;
-    radix_scatter_kernel<<<tiles, kSortThreads, 0, s>>>(src, dst, n, shift, tiles, hist);
+    const unsigned full = static_cast<unsigned>(n / kSortTile);
+    if (full > 0) radix_scatter_kernel<true><<<full, kSortThreads, 0, s>>>(src, dst, n, shift, tiles, 0u, hist);
+    if (full < tiles) radix_scatter_kernel<false><<<1, kSortThreads, 0, s>>>(src, dst, n, shift, tiles, full, hist);
     return cudaGetLastError();
 }
 
