@@ -123,7 +123,10 @@ struct IsSegmented<P, decltype(void(P::kSegmented))> {
 //                 parts of the tile (P::reduce_parts instead of P::reduce);
 //                 the consume step gets their exclusive prefixes, so each
 //                 consume warp knows its offset inside the tile without a
-//                 group-wide scan;
+//                 group-wide scan.  Segmented policies report each part's
+//                 value in part[q] and its head flag in part[kParts + q]; the
+//                 tile's pair is their in-order fold, and the consume step
+//                 gets the parts' own values with the head mask after them;
 //   kScratchBytes shared memory for the consume group beyond the B buffers.
 template <class P, class = void>
 struct PolicyParts {
@@ -216,7 +219,8 @@ struct ConsumeTile {
     unsigned char *buf; // the B buffer (P::kBBytes bytes)
     unsigned round;     // alternates the warp-totals buffers
     unsigned *warp_state;   // per-warp word kept across the block's tiles (0 at start)
-    const uint32_t *part_excl;   // exclusive prefixes of the parts' aggregates (P::kParts > 0; until release)
+    const uint32_t *part_excl;   // exclusive prefixes of the parts' aggregates (P::kParts > 0; until release;
+                                 // segmented: the parts' values, then their head mask)
     unsigned char *scratch;      // P::kScratchBytes of shared memory for the consume group
 };
 
@@ -231,7 +235,9 @@ struct PipeShape {
     static constexpr int kThreads = (NS + NR + R + 2) * 32;
     static constexpr unsigned kNoCopy = 0xffffffffu;
     static constexpr int kParts = PolicyParts<P>::value;
-    static constexpr int kPartSlots = kParts > 0 ? kParts : 1;
+    // segmented parts: the values, then one head flag per part (red_part) or
+    // a mask of them (rec_part)
+    static constexpr int kPartSlots = kParts > 0 ? (IsSegmented<P>::value ? 2 * kParts : kParts) : 1;
     struct Ctrl {
         uint64_t a_full[SA], a_empty[SA];
         uint64_t b_full[SB], b_empty[SB];
@@ -514,7 +520,22 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 S agg = from_bits<S>(ctrl->red[0]);
                 unsigned ex = ctrl->red_extra[0];
                 unsigned head = 0;
-                if (SEG) {
+                // segmented parts: their values and head mask, read once
+                uint32_t pval[SEG && G::kParts > 0 ? G::kParts : 1];
+                unsigned pmask = 0;
+                if constexpr (SEG && G::kParts > 0) {
+#pragma unroll
+                    for (int q = 0; q < G::kParts; ++q) {
+                        pval[q] = ctrl->red_part[q];
+                        if (ctrl->red_part[G::kParts + q] != 0) pmask |= 1u << q;
+                    }
+                    // in order: a part that holds a head restarts the fold
+                    agg = Op::identity();
+#pragma unroll
+                    for (int q = 0; q < G::kParts; ++q)
+                        agg = ((pmask >> q) & 1u) ? from_bits<S>(pval[q]) : op(agg, from_bits<S>(pval[q]));
+                    head = pmask != 0 ? 1u : 0u;
+                } else if (SEG) {
                     // in order: a warp whose part holds a head restarts the fold
                     agg = Op::identity();
 #pragma unroll
@@ -545,7 +566,12 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 ctrl->rec_tile[r] = t;
                 ctrl->rec_agg[r] = to_bits(agg);
                 ctrl->rec_head[r] = head;
-                if constexpr (G::kParts > 0) {
+                if constexpr (SEG && G::kParts > 0) {
+                    // the parts' own pairs: each consume warp combines those before it
+#pragma unroll
+                    for (int q = 0; q < G::kParts; ++q) ctrl->rec_part[r][q] = pval[q];
+                    ctrl->rec_part[r][G::kParts] = pmask;
+                } else if constexpr (G::kParts > 0) {
                     S acc = Op::identity();
                     for (int q = 0; q < G::kParts; ++q) {
                         ctrl->rec_part[r][q] = to_bits(acc);

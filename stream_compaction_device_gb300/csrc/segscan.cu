@@ -255,16 +255,32 @@ segscan_tile_kernel(const typename Op::S *__restrict__ in, const uint8_t *__rest
     store_rows<S, VECS, ALIGNED>(out, warp_base, n, lane, full, x);
 }
 
+// Fold of v over the warp (the result in every lane): one redux instruction
+// for the integer operators, shuffles for fp32.
+__device__ __forceinline__ uint32_t warp_fold(const AddU32 &, uint32_t v) { return __reduce_add_sync(kFullMask, v); }
+__device__ __forceinline__ uint32_t warp_fold(const XorU32 &, uint32_t v) { return __reduce_xor_sync(kFullMask, v); }
+__device__ __forceinline__ uint32_t warp_fold(const MaxU32 &, uint32_t v) { return __reduce_max_sync(kFullMask, v); }
+__device__ __forceinline__ int32_t warp_fold(const MaxI32 &, int32_t v) { return __reduce_max_sync(kFullMask, v); }
+template <class Op>
+__device__ __forceinline__ typename Op::S warp_fold(const Op &op, typename Op::S v)
+{
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
+    return v;
+}
+
 // Index of the highest nonzero byte of a nonzero word.
 __device__ __forceinline__ int top_byte(uint32_t w) { return (31 - __clz(static_cast<int>(w))) >> 3; }
 
 // ---------------------------------------------------------------------------
 // Pipelined policy (see pipeline_l2.cuh).  Both passes copy the tile's values
-// (kTile * 4 bytes) followed by its heads (kTile bytes).  Reduce warp w folds
-// the contiguous part [w * kPart, (w + 1) * kPart) of the tile: it finds the
-// last head there (a warp max) and folds the values from it on, so the
-// kernel's per-warp fold needs no order; the kernel then combines the warps
-// in order.
+// (kTile * 4 bytes) followed by its heads (kTile bytes).  The tile splits into
+// one part per consume warp; a reduce warp takes whole parts: it finds a
+// part's last head (a warp max) and folds the values from it on, so that fold
+// needs no order, and reports the part's (head, value) pair.  The kernel folds
+// the pairs in order into the tile's pair, and every consume warp combines the
+// pairs of the parts before its own with the tile's prefix -- no barrier
+// among the consume warps.
 // ---------------------------------------------------------------------------
 template <class OpT, bool INCLUSIVE, int NS_, int NR_, int VECS_, int SA_, int SB_, int R_, int PREFETCH = 0>
 struct SegScanPolicy {
@@ -276,11 +292,11 @@ struct SegScanPolicy {
     static constexpr int VECS = VECS_;
     static constexpr int kWarpItems = 32 * 4 * VECS;
     static constexpr int kTile = NS_ * 32 * 4 * VECS;
-    static constexpr int kPart = kTile / NR_;
-    static_assert(kPart % 16 == 0, "reduce parts of whole 16-head chunks");
     static constexpr size_t kValueBytes = static_cast<size_t>(kTile) * 4;
     static constexpr size_t kABytes = kValueBytes + static_cast<size_t>(kTile);
     static constexpr size_t kBBytes = kABytes;
+    static constexpr int kParts = NS_;                   // one part per consume warp
+    static constexpr bool kWarpIndependent = true;       // no barrier in consume()
     static constexpr bool kHasExtra = false;
     struct Args {
         const S *in;
@@ -317,12 +333,14 @@ struct SegScanPolicy {
     {
         a_copies(a, t, src, bytes, off);
     }
-    __device__ static void reduce(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int, S &v,
-                                  unsigned &extra)
+    // pass A: each part's pair -- value in part[q], head flag in
+    // part[kParts + q]; reduce warp rw takes parts rw, rw + NR, ...
+    __device__ static void reduce_parts(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int, S &v,
+                                        unsigned &extra, uint32_t *part)
     {
+        static_assert(NS_ % NR_ == 0 && kWarpItems == 512, "whole parts of 16 heads per lane");
         const Op op;
-        const int lane = rtid & 31;
-        const unsigned p0 = static_cast<unsigned>(rtid >> 5) * kPart;
+        const int lane = rtid & 31, rw = rtid >> 5;
         const unsigned len = tile_len(a, t);
         const unsigned vcp = values_copied(a, t), hcp = heads_copied(a, t);
         const size_t base = static_cast<size_t>(t) * kTile;
@@ -330,47 +348,53 @@ struct SegScanPolicy {
         const uint8_t *hd = abuf + kValueBytes;
         v = Op::identity();
         extra = 0;
-        if (p0 >= len) return;
-        const unsigned p1 = (p0 + kPart < len) ? p0 + kPart : len;
-        // last head of the part (-1: none)
-        int last = -1;
-        if (p1 == p0 + kPart && p1 <= hcp) {
-            const uint4 *h4 = reinterpret_cast<const uint4 *>(hd + p0);
-            for (int c = lane; c < kPart / 16; c += 32) {
-                const uint4 q = h4[c];
-                const int at = static_cast<int>(p0) + c * 16;
-                if (q.w) last = max(last, at + 12 + top_byte(q.w));
-                else if (q.z) last = max(last, at + 8 + top_byte(q.z));
-                else if (q.y) last = max(last, at + 4 + top_byte(q.y));
-                else if (q.x) last = max(last, at + top_byte(q.x));
+#pragma unroll
+        for (int i = 0; i < NS_ / NR_; ++i) {
+            const int q = rw + i * NR_;
+            const unsigned p0 = static_cast<unsigned>(q) * kWarpItems;
+            const unsigned p1 = (p0 + kWarpItems < len) ? p0 + kWarpItems : (p0 < len ? len : p0);
+            // last head of the part (-1: none); lane L looks at heads 16L .. 16L + 15
+            int last = -1;
+            if (p1 == p0 + kWarpItems && p1 <= hcp) {
+                const uint4 h = reinterpret_cast<const uint4 *>(hd + p0)[lane];
+                const int at = static_cast<int>(p0) + lane * 16;
+                if (h.w) last = at + 12 + top_byte(h.w);
+                else if (h.z) last = at + 8 + top_byte(h.z);
+                else if (h.y) last = at + 4 + top_byte(h.y);
+                else if (h.x) last = at + top_byte(h.x);
+            } else {
+                for (unsigned e = p0 + 16u * lane; e < p0 + 16u * lane + 16u && e < p1; ++e) {
+                    const uint8_t h = (e < hcp) ? hd[e] : a.heads[base + e];
+                    if (h != 0) last = static_cast<int>(e);
+                }
             }
-        } else {
-            for (unsigned e = p0 + lane; e < p1; e += 32) {
-                const uint8_t h = (e < hcp) ? hd[e] : a.heads[base + e];
-                if (h != 0) last = max(last, static_cast<int>(e));
+            last = __reduce_max_sync(kFullMask, last);
+            const unsigned from = last >= 0 ? static_cast<unsigned>(last) : p0;
+            S pv = Op::identity();
+            if (p1 == p0 + kWarpItems && p1 <= vcp) {
+                // lane L takes the 16-byte groups L, L + 32, L + 64, L + 96
+                const uint4 *v4 = reinterpret_cast<const uint4 *>(vals + p0);
+                const S id = Op::identity();
+#pragma unroll
+                for (int g = 0; g < kWarpItems / 128; ++g) {
+                    const unsigned e = p0 + 4u * static_cast<unsigned>(g * 32 + lane);
+                    const uint4 u = v4[g * 32 + lane];
+                    pv = op(pv, op(op(e >= from ? from_bits<S>(u.x) : id, e + 1 >= from ? from_bits<S>(u.y) : id),
+                                   op(e + 2 >= from ? from_bits<S>(u.z) : id, e + 3 >= from ? from_bits<S>(u.w) : id)));
+                }
+            } else {
+                for (unsigned e = from + lane; e < p1; e += 32) pv = op(pv, (e < vcp) ? vals[e] : a.in[base + e]);
+            }
+            pv = warp_fold(op, pv);
+            if (lane == 0) {
+                part[q] = to_bits(pv);
+                part[kParts + q] = last >= 0 ? 1u : 0u;
             }
         }
-        last = __reduce_max_sync(kFullMask, last);
-        const unsigned from = last >= 0 ? static_cast<unsigned>(last) : p0;
-        if (p1 == p0 + kPart && p1 <= vcp) {
-            const uint4 *v4 = reinterpret_cast<const uint4 *>(vals + p0);
-            for (int k = lane; k < kPart / 4; k += 32) {
-                const unsigned e = p0 + 4u * k;
-                if (e + 3 < from) continue;
-                const uint4 q = v4[k];
-                if (e >= from) v = op(v, from_bits<S>(q.x));
-                if (e + 1 >= from) v = op(v, from_bits<S>(q.y));
-                if (e + 2 >= from) v = op(v, from_bits<S>(q.z));
-                v = op(v, from_bits<S>(q.w));
-            }
-        } else {
-            for (unsigned e = from + lane; e < p1; e += 32) v = op(v, (e < vcp) ? vals[e] : a.in[base + e]);
-        }
-        extra = last >= 0 ? 1u : 0u;
     }
     __device__ static void after_reduce(const Args &, unsigned, unsigned) {}
     template <class Release>
-    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
+    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *, uint32_t *,
                                        int warp, int lane, Release &release)
     {
         const Op op;
@@ -409,22 +433,28 @@ struct SegScanPolicy {
                 hb[q] = m;
             }
         }
-        release();   // the tile is in registers now
+        // this warp's exclusive pair within the tile: lane q < kParts holds
+        // part q's pair; an in-order pair scan, then lane warp - 1's result
+        S pv = lane < kParts ? from_bits<S>(ct.part_excl[lane]) : Op::identity();
+        unsigned ph = lane < kParts ? (ct.part_excl[kParts] >> lane) & 1u : 0u;
+        release();   // the tile and the part pairs are in registers now
+#pragma unroll
+        for (int d = 1; d < kParts; d <<= 1) {
+            const S uv = __shfl_up_sync(kFullMask, pv, d);
+            const unsigned uh = __shfl_up_sync(kFullMask, ph, d);
+            if (lane >= d) seg_combine(op, uv, uh, pv, ph);
+        }
+        S xv = __shfl_sync(kFullMask, pv, warp > 0 ? warp - 1 : 0);
+        unsigned xh = __shfl_sync(kFullMask, ph, warp > 0 ? warp - 1 : 0);
+        if (warp == 0) {
+            xv = Op::identity();
+            xh = 0;
+        }
         S tv[VECS], ev[VECS], wv;
         unsigned th[VECS], eh[VECS], wh;
 #pragma unroll
         for (int q = 0; q < VECS; ++q) seg_fold4<Op>(op, x[q], hb[q], tv[q], th[q]);
         seg_warp_scan_rows<Op, VECS>(op, tv, th, lane, ev, eh, wv, wh);
-        // the warp pairs: values in wbuf0, heads in wbuf1 (the consume group
-        // meets at its decide barrier before every tile, so both are free)
-        if (lane == 0) {
-            wbuf0[warp] = to_bits(wv);
-            wbuf1[warp] = wh;
-        }
-        named_sync(kBarConsumeTotals, NS_ * 32);
-        S xv, totv;
-        unsigned xh, toth;
-        seg_scan_warp_pairs<Op, NS_>(op, wbuf0, wbuf1, warp, lane, xv, xh, totv, toth);
         seg_finish_rows<Op, INCLUSIVE, VECS>(op, ct.prefix, xv, xh, ev, eh, hb, x);
         if (base + kTile <= a.n) {
             uint4 *o4 = reinterpret_cast<uint4 *>(a.out + base + wbase);
@@ -441,7 +471,7 @@ struct SegScanPolicy {
                     if (e < a.n) a.out[e] = x[q][j];
                 }
         }
-        return 1;
+        return 0;   // no warp-totals buffer used
     }
 };
 
@@ -453,7 +483,10 @@ cudaError_t launch_seg_pipelined(const void *in, const uint8_t *heads, void *out
                                  unsigned spin_limit, cudaStream_t s)
 {
     using S = typename Op::S;
-    using P = SegScanPolicy<Op, INCLUSIVE, 16, 4, 4, 3, 2, 10, 1>;
+    // eight reduce warps (two parts each) and six records: measured at 2^28,
+    // 424 us against 532 us with four reduce warps and ten records -- the
+    // reduce step, not the records, bounds the tile rate
+    using P = SegScanPolicy<Op, INCLUSIVE, 16, 8, 4, 3, 2, 6, 1>;
     using G = PipeShape<P>;
     auto kernel = pipeline_l2_kernel<P>;
     static std::atomic<unsigned long long> attribute_set{0};   // one bit per device
