@@ -178,6 +178,40 @@ def test_bracket_unaligned(ds, mode, xoff, ooff):
         check_bracket(ds, x, store=False, xoff=xoff)
 
 
+@pytest.mark.parametrize("carry", ["default", "l2"])
+def test_bracket_check_only(ds, carry):
+    """The check without the scanned array: in the default mode from 2^17
+    elements (and in mode "l2" at every size) one cooperative launch folds
+    (sum, lowest prefix, highest prefix) runs; chunks whose prefixes cross a
+    wrap of int32 are checked again element by element."""
+    ds.set_carry_mode(carry)
+    try:
+        rng = np.random.default_rng(46)
+        sizes = [(1 << 17) - 1, 1 << 17, (1 << 17) + 3, 300_007, 16_384 * 152 + 5, 1_000_003, (1 << 22) + 1]
+        if carry == "l2":
+            sizes = [1, 5, 513, 4097, 16_385] + sizes[:3]
+        for n in sizes:
+            x = (2 * rng.integers(0, 2, n) - 1).astype(np.int32)
+            check_bracket(ds, x, store=False)                      # random walk: dips below zero
+            m = n // 2
+            d = dyck(m, rng)
+            if n % 2:
+                d = np.concatenate([d, np.array([1], np.int32)])
+            check_bracket(ds, d, store=False)                      # never negative
+            z = np.concatenate([d[1:], d[:1]])
+            check_bracket(ds, z, store=False)
+            big = rng.integers(I32_MIN, I32_MAX + 1, n, dtype=np.int32)
+            check_bracket(ds, big, store=False)                    # prefixes wrap many times
+            up = np.full(n, 1 << 20, dtype=np.int32)
+            check_bracket(ds, up, store=False)                     # exact prefix passes 2^31: wraps negative
+            down = np.full(n, -(1 << 20), dtype=np.int32)
+            down[0] = 5
+            check_bracket(ds, down, store=False)
+        assert ds.device_status() == 0
+    finally:
+        ds.set_carry_mode("default")
+
+
 def test_bracket_in_place(ds, mode):
     rng = np.random.default_rng(44)
     for n in (5, 8193, 600_001):
