@@ -51,6 +51,10 @@ __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], c
     const unsigned z_phase = out_aligned ? static_cast<unsigned>(zeros_at & 3) : 0u;
     const unsigned o_phase = out_aligned ? static_cast<unsigned>(ones_at & 3) : 0u;
     const unsigned o_base = out_aligned ? ((z_phase + zeros + 3u) & ~3u) : zeros;
+    // one store per key, its slot chosen by a select (a branch per key
+    // diverges on random bits); a whole part needs no bounds test
+    const bool whole = part_len == static_cast<unsigned>(32 * 4 * VECS);
+    const uint32_t o0 = o_base + o_phase;
     uint32_t row_base = 0;
 #pragma unroll
     for (int q = 0; q < VECS; ++q) {
@@ -59,12 +63,10 @@ __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], c
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t li = li0 + j;
-            if (li < part_len) {
-                if ((zmask[q] >> j) & 1u)
-                    stage[z_phase + zr++] = x[q][j];
-                else
-                    stage[o_base + o_phase + (li - zr)] = x[q][j];
-            }
+            const uint32_t z = (zmask[q] >> j) & 1u;
+            const uint32_t pos = z ? z_phase + zr : o0 + (li - zr);
+            if (whole || li < part_len) stage[pos] = x[q][j];
+            zr += z;
         }
         row_base += (tot >> (8 * q)) & 0xffu;
     }
@@ -137,6 +139,7 @@ struct SplitPolicy {
         const uint32_t *k1 = reinterpret_cast<const uint32_t *>(abuf);
         unsigned c[PPW], nz = 0;
         if (len == static_cast<unsigned>(kTile)) {
+            const bool next = a.next_zeros != nullptr;   // the next bit's zeros are wanted (inside a sort)
 #pragma unroll
             for (int i = 0; i < PPW; ++i) {
                 c[i] = 0;
@@ -144,7 +147,7 @@ struct SplitPolicy {
                 for (int k = 0; k < CH; ++k) {
                     const uint4 q = k4[(rw + i * NR_) * (kWarpItems / 4) + k * 32 + lane];
                     c[i] += zeros_of(q, a.bit);
-                    nz += zeros_of(q, a.next_bit);
+                    if (next) nz += zeros_of(q, a.next_bit);
                 }
             }
         } else {
@@ -203,8 +206,11 @@ struct SplitPolicy {
             }
             zmask[q] = m;
         }
+        // the zero total is fixed for the launch: one global read per warp,
+        // kept (plus one, so that 0 means "not read yet") in the warp's word
+        if (*ct.warp_state == 0) *ct.warp_state = *a.zeros_total + 1u;
         const size_t zeros_at = static_cast<size_t>(ct.prefix) + ct.part_excl[warp];
-        const size_t ones_at = static_cast<size_t>(*a.zeros_total) + (base + wbase - zeros_at);
+        const size_t ones_at = static_cast<size_t>(*ct.warp_state - 1u) + (base + wbase - zeros_at);
         const unsigned part_len = len > static_cast<unsigned>(wbase)
                                       ? (len - wbase < static_cast<unsigned>(kWarpItems) ? len - wbase
                                                                                           : static_cast<unsigned>(kWarpItems))
