@@ -494,6 +494,53 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_op(args):
+    """One library call at ``--n`` elements, ``--warmup`` + ``--steps`` times
+    back to back, for profiling a single kernel (``ncu -k ... -s W -c 1``):
+    prints the per-call time, which is not a bench line."""
+    import torch
+    import stream_compaction_device_gb300 as ds
+    from stream_compaction_device_gb300 import workloads as wl
+    ds.load()
+    n = args.n
+    if args.op == "compact50":
+        v = wl.compaction_values(n)
+        dv = torch.from_numpy(v).cuda()
+        f = torch.from_numpy(wl.predicate_flags(v, wl.threshold_for(0.5))).cuda()
+        out, cnt = torch.empty_like(dv), torch.empty(1, dtype=torch.int32, device="cuda")
+        fn = lambda: ds.compact(dv, f, out, cnt)
+    elif args.op == "segscan":
+        sv, sh = wl.segmented(n)
+        dv, dh = torch.from_numpy(sv).cuda(), torch.from_numpy(sh).cuda()
+        out = torch.empty_like(dv)
+        fn = lambda: ds.segmented_scan_inclusive(dv, dh, out)
+    elif args.op == "bracket_check":
+        x = torch.from_numpy(wl.brackets(n)).cuda()
+        res = torch.empty(2, dtype=torch.int32, device="cuda")
+        fn = lambda: ds.bracket_scan(x, result=res, store=False)
+    elif args.op == "split":
+        keys = torch.from_numpy(wl.radix_keys(n).view(np.int32)).cuda()
+        out = torch.empty_like(keys)
+        fn = lambda: ds.split_bit(keys, 17, out)
+    else:   # digit_sort
+        keys = torch.from_numpy(wl.radix_keys(n).view(np.int32)).cuda()
+        work, tmp = torch.empty_like(keys), torch.empty_like(keys)
+        def fn():
+            work.copy_(keys)
+            ds.radix_sort_digits(work, tmp)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    b.synchronize()
+    print(json.dumps({"op": args.op, "n": n, "ms_per_call": round(a.elapsed_time(b) / max(args.steps, 1), 5),
+                      "status": ds.device_status(), "note": "single-op run for profiling; not a bench line"}))
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
@@ -508,11 +555,15 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--op", choices=["scan", "compact50", "segscan", "bracket_check", "split", "digit_sort"],
+                   default="scan", help="scan: the benchmark; the others run one call repeatedly for profiling")
     args = p.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op != "scan":
+        run_op(args)
     else:
         run_ours(args)
 

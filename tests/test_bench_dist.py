@@ -53,3 +53,14 @@ def test_reference_arm_line(capsys):
     assert line["impl"] == "reference" and line["unit"] == "Gelem/s"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("op", ["compact50", "segscan", "bracket_check", "split", "digit_sort"])
+def test_single_op_mode(capsys, op):
+    """``bench.py --op``: one library call repeated for a profiler, its own line."""
+    import json
+    import bench
+    bench.main(["--op", op, "--n", "300007", "--steps", "2", "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["op"] == op and line["n"] == 300007 and line["status"] == 0 and line["ms_per_call"] > 0
