@@ -347,8 +347,6 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
             if (D > 0) {
                 t = __shfl_sync(kFullMask, queued, 0);
                 queued = __shfl_down_sync(kFullMask, queued, 1);
-                const unsigned nt = take();
-                if (lane == D - 1) queued = nt;
             } else {
                 t = take();
             }
@@ -359,9 +357,7 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                     mbar_arrive(&ctrl->a_full[a]);
                 }
                 ++ends;
-                continue;
-            }
-            if (lane == 0) {
+            } else if (lane == 0) {
                 const void *src[2] = {nullptr, nullptr};
                 unsigned bytes[2] = {0, 0}, off[2] = {0, 0};
                 PassACopies<P>::get(args, t, src, bytes, off);
@@ -382,6 +378,12 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                     ctrl->a_last[a] = G::kNoCopy;
                     mbar_arrive(&ctrl->a_full[a]);
                 }
+            }
+            // the next ticket only now: its atomic's round trip overlaps the
+            // copy just issued instead of delaying it
+            if (D > 0) {
+                const unsigned nt = take();
+                if (lane == D - 1) queued = nt;
             }
         }
         if (lane == 0)
