@@ -110,6 +110,24 @@ def test_segscan_head_patterns(ds, mode, inclusive):
     closing[31 * PIPE_TILE + 4000] = 1   # only inside the first group's closing tile
     closing[2 * GROUP + 31 * PIPE_TILE + 8000] = 1
     patterns["group-closing tiles only"] = closing
+    # the pipelined policy splits a tile into 512-element parts: heads at a
+    # part's first and last element, in alternate parts only, and in the
+    # tile's last part only
+    parts = np.zeros(n, np.uint8)
+    for t in (0, 2, 7, 40):
+        for q in (0, 1, 7, 15):
+            for off in (0, 511):
+                e = t * PIPE_TILE + q * 512 + off
+                if e < n:
+                    parts[e] = 1
+    patterns["part edges"] = parts
+    alt = np.zeros(n, np.uint8)
+    alt[(np.arange(n) // 512) % 2 == 1] = (rng.random(n) < 0.01)[(np.arange(n) // 512) % 2 == 1]
+    patterns["alternate parts"] = alt
+    last_part = np.zeros(n, np.uint8)
+    for t in range(0, n // PIPE_TILE, 3):
+        last_part[t * PIPE_TILE + 15 * 512 + 100] = 1
+    patterns["last part of every third tile"] = last_part
     for name, h in patterns.items():
         got = gpu_segscan(ds, x, h, "add", inclusive)
         ref = oracle.segscan(x, h, "add", inclusive)
