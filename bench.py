@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the pipelined
 # scan kernel at N = 2^28 (one-pass ncu capture of this benchmark's own
 # command); set to None whenever the kernel changes until it is re-captured.
-SCAN_TRAFFIC_BYTES = 2.115e9
+SCAN_TRAFFIC_BYTES = None
 
 
 def peak_hbm():
@@ -321,7 +321,7 @@ def run_ours(args):
             "hbm_gbs": round(achieved, 1), "pct_peak": round(100 * achieved / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": SCAN_TRAFFIC_BYTES,
-                         "kernel": "pipeline_l2_kernel<ScanPolicy<AddU32,exclusive,16,4,4,2,4,10,prefetch 1>>",
+                         "kernel": "pipeline_l2_kernel<ScanPolicy<AddU32,exclusive,16,4,4,2,4,10,prefetch 1,parts,2 tiles per ticket>>",
                          "algorithmic_bytes_per_launch": alg_bytes, "peak_kind": peak_kind},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
             "clocks": clock_info, "parity_sampled": parity_ok, "extra": extra,

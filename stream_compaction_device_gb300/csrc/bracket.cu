@@ -68,8 +68,10 @@ struct BracketEpilogue {
     }
 };
 
-// Pipelined scan policy with the same epilogue (geometry of the int32 scan).
-using BracketBase = ScanPolicy<AddU32, true, 16, 4, 4, 2, 4, 10, kL2EvictLast, kL2EvictFirst, true, 1>;
+// Pipelined scan policy with the same epilogue (geometry of the int32 scan:
+// parts folded in pass A, no barrier among the consume warps, two tiles per
+// ticket).
+using BracketBase = ScanPolicy<AddU32, true, 16, 4, 4, 2, 4, 10, kL2EvictLast, kL2EvictFirst, true, 1, true, 2>;
 
 struct BracketPolicy : BracketBase {
     struct Args : BracketBase::Args {
@@ -77,17 +79,18 @@ struct BracketPolicy : BracketBase {
         unsigned num_tiles;
     };
     template <class Release>
-    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
-                                       int warp, int lane, Release &release)
+    __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *, uint32_t *, int warp,
+                                       int lane, Release &release)
     {
         uint32_t x[VECS][4];
         load_x(a, ct, warp, lane, x);
-        release();   // the tile is in registers now
-        const uint32_t total = scan_x(ct, wbuf0, wbuf1, warp, lane, x);
-        bracket_mark<VECS>(a.result, x, ct.tile == a.num_tiles - 1, ct.prefix + total, warp * 32 + lane, lane,
+        const uint32_t pfx = ct.prefix + ct.part_excl[warp];
+        release();   // the tile and the part's prefix are in registers now
+        scan_x_from(pfx, lane, x);
+        bracket_mark<VECS>(a.result, x, ct.tile == a.num_tiles - 1, ct.prefix + ct.aggregate, warp * 32 + lane, lane,
                            *ct.warp_state);
         if (a.out != nullptr) store_x(a.out, a.n, ct.tile, warp, lane, x);
-        return 1;
+        return 0;
     }
 };
 

@@ -62,6 +62,20 @@ struct MaxF32 {
     __device__ __forceinline__ S operator()(S a, S b) const { return fmaxf(a, b); }
 };
 
+// Fold of v over the warp (the result in every lane): one redux instruction
+// for the integer operators, shuffles for fp32.
+__device__ __forceinline__ uint32_t warp_fold(const AddU32 &, uint32_t v) { return __reduce_add_sync(kFullMask, v); }
+__device__ __forceinline__ uint32_t warp_fold(const XorU32 &, uint32_t v) { return __reduce_xor_sync(kFullMask, v); }
+__device__ __forceinline__ uint32_t warp_fold(const MaxU32 &, uint32_t v) { return __reduce_max_sync(kFullMask, v); }
+__device__ __forceinline__ int32_t warp_fold(const MaxI32 &, int32_t v) { return __reduce_max_sync(kFullMask, v); }
+template <class Op>
+__device__ __forceinline__ typename Op::S warp_fold(const Op &op, typename Op::S v)
+{
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t to_bits(uint32_t v) { return v; }
 __device__ __forceinline__ uint32_t to_bits(int32_t v) { return static_cast<uint32_t>(v); }
 __device__ __forceinline__ uint32_t to_bits(float v) { return __float_as_uint(v); }

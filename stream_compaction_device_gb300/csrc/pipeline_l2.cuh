@@ -159,6 +159,17 @@ template <class P>
 struct PolicyAggregateAware<P, decltype(void(P::kAggregateAware))> {
     static constexpr bool value = P::kAggregateAware;
 };
+//   kTicketBatch  tiles per ticket of the A producer (default 1): a ticket
+//                 is one atomic on the stream's ticket counter, and the
+//                 tiles of a ticket are consecutive and go to one block.
+template <class P, class = void>
+struct PolicyTicketBatch {
+    static constexpr unsigned value = 1;
+};
+template <class P>
+struct PolicyTicketBatch<P, decltype(void(P::kTicketBatch))> {
+    static constexpr unsigned value = P::kTicketBatch;
+};
 template <class P, class = void>
 struct PolicyScratch {
     static constexpr size_t value = 0;
@@ -314,19 +325,30 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
         const uint64_t pol = l2_policy(P::kAHint);
         const uint64_t pre_pol = l2_policy_evict_last();
         bool tickets_done = false;
-        // takes the next ticket (num_tiles once they are done) and, for a real
+        // a ticket is a batch of K consecutive tiles (fewer atomic round
+        // trips); a block still takes its tiles in order
+        constexpr unsigned K = PolicyTicketBatch<P>::value;
+        static_assert(K >= 1, "tiles per ticket");
+        const unsigned batches = (num_tiles + K - 1) / K;
+        unsigned batch_next = 0, batch_end = 0;   // tiles left of the current batch
+        // takes the next tile (num_tiles once they are done) and, for a real
         // tile, starts its L2 prefetch
         auto take = [&]() -> unsigned {
             if (tickets_done) return num_tiles;
-            unsigned t = 0;
-            if (lane == 0) t = atomicAdd(&st->ticket, 1u);
-            t = __shfl_sync(kFullMask, t, 0);
-            if (t >= num_tiles) {
-                tickets_done = true;
-                // the block that takes the launch's last ticket closes the launch
-                if (t == num_tiles + gridDim.x - 1) finish_launch(st, status, num_tiles, capacity, lane);
-                return num_tiles;
+            if (batch_next >= batch_end) {
+                unsigned b = 0;
+                if (lane == 0) b = atomicAdd(&st->ticket, 1u);
+                b = __shfl_sync(kFullMask, b, 0);
+                if (b >= batches) {
+                    tickets_done = true;
+                    // the block that takes the launch's last ticket closes the launch
+                    if (b == batches + gridDim.x - 1) finish_launch(st, status, num_tiles, capacity, lane);
+                    return num_tiles;
+                }
+                batch_next = b * K;
+                batch_end = batch_next + K < num_tiles ? batch_next + K : num_tiles;
             }
+            const unsigned t = batch_next++;
             if (D > 0 && lane == 0) P::prefetch_l2(args, t, pre_pol);
             return t;
         };
@@ -635,8 +657,11 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
 // ---------------------------------------------------------------------------
 // AH / BH: L2 hints of the pass-A and pass-B copies; STREAM_OUT: evict-first
 // (.cs) output stores.
+// PARTS: pass A also folds each consume warp's 512-element part, so every
+// consume warp starts from its own prefix and the consume step has no
+// barrier; TB: tiles per ticket.
 template <class OpT, bool INCLUSIVE, int NS_, int NR_, int VECS_, int SA_, int SB_, int R_, int AH = kL2EvictLast,
-          int BH = kL2EvictFirst, bool STREAM_OUT = true, int PREFETCH = 0>
+          int BH = kL2EvictFirst, bool STREAM_OUT = true, int PREFETCH = 0, bool PARTS = false, unsigned TB = 1>
 struct ScanPolicy {
     using Op = OpT;
     static constexpr int kAHint = AH, kBHint = BH, kPrefetch = PREFETCH;
@@ -648,6 +673,9 @@ struct ScanPolicy {
     static constexpr size_t kABytes = static_cast<size_t>(kTile) * 4;
     static constexpr size_t kBBytes = static_cast<size_t>(kTile) * 4;
     static constexpr bool kHasExtra = false;
+    static constexpr int kParts = PARTS ? NS_ : 0;   // one part per consume warp
+    static constexpr bool kWarpIndependent = PARTS;
+    static constexpr unsigned kTicketBatch = TB;
     struct Args {
         const S *in;
         S *out;
@@ -695,6 +723,51 @@ struct ScanPolicy {
             for (unsigned e = rtid; e < len; e += nthr) v0 = op(v0, e < cp ? buf[e] : a.in[base + e]);
         }
         v = op(op(v0, v1), op(v2, v3));
+    }
+    // pass A with parts: part q (consume warp q's kWarpItems elements) folded
+    // into part[q]; reduce warp rw takes parts rw, rw + NR, ...; v: the fold
+    // of this warp's parts in lane 0 (the kernel folds the lanes and warps)
+    __device__ static void reduce_parts(const Args &a, const unsigned char *abuf, unsigned t, int rtid, int, S &v,
+                                        unsigned &, uint32_t *part)
+    {
+        static_assert(NS_ % NR_ == 0, "whole parts per reduce warp");
+        constexpr int PPW = NS_ / NR_;
+        const Op op;
+        const int lane = rtid & 31, rw = rtid >> 5;
+        const S *buf = reinterpret_cast<const S *>(abuf);
+        const unsigned cp = copied(a, t), len = tile_len(a, t);
+        const size_t base = static_cast<size_t>(t) * kTile;
+        // every part's loads first, then the folds and stores: a store to
+        // part[] between them would keep the next part's loads behind it
+        S pv[PPW];
+        if (cp == static_cast<unsigned>(kTile)) {
+#pragma unroll
+            for (int i = 0; i < PPW; ++i) {
+                const uint4 *b4 = reinterpret_cast<const uint4 *>(buf + (rw + i * NR_) * kWarpItems);
+                pv[i] = Op::identity();
+#pragma unroll
+                for (int k = 0; k < VECS; ++k) {
+                    const uint4 u = b4[k * 32 + lane];
+                    pv[i] = op(pv[i], op(op(from_bits<S>(u.x), from_bits<S>(u.y)), op(from_bits<S>(u.z), from_bits<S>(u.w))));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < PPW; ++i) {
+                const unsigned p0 = static_cast<unsigned>((rw + i * NR_) * kWarpItems);
+                pv[i] = Op::identity();
+                for (unsigned e = p0 + lane; e < p0 + kWarpItems && e < len; e += 32)
+                    pv[i] = op(pv[i], e < cp ? buf[e] : a.in[base + e]);
+            }
+        }
+        S mine = Op::identity();
+#pragma unroll
+        for (int i = 0; i < PPW; ++i) {
+            const S w = warp_fold(op, pv[i]);
+            if (lane == 0) part[rw + i * NR_] = to_bits(w);
+            mine = op(mine, w);
+        }
+        v = (lane == 0) ? mine : Op::identity();
     }
     __device__ static void after_reduce(const Args &, unsigned, unsigned) {}
     // This warp's rows of the consumed tile, from the B buffer (elements past
@@ -782,16 +855,51 @@ struct ScanPolicy {
                 }
         }
     }
+    // Scans the rows in place from `pfx`, the prefix of this warp's part
+    // (no barrier: the parts' prefixes come from pass A).
+    __device__ static void scan_x_from(S pfx, int lane, S (&x)[VECS][4])
+    {
+        const Op op;
+        S tt[VECS];
+#pragma unroll
+        for (int q = 0; q < VECS; ++q) tt[q] = op(op(x[q][0], x[q][1]), op(x[q][2], x[q][3]));
+        S row_excl[VECS], warp_total;
+        warp_scan_rows<Op, VECS>(op, tt, lane, row_excl, warp_total);
+#pragma unroll
+        for (int q = 0; q < VECS; ++q) {
+            S cur = op(pfx, row_excl[q]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const S v = x[q][j];
+                if (INCLUSIVE) {
+                    cur = op(cur, v);
+                    x[q][j] = cur;
+                } else {
+                    x[q][j] = cur;
+                    cur = op(cur, v);
+                }
+            }
+        }
+    }
     template <class Release>
     __device__ static unsigned consume(const Args &a, const ConsumeTile<S> &ct, uint32_t *wbuf0, uint32_t *wbuf1,
                                        int warp, int lane, Release &release)
     {
         S x[VECS][4];
         load_x(a, ct, warp, lane, x);
-        release();   // the tile is in registers now
-        scan_x(ct, wbuf0, wbuf1, warp, lane, x);
-        store_x(a.out, a.n, ct.tile, warp, lane, x);
-        return 1;   // one warp-totals buffer used
+        if constexpr (PARTS) {
+            const Op op;
+            const S pfx = op(ct.prefix, from_bits<S>(ct.part_excl[warp]));
+            release();   // the tile and the part's prefix are in registers now
+            scan_x_from(pfx, lane, x);
+            store_x(a.out, a.n, ct.tile, warp, lane, x);
+            return 0;
+        } else {
+            release();   // the tile is in registers now
+            scan_x(ct, wbuf0, wbuf1, warp, lane, x);
+            store_x(a.out, a.n, ct.tile, warp, lane, x);
+            return 1;   // one warp-totals buffer used
+        }
     }
 };
 

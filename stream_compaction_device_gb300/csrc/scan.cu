@@ -179,11 +179,13 @@ cudaError_t launch_lookback(const void *in, void *out, size_t n, const Workspace
 
 // Geometry of the pipelined scan: 16 consume warps x 4 rows (8,192-element
 // tiles), 4 reduce warps, 2 A buffers, 4 B buffers, 10 in-flight records
-// (1,024 threads, about 193 KiB of shared memory: one block per SM); tickets
-// are taken one tile ahead and prefetched into L2.  Chosen by sweeps on
-// GB300: the reduce step sits on the A ring's turnaround, so four reduce
-// warps beat two (by 3-4%); deeper prefetch and more records overflow what
-// L2 keeps.
+// (1,024 threads, about 193 KiB of shared memory: one block per SM); tiles
+// are taken one ahead and prefetched into L2.  Chosen by sweeps on GB300:
+// the reduce step sits on the A ring's turnaround, so four reduce warps beat
+// two (by 3-4%); deeper prefetch and more records overflow what L2 keeps.
+// Pass A also folds each consume warp's part, so the consume warps need no
+// barrier, and a ticket hands out two tiles: together 1.2% faster at 2^28
+// (either alone gained nothing, two tiles per ticket alone lost 3%).
 constexpr unsigned kWaitLimit = 1u << 18;   // bounded mbarrier polls (~1 us each at most)
 constexpr size_t kPipelineMinN = size_t(1) << 20;
 // Sizes the L2-resident scan takes by default: measured on GB300 (L2 flushed
@@ -197,7 +199,7 @@ cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspac
                              cudaStream_t s)
 {
     using S = typename Op::S;
-    using P = ScanPolicy<Op, INCLUSIVE, 16, 4, 4, 2, 4, 10, kL2EvictLast, kL2EvictFirst, true, 1>;
+    using P = ScanPolicy<Op, INCLUSIVE, 16, 4, 4, 2, 4, 10, kL2EvictLast, kL2EvictFirst, true, 1, true, 2>;
     using G = PipeShape<P>;
     auto kernel = pipeline_l2_kernel<P>;
     static std::atomic<unsigned long long> attribute_set{0};   // one bit per device

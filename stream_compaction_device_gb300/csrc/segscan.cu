@@ -255,20 +255,6 @@ segscan_tile_kernel(const typename Op::S *__restrict__ in, const uint8_t *__rest
     store_rows<S, VECS, ALIGNED>(out, warp_base, n, lane, full, x);
 }
 
-// Fold of v over the warp (the result in every lane): one redux instruction
-// for the integer operators, shuffles for fp32.
-__device__ __forceinline__ uint32_t warp_fold(const AddU32 &, uint32_t v) { return __reduce_add_sync(kFullMask, v); }
-__device__ __forceinline__ uint32_t warp_fold(const XorU32 &, uint32_t v) { return __reduce_xor_sync(kFullMask, v); }
-__device__ __forceinline__ uint32_t warp_fold(const MaxU32 &, uint32_t v) { return __reduce_max_sync(kFullMask, v); }
-__device__ __forceinline__ int32_t warp_fold(const MaxI32 &, int32_t v) { return __reduce_max_sync(kFullMask, v); }
-template <class Op>
-__device__ __forceinline__ typename Op::S warp_fold(const Op &op, typename Op::S v)
-{
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
-    return v;
-}
-
 // Index of the highest nonzero byte of a nonzero word.
 __device__ __forceinline__ int top_byte(uint32_t w) { return (31 - __clz(static_cast<int>(w))) >> 3; }
 
