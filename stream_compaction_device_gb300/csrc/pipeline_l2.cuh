@@ -283,6 +283,7 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
     using G = PipeShape<P>;
     constexpr int NS = G::NS, NR = G::NR, R = G::R, SA = G::SA, SB = G::SB;
     constexpr bool SEG = IsSegmented<P>::value;
+    static_assert(!SEG || G::kParts > 0, "a segmented policy reports its parts' pairs");
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *abuf = smem + G::kABase;
     unsigned char *bbuf = smem + G::kBBase;
@@ -533,7 +534,7 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
             if (lane == 0) mbar_arrive(&ctrl->a_empty[a]);   // buffer read: free it
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
-            if (P::kHasExtra || SEG) extra = __reduce_add_sync(kFullMask, extra);
+            if (P::kHasExtra) extra = __reduce_add_sync(kFullMask, extra);
             if (lane == 0) {
                 ctrl->red[rw] = to_bits(v);
                 ctrl->red_extra[rw] = extra;
@@ -559,19 +560,6 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                     for (int q = 0; q < G::kParts; ++q)
                         agg = ((pmask >> q) & 1u) ? from_bits<S>(pval[q]) : op(agg, from_bits<S>(pval[q]));
                     head = pmask != 0 ? 1u : 0u;
-                } else if (SEG) {
-                    // in order: a warp whose part holds a head restarts the fold
-                    agg = Op::identity();
-#pragma unroll
-                    for (int w = 0; w < NR; ++w) {
-                        const S vw = from_bits<S>(ctrl->red[w]);
-                        if (ctrl->red_extra[w] != 0) {
-                            agg = vw;
-                            head = 1;
-                        } else {
-                            agg = op(agg, vw);
-                        }
-                    }
                 } else {
 #pragma unroll
                     for (int w = 1; w < NR; ++w) {
