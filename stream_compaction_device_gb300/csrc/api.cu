@@ -244,10 +244,16 @@ devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out
     if (n == 0) return from_cuda(cudaMemsetAsync(count, 0, sizeof(int32_t), stream));
     const unsigned tiles = tiles_for(n, kCompactTile);
     Workspace ws;
-    const devscan_status st = acquire(stream, tiles, &ws);
+    devscan_status st = acquire(stream, tiles, &ws);
     if (st != DEVSCAN_OK) return st;
-    return from_cuda(launch_compact(in, flags, out, count, n, g_carry_mode.load(std::memory_order_relaxed), ws,
-                                    kSpinLimit, stream));
+    const int carry = g_carry_mode.load(std::memory_order_relaxed);
+    void *part_words = nullptr;   // the two-launch path's part counts and offsets
+    if (carry == kCarryL2Resident || (carry == kCarryDefault && n >= kCompactTwoPassMinN)) {
+        st = acquire_extra(stream, compact_part_words(n) * sizeof(uint32_t), &part_words);
+        if (st != DEVSCAN_OK) return st;
+    }
+    return from_cuda(launch_compact(in, flags, out, count, n, carry, ws, kSpinLimit, stream,
+                                    static_cast<uint32_t *>(part_words)));
 }
 
 devscan_status compact_gt_i32(const int32_t *in, int32_t threshold, int32_t *out, int32_t *count, size_t n,

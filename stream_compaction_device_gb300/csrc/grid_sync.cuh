@@ -1,12 +1,30 @@
-// Grid-wide barrier for cooperative launches (sm_103a): every block of the
-// grid is resident, so a counter in the stream's device state can gather
-// them.  Used by the kernels that fold their chunks, meet once, then finish
-// with every chunk's offset known.
+// Helpers of the cooperative launches (sm_103a): loads whose lines L2 keeps
+// for a second read, and a grid-wide barrier -- every block of the grid is
+// resident, so a counter in the stream's device state can gather them.  Used
+// by the kernels that fold their chunks, meet once, then finish with every
+// chunk's offset known.
 #pragma once
 
 #include "core.cuh"
 
 namespace devscan {
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 128-bit load whose lines L2 keeps (evict_last).
+__device__ __forceinline__ uint4 ld_keep(const uint4 *p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 {

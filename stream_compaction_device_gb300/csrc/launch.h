@@ -62,8 +62,16 @@ cudaError_t launch_stalled_wait(const Workspace &ws, unsigned spin_limit, cudaSt
 
 // `carry` (kCarry*): the pipelined kernel for kCarryPipelined, the one-tile
 // kernel for kCarryLookback, the measured size threshold otherwise.
+// part_words: compact_part_words(n) words of per-stream scratch for the
+// two-launch path (taken, for 16-byte-aligned values and flags, from
+// kCompactTwoPassMinN elements and in carry mode 4), or null.  Measured on
+// GB300: it beats the pipeline from 2^24 (1% kept: 59 against 75 us at 2^26;
+// 50% and 99%: level or ahead) and loses below 2^23 to its second launch.
+constexpr size_t kCompactTwoPassMinN = size_t(1) << 23;
+size_t compact_part_words(size_t n);
 cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out, int32_t *count, size_t n,
-                           int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+                           int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s,
+                           uint32_t *part_words = nullptr);
 
 // Zero count of bit `bit` over keys[0, n) added into *zeros (which the caller
 // has cleared).

@@ -27,23 +27,6 @@
 namespace devscan {
 namespace {
 
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// 128-bit load whose lines L2 keeps (evict_last).
-__device__ __forceinline__ uint4 ld_keep(const uint4 *p, uint64_t pol)
-{
-    uint4 v;
-    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p), "l"(pol));
-    return v;
-}
-
 template <class Op, bool INCLUSIVE, int THREADS, int VECS>
 __global__ void __launch_bounds__(THREADS, 1)
 l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,

@@ -22,10 +22,11 @@ def ds():
     return m
 
 
-@pytest.fixture(params=["lookback", "pipelined"])
+@pytest.fixture(params=["lookback", "pipelined", "l2"])
 def mode(request, ds):
     """Run a test once on each kernel family (one tile per block; the
-    persistent two-pass pipeline)."""
+    persistent two-pass pipeline; for compaction in mode "l2", the two-launch
+    count-then-write path at every size)."""
     ds.set_carry_mode(request.param)
     yield request.param
     ds.set_carry_mode("default")
