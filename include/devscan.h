@@ -220,10 +220,10 @@ devscan_status devscan_stream_release(cudaStream_t stream);
  * mentions chaining blocks inside one launch):
  *   0 = default: for 16-byte-aligned in/out the scans take 4 for
  *       2^17 <= n <= 2^24 and 3 above; compaction with flags takes 3 from
- *       n = 2^19 and 4 from 2^23; the split, the bracket scan and the
- *       segmented scan take 3 from n = 2^19; the bracket check without the
- *       scanned array (out == NULL) takes 4 from n = 2^17 (below 2^31);
- *       everything else takes 1;
+ *       n = 2^19 and 4 from 2^23; split_bit_u32 takes 4 from 2^20; the
+ *       sorts' splits, the bracket scan and the segmented scan take 3 from
+ *       n = 2^19; the bracket check without the scanned array (out == NULL)
+ *       takes 4 from n = 2^17 (below 2^31); everything else takes 1;
  *   1 = one tile per block, single-pass decoupled look-back;
  *   2 = reduce-then-scan (three launches, one extra read of the input);
  *   3 = pipelined single pass: persistent warp-specialised blocks with bulk
@@ -235,8 +235,9 @@ devscan_status devscan_stream_release(cudaStream_t stream);
  *       the fused-predicate compaction, split, the segmented scan and the
  *       bracket scan with its array stored use 3); the bracket check alone
  *       takes its one-read cooperative kernel at every size below 2^31, and
- *       compaction with flags its two-launch path (a cooperative count and
- *       scan of 512-element parts, then a warp per part writing its run).
+ *       compaction with flags and split_bit_u32 their two-launch paths (a
+ *       cooperative count and scan of 512-element parts, then a warp per
+ *       part writing its runs).
  * Compaction and the split follow the same choice between 1 and 3 (their
  * pipelined kernels need 16-byte-aligned inputs, and flags too for
  * compaction).  Process-wide; meant for measurement.  Returns

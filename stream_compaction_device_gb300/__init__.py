@@ -242,7 +242,8 @@ def device_status(stream=None) -> int:
 def set_carry_mode(mode: str) -> None:
     """'default', 'lookback' (one tile per block), 'rts' (reduce-then-scan),
     'pipelined' (persistent warp-specialised single pass) or 'l2' (the
-    L2-resident cooperative scan, scans only), process-wide."""
+    cooperative forms: the L2-resident scan, the one-read bracket check, the
+    two-launch compaction with flags and split), process-wide."""
     code = {"default": 0, "lookback": 1, "rts": 2, "pipelined": 3, "l2": 4}[mode]
     _lib.check(load().devscan_set_carry_mode(code), "devscan_set_carry_mode")
 

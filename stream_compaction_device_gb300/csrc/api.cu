@@ -309,11 +309,19 @@ devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_
     devscan_status st = acquire(stream, tiles, &ws);
     if (st != DEVSCAN_OK) return st;
     unsigned *z = &ws.state->zeros[40];
+    const int carry = g_carry_mode.load(std::memory_order_relaxed);
+    if (reinterpret_cast<uintptr_t>(keys) % 16 == 0 &&
+        (carry == kCarryL2Resident || (carry == kCarryDefault && n >= kSplitTwoPassMinN))) {
+        void *part_words = nullptr;   // the parts' zero offsets
+        st = acquire_extra(stream, split_part_words(n) * sizeof(uint32_t), &part_words);
+        if (st != DEVSCAN_OK) return st;
+        return from_cuda(launch_split_two_pass(keys, out, n, bit, z, static_cast<uint32_t *>(part_words), ws,
+                                               kSpinLimit, stream));
+    }
     if (cudaMemsetAsync(z, 0, sizeof(unsigned), stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
     cudaError_t e = launch_count_zeros(keys, n, bit, z, ws, stream);
     if (e != cudaSuccess) return DEVSCAN_ERR_CUDA;
-    return from_cuda(launch_split(keys, out, n, bit, z, nullptr, g_carry_mode.load(std::memory_order_relaxed), ws,
-                                  kSpinLimit, stream));
+    return from_cuda(launch_split(keys, out, n, bit, z, nullptr, carry, ws, kSpinLimit, stream));
 }
 
 devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStream_t stream)

@@ -78,6 +78,18 @@ cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out
 cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned *zeros, const Workspace &ws,
                                cudaStream_t s);
 
+// A standalone split in two launches: zeros counted per 512-key part (their
+// offsets and the total into *zeros), then a warp per part writes its runs;
+// part_words: split_part_words(n) words of per-stream scratch.  Taken for
+// 16-byte-aligned keys from kSplitTwoPassMinN keys and in carry mode 4;
+// measured on GB300 it beats the count pass plus the pipelined split at every
+// size from 2^20 (138 against 170 us at 2^26).  A sort's passes keep the
+// pipeline, which counts the next bit's zeros as it goes.
+constexpr size_t kSplitTwoPassMinN = size_t(1) << 20;
+size_t split_part_words(size_t n);
+cudaError_t launch_split_two_pass(const uint32_t *keys, uint32_t *out, size_t n, int bit, unsigned *zeros,
+                                  uint32_t *part_words, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
 // One split pass by bit `bit` given the total zero count *zeros.  When
 // next_zeros is not null, the pass also adds the zero count of bit
 // `bit + 1` into *next_zeros.

@@ -14,6 +14,7 @@
 #include <atomic>
 
 #include "core.cuh"
+#include "grid_sync.cuh"
 #include "launch.h"
 #include "pipeline_l2.cuh"
 #include "split_policy.cuh"
@@ -177,6 +178,179 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
         count_zeros_kernel<THREADS, true><<<grid, THREADS, 0, s>>>(keys, n, bit, zeros);
     else
         count_zeros_kernel<THREADS, false><<<grid, THREADS, 0, s>>>(keys, n, bit, zeros);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Two-launch split (a standalone split, which must count the zeros first
+// anyway): one cooperative launch counts the zeros of every 512-key part,
+// meets at a grid barrier and turns the counts into the parts' exclusive
+// offsets and the total Z; then a warp per part ranks its keys and writes its
+// zeros run at its offset and its ones run at Z + (keys before the part -
+// its offset).  The same bytes as the count pass plus the pipelined split
+// (12 per key), without a chain between tiles.
+// ---------------------------------------------------------------------------
+constexpr int kSplitPart = 512, kSplitCountThreads = 1024, kSplitWriteWarps = 8, kSplitCountBatch = 2;
+
+// off[p]: zeros of bit `bit` in parts 0 .. p-1 (first the part's own count);
+// *zeros = all zeros.  Block b takes parts [b * chunk, (b + 1) * chunk).
+__global__ void __launch_bounds__(kSplitCountThreads, 1)
+split_count_kernel(const uint32_t *__restrict__ keys, size_t n, int bit, unsigned parts, unsigned chunk,
+                   uint32_t *__restrict__ off, uint32_t *__restrict__ block_sums, unsigned *__restrict__ zeros,
+                   DevState *st, unsigned spin_limit)
+{
+    constexpr int NW = kSplitCountThreads / 32, B = kSplitCountBatch;
+    __shared__ uint32_t s_w[NW];
+    __shared__ uint32_t s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned p0 = blockIdx.x * chunk, p1 = p0 + chunk < parts ? p0 + chunk : parts;
+    // phase 1: warp w takes parts p0 + w, p0 + w + NW, ..., B at a time;
+    // lane L reads the part's 16-byte groups L, L + 32, L + 64, L + 96
+    uint32_t mine = 0;
+    for (unsigned pb = p0 + warp; pb < p1; pb += NW * B) {
+        uint4 q[B][4];
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const unsigned p = pb + k * NW;
+            if (p < p1 && static_cast<size_t>(p + 1) * kSplitPart <= n) {
+                const uint4 *k4 = reinterpret_cast<const uint4 *>(keys + static_cast<size_t>(p) * kSplitPart);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) q[k][g] = __ldcs(k4 + g * 32 + lane);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const unsigned p = pb + k * NW;
+            if (p >= p1) break;   // warp-uniform
+            uint32_t z = 0;
+            if (static_cast<size_t>(p + 1) * kSplitPart <= n) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) z += zeros_of(q[k][g], bit);
+            } else {
+                const size_t e0 = static_cast<size_t>(p) * kSplitPart;
+                for (size_t e = e0 + lane; e < n && e < e0 + kSplitPart; e += 32) z += ((keys[e] >> bit) & 1u) ? 0u : 1u;
+            }
+            z = __reduce_add_sync(kFullMask, z);
+            if (lane == 0) off[p] = z;
+            mine += z;
+        }
+    }
+    if (lane == 0) s_w[warp] = mine;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t v = __reduce_add_sync(kFullMask, s_w[lane]);
+        if (lane == 0) block_sums[blockIdx.x] = v;
+    }
+
+    const bool ok = grid_barrier(st, gridDim.x, spin_limit);
+
+    // phase 2: the counts become offsets in place, a block of parts at a time
+    if (warp == 0) {
+        uint32_t v = 0;
+        if (ok)
+            for (unsigned b = lane; b < blockIdx.x; b += 32) v += __ldcg(block_sums + b);
+        v = __reduce_add_sync(kFullMask, v);
+        if (lane == 0) s_carry = v;
+    }
+    __syncthreads();
+    uint32_t carry = s_carry;
+    for (unsigned base = p0; base < p1; base += kSplitCountThreads) {
+        const unsigned p = base + tid;
+        const uint32_t c = p < p1 ? off[p] : 0u;   // this thread's own part: read before it is overwritten
+        // exclusive scan over the block
+        uint32_t inc = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
+            if (lane >= d) inc += u;
+        }
+        if (lane == 31) s_w[warp] = inc;
+        __syncthreads();
+        uint32_t w = s_w[lane], wi = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t u = __shfl_up_sync(kFullMask, wi, d);
+            if (lane >= d) wi += u;
+        }
+        const uint32_t total = __shfl_sync(kFullMask, wi, NW - 1);
+        const uint32_t excl = __shfl_sync(kFullMask, wi - w, warp) + inc - c;
+        if (p < p1) off[p] = carry + excl;
+        carry += total;
+        __syncthreads();   // s_w is read before the next round writes it
+    }
+    if (blockIdx.x == gridDim.x - 1 && tid == 0) *zeros = carry;
+    grid_depart(st, gridDim.x);
+}
+
+// Warp w of block b splits part b * kSplitWriteWarps + w.
+template <bool OUT_ALIGNED>
+__global__ void __launch_bounds__(kSplitWriteWarps * 32)
+split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size_t n, int bit, unsigned parts,
+                   const uint32_t *__restrict__ off, const unsigned *__restrict__ zeros)
+{
+    constexpr int kStage = kSplitPart + 12;   // the zeros, the ones from the next 16-byte boundary, a spare chunk
+    __shared__ __align__(16) uint32_t s_stage[kSplitWriteWarps][kStage];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned p = blockIdx.x * kSplitWriteWarps + warp;
+    if (p >= parts) return;   // the whole warp: no barrier follows
+    const size_t b = static_cast<size_t>(p) * kSplitPart;
+    const unsigned part_len = n - b < static_cast<size_t>(kSplitPart) ? static_cast<unsigned>(n - b) : kSplitPart;
+    uint32_t x[4][4], zmask[4];
+    if (part_len == static_cast<unsigned>(kSplitPart)) {
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(keys + b);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 u = __ldcs(k4 + q * 32 + lane);
+            x[q][0] = u.x;
+            x[q][1] = u.y;
+            x[q][2] = u.z;
+            x[q][3] = u.w;
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m |= ((x[q][j] >> bit) & 1u) << j;
+            zmask[q] = m ^ 0xfu;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const unsigned i = static_cast<unsigned>((q * 32 + lane) * 4 + j);
+                x[q][j] = i < part_len ? keys[b + i] : 0u;
+                if (i < part_len && !((x[q][j] >> bit) & 1u)) m |= 1u << j;
+            }
+            zmask[q] = m;
+        }
+    }
+    const size_t zeros_at = off[p];
+    const size_t ones_at = static_cast<size_t>(*zeros) + (b - zeros_at);
+    split_write_warp<4>(x, zmask, part_len, zeros_at, ones_at, lane, s_stage[warp], out, OUT_ALIGNED, n);
+}
+
+size_t split_part_words(size_t n) { return (n + kSplitPart - 1) / kSplitPart; }
+
+cudaError_t launch_split_two_pass(const uint32_t *keys, uint32_t *out, size_t n, int bit, unsigned *zeros,
+                                  uint32_t *part_words, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+{
+    const unsigned parts = static_cast<unsigned>(split_part_words(n));
+    unsigned blocks = static_cast<unsigned>(ws.num_sms);
+    const unsigned need = (parts + 31) / 32;
+    if (blocks > need) blocks = need;
+    const unsigned chunk = (parts + blocks - 1) / blocks;
+    blocks = (parts + chunk - 1) / chunk;
+    uint32_t *sums = ws.tile_sums;
+    DevState *st = ws.state;
+    void *args[] = {const_cast<uint32_t **>(&keys), &n, &bit, const_cast<unsigned *>(&parts),
+                    const_cast<unsigned *>(&chunk), &part_words, &sums, &zeros, &st, &spin_limit};
+    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(&split_count_kernel), dim3(blocks),
+                                                dim3(kSplitCountThreads), args, 0, s);
+    if (e != cudaSuccess) return e;
+    const unsigned wblocks = (parts + kSplitWriteWarps - 1) / kSplitWriteWarps;
+    if (reinterpret_cast<uintptr_t>(out) % 16 == 0)
+        split_write_kernel<true><<<wblocks, kSplitWriteWarps * 32, 0, s>>>(keys, out, n, bit, parts, part_words, zeros);
+    else
+        split_write_kernel<false><<<wblocks, kSplitWriteWarps * 32, 0, s>>>(keys, out, n, bit, parts, part_words, zeros);
     return cudaGetLastError();
 }
 
