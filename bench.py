@@ -502,6 +502,8 @@ def run_op(args):
     import stream_compaction_device_gb300 as ds
     from stream_compaction_device_gb300 import workloads as wl
     ds.load()
+    if args.carry != "default":
+        ds.set_carry_mode(args.carry)
     n = args.n
     if args.op == "compact50":
         v = wl.compaction_values(n)
@@ -548,7 +550,7 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--n", type=int, default=N_HEADLINE)
-    p.add_argument("--carry", choices=["default", "lookback", "rts"], default="default")
+    p.add_argument("--carry", choices=["default", "lookback", "rts", "pipelined"], default="default")
     p.add_argument("--extra-reps", type=int, default=20)
     p.add_argument("--cpu-budget", type=float, default=10.0)
     p.add_argument("--no-extras", action="store_true")

@@ -315,8 +315,7 @@ devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_
         void *part_words = nullptr;   // the parts' zero offsets
         st = acquire_extra(stream, split_part_words(n) * sizeof(uint32_t), &part_words);
         if (st != DEVSCAN_OK) return st;
-        return from_cuda(launch_split_two_pass(keys, out, n, bit, z, static_cast<uint32_t *>(part_words), ws,
-                                               kSpinLimit, stream));
+        return from_cuda(launch_split_two_pass(keys, out, n, bit, z, static_cast<uint32_t *>(part_words), ws, stream));
     }
     if (cudaMemsetAsync(z, 0, sizeof(unsigned), stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
     cudaError_t e = launch_count_zeros(keys, n, bit, z, ws, stream);

@@ -134,148 +134,117 @@ compact_kernel(const uint32_t *__restrict__ in, const uint8_t *__restrict__ flag
 // ---------------------------------------------------------------------------
 // Two-launch compaction with flags (pgsm.cn "SIMT数据依赖与并行前缀和" section
 // 4.2's count-then-scatter order, on parts of 512 elements):
-//   compact_count_kernel  one cooperative launch: every 512-element part's
-//                         keep mask (one bit per element, 64 bytes) and kept
-//                         count, a grid barrier, then the exclusive offsets
-//                         of the parts and *count;
-//   compact_write_kernel  a warp per part takes its mask, ranks its kept
-//                         elements, stages them and writes one run at the
-//                         part's offset; a part that keeps at most
-//                         kSparseKept elements loads only the 16-byte groups
-//                         of values that hold one.
+//   compact_count_kernel  a block per SM streams its chunk of parts through
+//                         shared memory: every part's keep mask (one bit per
+//                         element, 64 bytes) and kept count, then the parts'
+//                         offsets within the chunk; the last block to finish
+//                         scans the chunk totals into chunk carries and
+//                         writes *count;
+//   compact_write_kernel  launched as a programmatic dependent of the count
+//                         (its launch overlaps the count's tail): a warp per
+//                         part takes its mask, ranks its kept elements,
+//                         stages them and writes one run at the part's
+//                         offset plus its chunk's carry; a part that keeps at
+//                         most kSparseKept elements loads only the 16-byte
+//                         groups of values that hold one.
 // No part waits on another, so the write launch streams.  HBM moves the
 // flags once, the masks (1/8 of the flags) twice, the values once (only
 // their kept groups for sparse parts) and the kept values once.
 // ---------------------------------------------------------------------------
 constexpr int kPartElems = 512;
 constexpr unsigned kSparseKept = 32;
-constexpr int kCountThreads = 1024, kWriteWarps = 8, kCountBatch = 4;
-
-// Exclusive add-scan of one value per thread over the block; `total` gets the
-// block's sum.  s_w holds THREADS / 32 words; the caller separates two calls
-// with a barrier.
-template <int THREADS>
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *s_w, int tid, uint32_t &total)
-{
-    constexpr int NW = THREADS / 32;
-    const int lane = tid & 31, warp = tid >> 5;
-    uint32_t inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
-        if (lane >= d) inc += u;
-    }
-    if (lane == 31) s_w[warp] = inc;
-    __syncthreads();
-    uint32_t w = lane < NW ? s_w[lane] : 0u, wi = w;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t u = __shfl_up_sync(kFullMask, wi, d);
-        if (lane >= d) wi += u;
-    }
-    total = __shfl_sync(kFullMask, wi, NW - 1);
-    return __shfl_sync(kFullMask, wi - w, warp) + inc - v;
-}
+constexpr int kCountThreads = 1024, kCountStageParts = 128, kCountStages = 3, kWriteWarps = 8, kWriteMinBlocks = 1;
+constexpr unsigned kCountWaitLimit = 1u << 18;
+constexpr unsigned kMaxCountBlocks = 512;   // chunk totals and carries share the workspace's tile sums
 
 // mask[16 p .. 16 p + 15] = part p's keep bits (bit i of word w: element
-// 32 w + i); cnt[p] = its kept elements; then off[p] = kept elements of parts
-// 0 .. p-1; *count = all kept.  Block b takes parts [b * chunk, (b + 1) *
-// chunk) (block_sums: one word per block).
-__global__ void __launch_bounds__(kCountThreads, 1)
+// 32 w + i); cnt[p] = its kept elements; off[p] = kept elements of the parts
+// before p in its chunk.  Block b takes the chunk of parts [b * chunk,
+// (b + 1) * chunk): its whole parts stream through NSTG shared-memory stages
+// of SP parts (dynamic shared memory), the ragged last part of the input
+// takes plain loads.  The last block writes carry[b] = kept elements of the
+// chunks before b, and *count (block_sums: one word per block).
+template <int THREADS, int SP, int NSTG>
+__global__ void __launch_bounds__(THREADS, 1)
 compact_count_kernel(const uint8_t *__restrict__ flags, size_t n, unsigned parts, unsigned chunk,
                      uint32_t *__restrict__ mask, uint32_t *__restrict__ cnt, uint32_t *__restrict__ off,
-                     uint32_t *__restrict__ block_sums, int32_t *__restrict__ count, DevState *st,
-                     unsigned spin_limit)
+                     uint32_t *__restrict__ block_sums, uint32_t *__restrict__ carry, int32_t *__restrict__ count,
+                     DevState *st)
 {
-    constexpr int NW = kCountThreads / 32;
+    static_assert(THREADS >= static_cast<int>(kMaxCountBlocks), "the last block scans one chunk total per thread");
+    constexpr int NW = THREADS / 32;
+    extern __shared__ __align__(128) uint8_t s_ring[];
+    __shared__ uint64_t s_full[NSTG];
     __shared__ uint32_t s_w[NW];
-    __shared__ uint32_t s_carry;
+    allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned p0 = blockIdx.x * chunk, p1 = p0 + chunk < parts ? p0 + chunk : parts;
+    const unsigned whole = static_cast<unsigned>(n / kPartElems);
+    const unsigned q1 = p1 < whole ? p1 : (p0 > whole ? p0 : whole);   // [p0, q1): whole parts
 
-    // phase 1: warp w takes parts p0 + w, p0 + w + NW, ..., kCountBatch at a
-    // time (their loads issued together); lane L reads flags 16L .. 16L + 15
-    uint32_t mine = 0;
-    for (unsigned pb = p0 + warp; pb < p1; pb += NW * kCountBatch) {
-        uint4 q[kCountBatch];
-#pragma unroll
-        for (int k = 0; k < kCountBatch; ++k) {
-            const unsigned p = pb + k * NW;
-            if (p < p1 && static_cast<size_t>(p + 1) * kPartElems <= n)
-                q[k] = __ldcs(reinterpret_cast<const uint4 *>(flags + static_cast<size_t>(p) * kPartElems + 16u * lane));
-        }
-#pragma unroll
-        for (int k = 0; k < kCountBatch; ++k) {
-            const unsigned p = pb + k * NW;
-            if (p >= p1) break;   // warp-uniform
-            uint32_t m16 = 0;
-            if (static_cast<size_t>(p + 1) * kPartElems <= n) {
-                m16 = nonzero_byte_mask(q[k].x) | (nonzero_byte_mask(q[k].y) << 4) |
-                      (nonzero_byte_mask(q[k].z) << 8) | (nonzero_byte_mask(q[k].w) << 12);
-            } else {
-                const size_t e = static_cast<size_t>(p) * kPartElems + 16u * lane;
-                for (unsigned j = 0; j < 16; ++j)
-                    if (e + j < n && flags[e + j] != 0) m16 |= 1u << j;
-            }
-            const uint32_t hi = __shfl_down_sync(kFullMask, m16, 1);
-            if ((lane & 1) == 0) mask[static_cast<size_t>(p) * 16 + (lane >> 1)] = m16 | (hi << 16);
-            const uint32_t c = __reduce_add_sync(kFullMask, static_cast<uint32_t>(__popc(m16)));
-            if (lane == 0) cnt[p] = c;
-            mine += c;
-        }
+    // phase 1: a part per warp; lane L takes flags 16 L .. 16 L + 15
+    auto part_done = [&](unsigned p, uint32_t m16) {
+        const uint32_t hi = __shfl_down_sync(kFullMask, m16, 1);
+        if ((lane & 1) == 0) mask[static_cast<size_t>(p) * 16 + (lane >> 1)] = m16 | (hi << 16);
+        const uint32_t c = __reduce_add_sync(kFullMask, static_cast<uint32_t>(__popc(m16)));
+        if (lane == 0) cnt[p] = c;
+    };
+    const bool streamed = stream_parts<kPartElems, SP, NSTG>(
+        flags, p0, q1, s_ring, s_full, kCountWaitLimit, [&](unsigned p, const uint8_t *part) {
+            const uint4 q = reinterpret_cast<const uint4 *>(part)[lane];
+            part_done(p, nonzero_byte_mask(q.x) | (nonzero_byte_mask(q.y) << 4) | (nonzero_byte_mask(q.z) << 8) |
+                             (nonzero_byte_mask(q.w) << 12));
+        });
+    if (!streamed && tid == 0) atomicOr(&st->error, kErrTimeout);
+    for (unsigned p = q1 + warp; p < p1; p += NW) {   // the input's ragged last part
+        const size_t e = static_cast<size_t>(p) * kPartElems + 16u * lane;
+        uint32_t m16 = 0;
+        for (unsigned j = 0; j < 16; ++j)
+            if (e + j < n && flags[e + j] != 0) m16 |= 1u << j;
+        part_done(p, m16);
     }
-    if (lane == 0) s_w[warp] = mine;
-    __syncthreads();
-    if (warp == 0) {
-        const uint32_t v = __reduce_add_sync(kFullMask, s_w[lane]);
-        if (lane == 0) block_sums[blockIdx.x] = v;
-    }
+    __syncthreads();   // every part's count written
 
-    const bool ok = grid_barrier(st, gridDim.x, spin_limit);
-
-    // phase 2: the block's prefix, then its parts' offsets, a block of parts at a time
-    if (warp == 0) {
-        uint32_t v = 0;
-        if (ok)
-            for (unsigned b = lane; b < blockIdx.x; b += 32) v += __ldcg(block_sums + b);
-        v = __reduce_add_sync(kFullMask, v);
-        if (lane == 0) s_carry = v;
-    }
-    __syncthreads();
-    uint32_t carry = s_carry;
-    for (unsigned base = p0; base < p1; base += kCountThreads) {
+    // phase 2: the parts' offsets within the chunk, THREADS parts at a time
+    uint32_t run = 0;
+    for (unsigned base = p0; base < p1; base += THREADS) {
         const unsigned p = base + tid;
-        const uint32_t c = p < p1 ? cnt[p] : 0u;   // written by this block before the barrier
+        const uint32_t c = p < p1 ? cnt[p] : 0u;
         uint32_t total;
-        const uint32_t excl = block_excl_scan<kCountThreads>(c, s_w, tid, total);
-        if (p < p1) off[p] = carry + excl;
-        carry += total;
+        const uint32_t excl = block_excl_scan<THREADS>(c, s_w, tid, total);
+        if (p < p1) off[p] = run + excl;
+        run += total;
         __syncthreads();   // s_w is read before the next round writes it
     }
-    if (blockIdx.x == gridDim.x - 1 && tid == 0) *count = static_cast<int32_t>(carry);
-    grid_depart(st, gridDim.x);
+    uint32_t all;
+    if (last_block_carries<THREADS>(run, block_sums, carry, st, s_w, all) && tid == 0)
+        *count = static_cast<int32_t>(all);
 }
 
 // Warp w of block b writes part b * kWriteWarps + w.  Lane L's row q holds
 // elements 128 q + 4 L .. + 3 of the part: mask word 4 q + L / 8, bits
-// 4 (L % 8) .. + 3.
-template <bool OUT_ALIGNED>
-__global__ void __launch_bounds__(kWriteWarps * 32)
+// 4 (L % 8) .. + 3.  The part's kept count comes from its mask, so the mask,
+// offset and carry loads go out together and the values follow them.
+template <bool OUT_ALIGNED, int MIN_BLOCKS>
+__global__ void __launch_bounds__(kWriteWarps * 32, MIN_BLOCKS)
 compact_write_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, size_t n, unsigned parts,
-                     const uint32_t *__restrict__ mask, const uint32_t *__restrict__ cnt,
-                     const uint32_t *__restrict__ off)
+                     unsigned chunk, const uint32_t *__restrict__ mask, const uint32_t *__restrict__ off,
+                     const uint32_t *__restrict__ carry)
 {
     __shared__ __align__(16) uint32_t s_stage[kWriteWarps][kPartElems + 4];
+    wait_primary_grid();   // the count launch's masks, offsets and carries
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned p = blockIdx.x * kWriteWarps + warp;
     if (p >= parts) return;   // the whole warp: no barrier follows
-    const uint32_t c = cnt[p];
-    if (c == 0) return;
-    const size_t b = static_cast<size_t>(p) * kPartElems;
     const uint32_t *mw = mask + static_cast<size_t>(p) * 16;
     uint32_t x[4][4], keep[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) keep[q] = (mw[4 * q + (lane >> 3)] >> (4 * (lane & 7))) & 0xfu;
+    const uint32_t o = off[p] + carry[p / chunk];
+    const uint32_t c = __reduce_add_sync(kFullMask, static_cast<uint32_t>(__popc(keep[0] | (keep[1] << 4) |
+                                                                                   (keep[2] << 8) | (keep[3] << 12))));
+    if (c == 0) return;
+    const size_t b = static_cast<size_t>(p) * kPartElems;
     if (b + kPartElems <= n) {
         const uint4 *v4 = reinterpret_cast<const uint4 *>(in + b);
 #pragma unroll
@@ -294,36 +263,57 @@ compact_write_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out
             for (int j = 0; j < 4; ++j)
                 x[q][j] = ((keep[q] >> j) & 1u) ? in[b + static_cast<size_t>((q * 32 + lane) * 4 + j)] : 0u;
     }
-    compact_write_warp<4>(x, keep, off[p], lane, s_stage[warp], out, OUT_ALIGNED, n);
+    compact_write_warp<4>(x, keep, o, lane, s_stage[warp], out, OUT_ALIGNED, n);
 }
 
 size_t compact_part_words(size_t n) { return 18 * ((n + kPartElems - 1) / kPartElems); }   // mask, count, offset
 
+// Parts per chunk of the count launch: one chunk per SM (fewer for small
+// inputs, at least a part per warp each), at most kMaxCountBlocks chunks.
+inline unsigned count_chunk(unsigned parts, unsigned warps, int num_sms)
+{
+    unsigned blocks = static_cast<unsigned>(num_sms) < kMaxCountBlocks ? static_cast<unsigned>(num_sms) : kMaxCountBlocks;
+    const unsigned need = (parts + warps - 1) / warps;
+    if (blocks > need) blocks = need;
+    return (parts + blocks - 1) / blocks;
+}
+
+// The count launch: THREADS per block, NSTG * SP * 512 bytes of stages.
+// part_words: mask[16 parts] | cnt[parts] | off[parts]; the workspace's tile
+// sums hold the chunk totals (first kMaxCountBlocks words) and carries (next).
+template <int THREADS, int SP, int NSTG>
+cudaError_t launch_compact_count(const uint8_t *flags, size_t n, uint32_t *part_words, int32_t *count,
+                                 unsigned chunk, const Workspace &ws, cudaStream_t s)
+{
+    static std::atomic<unsigned long long> smem_set{0};
+    constexpr int kSmem = NSTG * SP * kPartElems;
+    auto kernel = compact_count_kernel<THREADS, SP, NSTG>;
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kernel), kSmem, smem_set);
+    if (e != cudaSuccess) return e;
+    const unsigned parts = static_cast<unsigned>((n + kPartElems - 1) / kPartElems);
+    const unsigned blocks = (parts + chunk - 1) / chunk;
+    uint32_t *mask = part_words, *cnt = part_words + static_cast<size_t>(parts) * 16, *off = cnt + parts;
+    kernel<<<blocks, THREADS, kSmem, s>>>(flags, n, parts, chunk, mask, cnt, off, ws.tile_sums,
+                                          ws.tile_sums + kMaxCountBlocks, count, ws.state);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_compact_two_pass(const uint32_t *in, const uint8_t *flags, uint32_t *out, int32_t *count,
                                     size_t n, bool out_aligned, uint32_t *part_words, const Workspace &ws,
-                                    unsigned spin_limit, cudaStream_t s)
+                                    cudaStream_t s)
 {
     const unsigned parts = static_cast<unsigned>((n + kPartElems - 1) / kPartElems);
-    uint32_t *mask = part_words, *cnt = part_words + static_cast<size_t>(parts) * 16, *off = cnt + parts;
-    // one block per SM, at least 32 parts (a part per warp) each
-    unsigned blocks = static_cast<unsigned>(ws.num_sms);
-    const unsigned need = (parts + 31) / 32;
-    if (blocks > need) blocks = need;
-    const unsigned chunk = (parts + blocks - 1) / blocks;
-    blocks = (parts + chunk - 1) / chunk;
-    uint32_t *sums = ws.tile_sums;
-    DevState *st = ws.state;
-    void *args[] = {const_cast<uint8_t **>(&flags), &n, const_cast<unsigned *>(&parts), const_cast<unsigned *>(&chunk),
-                    &mask, &cnt, &off, &sums, &count, &st, &spin_limit};
-    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(&compact_count_kernel), dim3(blocks),
-                                                dim3(kCountThreads), args, 0, s);
+    const unsigned chunk = count_chunk(parts, kCountThreads / 32, ws.num_sms);
+    cudaError_t e = launch_compact_count<kCountThreads, kCountStageParts, kCountStages>(flags, n, part_words, count,
+                                                                                        chunk, ws, s);
     if (e != cudaSuccess) return e;
+    const uint32_t *mask = part_words, *off = part_words + static_cast<size_t>(parts) * 17;
+    const uint32_t *carry = ws.tile_sums + kMaxCountBlocks;
     const unsigned wblocks = (parts + kWriteWarps - 1) / kWriteWarps;
-    if (out_aligned)
-        compact_write_kernel<true><<<wblocks, kWriteWarps * 32, 0, s>>>(in, out, n, parts, mask, cnt, off);
-    else
-        compact_write_kernel<false><<<wblocks, kWriteWarps * 32, 0, s>>>(in, out, n, parts, mask, cnt, off);
-    return cudaGetLastError();
+    return out_aligned ? launch_dependent(compact_write_kernel<true, kWriteMinBlocks>, wblocks, kWriteWarps * 32, s, in,
+                                          out, n, parts, chunk, mask, off, carry)
+                       : launch_dependent(compact_write_kernel<false, kWriteMinBlocks>, wblocks, kWriteWarps * 32, s,
+                                          in, out, n, parts, chunk, mask, off, carry);
 }
 
 // Ring depths measured on GB300 at 2^26: flags pass A (8 KB per tile) with
@@ -343,7 +333,7 @@ cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out
     const bool bulk_ok = (reinterpret_cast<uintptr_t>(in) % 16 == 0) && (reinterpret_cast<uintptr_t>(flags) % 16 == 0);
     if (bulk_ok && part_words != nullptr &&
         (carry == kCarryL2Resident || (carry == kCarryDefault && n >= kCompactTwoPassMinN)))
-        return launch_compact_two_pass(vin, flags, vout, count, n, out_aligned, part_words, ws, spin_limit, s);
+        return launch_compact_two_pass(vin, flags, vout, count, n, out_aligned, part_words, ws, s);
     const bool pipelined =
         bulk_ok && (carry == kCarryPipelined || (carry != kCarryLookback && n >= kCompactPipelineMinN));
     if (pipelined) {

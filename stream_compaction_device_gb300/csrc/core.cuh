@@ -103,7 +103,8 @@ struct DevState {
     unsigned ticket;
     unsigned error;
     unsigned cursor;
-    unsigned grid_arrive;   // blocks that reached the grid barrier (L2-resident scan)
+    unsigned grid_arrive;   // blocks that reached the grid barrier, or that handed in their totals
+                            // (the last one of those resets it)
     unsigned grid_depart;   // blocks that left it; the last one resets both
     unsigned pad[10];
     unsigned zeros[48];

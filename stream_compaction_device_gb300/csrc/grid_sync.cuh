@@ -1,11 +1,16 @@
-// Helpers of the cooperative launches (sm_103a): loads whose lines L2 keeps
-// for a second read, and a grid-wide barrier -- every block of the grid is
-// resident, so a counter in the stream's device state can gather them.  Used
-// by the kernels that fold their chunks, meet once, then finish with every
-// chunk's offset known.
+// Helpers of the kernels that fold their chunks, combine the chunk totals
+// once, then finish with every chunk's offset known (sm_103a): loads whose
+// lines L2 keeps for a second read, a block's stream of whole parts through a
+// ring of bulk-copied shared-memory stages, a block-wide exclusive scan, the
+// last-arriving block's scan of the block totals, a grid-wide barrier (every
+// block of a cooperative launch is resident, so a counter in the stream's
+// device state can gather them), and programmatic dependent launch.
 #pragma once
 
+#include <atomic>
+
 #include "core.cuh"
+#include "pipeline.cuh"
 
 namespace devscan {
 
@@ -32,6 +37,117 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
     asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+
+// The block streams parts [p0, p1) of `src` (PART_BYTES each, every one whole
+// and inside the buffer, `src` 16-byte aligned) through NSTG shared-memory
+// stages of SP parts: thread 0 issues one bulk copy per stage, warp w calls
+// fn(part, its bytes in shared memory) for the stage's parts w, w + warps, ...
+// and a stage is refilled once every warp is done with it, so NSTG - 1 copies
+// stay in flight while a stage is read.  `ring` holds NSTG * SP * PART_BYTES
+// bytes (16-byte aligned), `full` NSTG mbarriers.  Returns false when a wait
+// ran out; the copies still in flight have then been waited for.
+template <int PART_BYTES, int SP, int NSTG, typename Fn>
+__device__ bool stream_parts(const uint8_t *src, unsigned p0, unsigned p1, uint8_t *ring, uint64_t *full,
+                             unsigned wait_limit, Fn &&fn)
+{
+    static_assert(PART_BYTES % 16 == 0, "a bulk copy moves a multiple of 16 bytes");
+    const int tid = threadIdx.x, warp = tid >> 5, warps = blockDim.x >> 5;
+    const unsigned stages = p1 > p0 ? (p1 - p0 + SP - 1) / SP : 0u;
+    if (tid == 0) {
+        for (int s = 0; s < NSTG; ++s) mbar_init(&full[s], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    auto issue = [&](unsigned k) {
+        const unsigned a = p0 + k * SP, m = p1 - a < SP ? p1 - a : SP;
+        uint64_t *bar = &full[k % NSTG];
+        mbar_arrive_expect_tx(bar, m * PART_BYTES);
+        bulk_load(ring + static_cast<size_t>(k % NSTG) * SP * PART_BYTES, src + static_cast<size_t>(a) * PART_BYTES,
+                  m * PART_BYTES, bar);
+    };
+    if (tid == 0)
+        for (unsigned k = 0; k < NSTG && k < stages; ++k) issue(k);
+    unsigned k = 0;
+    bool ok = true;
+    for (; k < stages; ++k) {
+        const unsigned slot = k % NSTG;
+        const bool landed = mbar_wait(&full[slot], (k / NSTG) & 1u, wait_limit);
+        if (landed) {
+            const unsigned a = p0 + k * SP, m = p1 - a < SP ? p1 - a : SP;
+            const uint8_t *stage = ring + static_cast<size_t>(slot) * SP * PART_BYTES;
+            for (unsigned j = warp; j < m; j += warps) fn(a + j, stage + j * PART_BYTES);
+        }
+        if (!__syncthreads_and(landed)) {   // every thread takes the same branch
+            ok = false;
+            break;
+        }
+        if (tid == 0 && k + NSTG < stages) issue(k + NSTG);
+    }
+    if (!ok && tid == 0)   // stages k .. k + NSTG - 1 may still be landing
+        for (unsigned j = k; j < stages && j < k + NSTG; ++j) (void)mbar_wait(&full[j % NSTG], (j / NSTG) & 1u, wait_limit);
+    __syncthreads();
+    return ok;
+}
+
+// Exclusive add-scan of one value per thread over the block; `total` gets the
+// block's sum.  s_w holds THREADS / 32 words; the caller separates two calls
+// with a barrier.
+template <int THREADS>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *s_w, int tid, uint32_t &total)
+{
+    constexpr int NW = THREADS / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
+        if (lane >= d) inc += u;
+    }
+    if (lane == 31) s_w[warp] = inc;
+    __syncthreads();
+    uint32_t w = lane < NW ? s_w[lane] : 0u, wi = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_up_sync(kFullMask, wi, d);
+        if (lane >= d) wi += u;
+    }
+    total = __shfl_sync(kFullMask, wi, NW - 1);
+    return __shfl_sync(kFullMask, wi - w, warp) + inc - v;
+}
+
+// Every block of the grid calls this once with its total (block-uniform).
+// The last block to arrive writes carry[b] = totals of blocks 0 .. b-1 for
+// every block b, resets the arrival counter for the next launch on the
+// stream, and returns true with the grand total in `total`; the others
+// return false.  Needs gridDim.x <= THREADS; s_w as for block_excl_scan,
+// free on entry.
+template <int THREADS>
+__device__ bool last_block_carries(uint32_t block_total, uint32_t *block_sums, uint32_t *carry, DevState *st,
+                                   uint32_t *s_w, uint32_t &total)
+{
+    __shared__ int s_last;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        block_sums[blockIdx.x] = block_total;
+        __threadfence();   // the total before the arrival that counts it
+        s_last = atomicAdd(&st->grid_arrive, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last) return false;
+    __threadfence();
+    const uint32_t v = tid < static_cast<int>(gridDim.x) ? __ldcg(block_sums + tid) : 0u;
+    const uint32_t excl = block_excl_scan<THREADS>(v, s_w, tid, total);
+    if (tid < static_cast<int>(gridDim.x)) carry[tid] = excl;
+    if (tid == 0) st->grid_arrive = 0;
+    return true;
+}
+
+// Programmatic dependent launch: a grid launched after this one with
+// launch_dependent() may start once every block here has called
+// allow_dependent_launch() (or exited); it waits in wait_primary_grid() until
+// this grid has completed and its writes are visible.
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_primary_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // All `blocks` blocks meet here.  Returns false (and records a timeout) when
 // the wait runs out.
@@ -66,6 +182,42 @@ __device__ inline void grid_depart(DevState *st, unsigned blocks)
         st->grid_arrive = 0;
         st->grid_depart = 0;
     }
+}
+
+// Host side: raise `kernel`'s dynamic shared-memory limit to `bytes`, once
+// per device (`done` holds a bit per device).
+inline cudaError_t allow_dynamic_smem(const void *kernel, int bytes, std::atomic<unsigned long long> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if ((done.load() & bit) == 0) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        done.fetch_or(bit);
+    }
+    return cudaSuccess;
+}
+
+// Host side: launch `kernel` on `s` as a programmatic dependent of the grid
+// before it (see allow_dependent_launch); without a wait_primary_grid() call
+// first, the kernel must not read what that grid writes.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned threads, cudaStream_t s,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
 }  // namespace devscan

@@ -88,7 +88,7 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
 constexpr size_t kSplitTwoPassMinN = size_t(1) << 20;
 size_t split_part_words(size_t n);
 cudaError_t launch_split_two_pass(const uint32_t *keys, uint32_t *out, size_t n, int bit, unsigned *zeros,
-                                  uint32_t *part_words, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+                                  uint32_t *part_words, const Workspace &ws, cudaStream_t s);
 
 // One split pass by bit `bit` given the total zero count *zeros.  When
 // next_zeros is not null, the pass also adds the zero count of bit

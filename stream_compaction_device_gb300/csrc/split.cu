@@ -183,110 +183,85 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
 
 // ---------------------------------------------------------------------------
 // Two-launch split (a standalone split, which must count the zeros first
-// anyway): one cooperative launch counts the zeros of every 512-key part,
-// meets at a grid barrier and turns the counts into the parts' exclusive
-// offsets and the total Z; then a warp per part ranks its keys and writes its
-// zeros run at its offset and its ones run at Z + (keys before the part -
-// its offset).  The same bytes as the count pass plus the pipelined split
-// (12 per key), without a chain between tiles.
+// anyway): a block per SM streams its chunk of 512-key parts through shared
+// memory, counts every part's zeros and turns the counts into offsets within
+// the chunk; the last block to finish scans the chunk totals into chunk
+// carries and the total Z.  The write launch, a programmatic dependent of the
+// count (its keys load while the count ends), gives a warp per part: it ranks
+// its keys and writes its zeros run at its offset plus its chunk's carry and
+// its ones run at Z + (keys before the part - that offset).  The same bytes as
+// the count pass plus the pipelined split (12 per key), without a chain
+// between tiles.
 // ---------------------------------------------------------------------------
-constexpr int kSplitPart = 512, kSplitCountThreads = 1024, kSplitWriteWarps = 8, kSplitCountBatch = 2;
+constexpr int kSplitPart = 512, kSplitCountThreads = 512, kSplitStageParts = 32, kSplitStages = 3,
+              kSplitWriteWarps = 8;
+constexpr unsigned kSplitCountWaitLimit = 1u << 18;
+constexpr unsigned kSplitMaxCountBlocks = 512;   // chunk totals and carries share the workspace's tile sums
 
-// off[p]: zeros of bit `bit` in parts 0 .. p-1 (first the part's own count);
-// *zeros = all zeros.  Block b takes parts [b * chunk, (b + 1) * chunk).
-__global__ void __launch_bounds__(kSplitCountThreads, 1)
+// off[p]: zeros of bit `bit` in the parts before p in its chunk.  Block b
+// takes the chunk of parts [b * chunk, (b + 1) * chunk): its whole parts
+// stream through NSTG shared-memory stages of SP parts (dynamic shared
+// memory), the ragged last part of the input takes plain loads.  The last
+// block writes carry[b] = zeros in the chunks before b, and *zeros = all
+// zeros (block_sums: one word per block).
+template <int THREADS, int SP, int NSTG>
+__global__ void __launch_bounds__(THREADS, 1)
 split_count_kernel(const uint32_t *__restrict__ keys, size_t n, int bit, unsigned parts, unsigned chunk,
-                   uint32_t *__restrict__ off, uint32_t *__restrict__ block_sums, unsigned *__restrict__ zeros,
-                   DevState *st, unsigned spin_limit)
+                   uint32_t *__restrict__ off, uint32_t *__restrict__ block_sums, uint32_t *__restrict__ carry,
+                   unsigned *__restrict__ zeros, DevState *st)
 {
-    constexpr int NW = kSplitCountThreads / 32, B = kSplitCountBatch;
+    static_assert(THREADS >= static_cast<int>(kSplitMaxCountBlocks), "the last block scans one chunk total per thread");
+    constexpr int NW = THREADS / 32;
+    extern __shared__ __align__(128) uint8_t s_ring[];
+    __shared__ uint64_t s_full[NSTG];
     __shared__ uint32_t s_w[NW];
-    __shared__ uint32_t s_carry;
+    allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned p0 = blockIdx.x * chunk, p1 = p0 + chunk < parts ? p0 + chunk : parts;
-    // phase 1: warp w takes parts p0 + w, p0 + w + NW, ..., B at a time;
-    // lane L reads the part's 16-byte groups L, L + 32, L + 64, L + 96
-    uint32_t mine = 0;
-    for (unsigned pb = p0 + warp; pb < p1; pb += NW * B) {
-        uint4 q[B][4];
-#pragma unroll
-        for (int k = 0; k < B; ++k) {
-            const unsigned p = pb + k * NW;
-            if (p < p1 && static_cast<size_t>(p + 1) * kSplitPart <= n) {
-                const uint4 *k4 = reinterpret_cast<const uint4 *>(keys + static_cast<size_t>(p) * kSplitPart);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) q[k][g] = __ldcs(k4 + g * 32 + lane);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < B; ++k) {
-            const unsigned p = pb + k * NW;
-            if (p >= p1) break;   // warp-uniform
+    const unsigned whole = static_cast<unsigned>(n / kSplitPart);
+    const unsigned q1 = p1 < whole ? p1 : (p0 > whole ? p0 : whole);   // [p0, q1): whole parts
+    // phase 1: a part per warp; lane L reads the part's 16-byte groups L, L + 32, L + 64, L + 96
+    const bool streamed = stream_parts<kSplitPart * 4, SP, NSTG>(
+        reinterpret_cast<const uint8_t *>(keys), p0, q1, s_ring, s_full, kSplitCountWaitLimit,
+        [&](unsigned p, const uint8_t *part) {
+            const uint4 *k4 = reinterpret_cast<const uint4 *>(part);
             uint32_t z = 0;
-            if (static_cast<size_t>(p + 1) * kSplitPart <= n) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) z += zeros_of(q[k][g], bit);
-            } else {
-                const size_t e0 = static_cast<size_t>(p) * kSplitPart;
-                for (size_t e = e0 + lane; e < n && e < e0 + kSplitPart; e += 32) z += ((keys[e] >> bit) & 1u) ? 0u : 1u;
-            }
+            for (int g = 0; g < 4; ++g) z += zeros_of(k4[g * 32 + lane], bit);
             z = __reduce_add_sync(kFullMask, z);
             if (lane == 0) off[p] = z;
-            mine += z;
-        }
+        });
+    if (!streamed && tid == 0) atomicOr(&st->error, kErrTimeout);
+    for (unsigned p = q1 + warp; p < p1; p += NW) {   // the input's ragged last part
+        const size_t e0 = static_cast<size_t>(p) * kSplitPart;
+        uint32_t z = 0;
+        for (size_t e = e0 + lane; e < n && e < e0 + kSplitPart; e += 32) z += ((keys[e] >> bit) & 1u) ? 0u : 1u;
+        z = __reduce_add_sync(kFullMask, z);
+        if (lane == 0) off[p] = z;
     }
-    if (lane == 0) s_w[warp] = mine;
-    __syncthreads();
-    if (warp == 0) {
-        const uint32_t v = __reduce_add_sync(kFullMask, s_w[lane]);
-        if (lane == 0) block_sums[blockIdx.x] = v;
-    }
+    __syncthreads();   // every part's count written
 
-    const bool ok = grid_barrier(st, gridDim.x, spin_limit);
-
-    // phase 2: the counts become offsets in place, a block of parts at a time
-    if (warp == 0) {
-        uint32_t v = 0;
-        if (ok)
-            for (unsigned b = lane; b < blockIdx.x; b += 32) v += __ldcg(block_sums + b);
-        v = __reduce_add_sync(kFullMask, v);
-        if (lane == 0) s_carry = v;
-    }
-    __syncthreads();
-    uint32_t carry = s_carry;
-    for (unsigned base = p0; base < p1; base += kSplitCountThreads) {
+    // phase 2: the counts become offsets within the chunk, in place, THREADS parts at a time
+    uint32_t run = 0;
+    for (unsigned base = p0; base < p1; base += THREADS) {
         const unsigned p = base + tid;
         const uint32_t c = p < p1 ? off[p] : 0u;   // this thread's own part: read before it is overwritten
-        // exclusive scan over the block
-        uint32_t inc = c;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
-            if (lane >= d) inc += u;
-        }
-        if (lane == 31) s_w[warp] = inc;
-        __syncthreads();
-        uint32_t w = s_w[lane], wi = w;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t u = __shfl_up_sync(kFullMask, wi, d);
-            if (lane >= d) wi += u;
-        }
-        const uint32_t total = __shfl_sync(kFullMask, wi, NW - 1);
-        const uint32_t excl = __shfl_sync(kFullMask, wi - w, warp) + inc - c;
-        if (p < p1) off[p] = carry + excl;
-        carry += total;
+        uint32_t total;
+        const uint32_t excl = block_excl_scan<THREADS>(c, s_w, tid, total);
+        if (p < p1) off[p] = run + excl;
+        run += total;
         __syncthreads();   // s_w is read before the next round writes it
     }
-    if (blockIdx.x == gridDim.x - 1 && tid == 0) *zeros = carry;
-    grid_depart(st, gridDim.x);
+    uint32_t all;
+    if (last_block_carries<THREADS>(run, block_sums, carry, st, s_w, all) && tid == 0) *zeros = all;
 }
 
 // Warp w of block b splits part b * kSplitWriteWarps + w.
 template <bool OUT_ALIGNED>
 __global__ void __launch_bounds__(kSplitWriteWarps * 32)
 split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size_t n, int bit, unsigned parts,
-                   const uint32_t *__restrict__ off, const unsigned *__restrict__ zeros)
+                   unsigned chunk, const uint32_t *__restrict__ off, const uint32_t *__restrict__ carry,
+                   const unsigned *__restrict__ zeros)
 {
     constexpr int kStage = kSplitPart + 12;   // the zeros, the ones from the next 16-byte boundary, a spare chunk
     __shared__ __align__(16) uint32_t s_stage[kSplitWriteWarps][kStage];
@@ -323,35 +298,57 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
             zmask[q] = m;
         }
     }
-    const size_t zeros_at = off[p];
+    wait_primary_grid();   // the count launch's offsets, carries and Z (the keys need no wait)
+    const size_t zeros_at = static_cast<size_t>(off[p]) + carry[p / chunk];
     const size_t ones_at = static_cast<size_t>(*zeros) + (b - zeros_at);
     split_write_warp<4>(x, zmask, part_len, zeros_at, ones_at, lane, s_stage[warp], out, OUT_ALIGNED, n);
 }
 
 size_t split_part_words(size_t n) { return (n + kSplitPart - 1) / kSplitPart; }
 
+// The count launch: THREADS per block, NSTG * SP * 2048 bytes of stages;
+// `chunk` parts per block.  The workspace's tile sums hold the chunk totals
+// (first kSplitMaxCountBlocks words) and carries (next).
+template <int THREADS, int SP, int NSTG>
+cudaError_t launch_split_count(const uint32_t *keys, size_t n, int bit, uint32_t *off, unsigned *zeros, unsigned chunk,
+                               const Workspace &ws, cudaStream_t s)
+{
+    static std::atomic<unsigned long long> smem_set{0};
+    constexpr int kSmem = NSTG * SP * kSplitPart * 4;
+    auto kernel = split_count_kernel<THREADS, SP, NSTG>;
+    cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kernel), kSmem, smem_set);
+    if (e != cudaSuccess) return e;
+    const unsigned parts = static_cast<unsigned>(split_part_words(n));
+    const unsigned blocks = (parts + chunk - 1) / chunk;
+    kernel<<<blocks, THREADS, kSmem, s>>>(keys, n, bit, parts, chunk, off, ws.tile_sums,
+                                          ws.tile_sums + kSplitMaxCountBlocks, zeros, ws.state);
+    return cudaGetLastError();
+}
+
+// Parts per chunk: one chunk per SM (fewer for small inputs, at least a part
+// per warp each), at most kSplitMaxCountBlocks chunks.
+unsigned split_count_chunk(unsigned parts, unsigned warps, int num_sms)
+{
+    unsigned blocks = std::min<unsigned>(static_cast<unsigned>(num_sms), kSplitMaxCountBlocks);
+    blocks = std::min(blocks, (parts + warps - 1) / warps);
+    return (parts + blocks - 1) / blocks;
+}
+
 cudaError_t launch_split_two_pass(const uint32_t *keys, uint32_t *out, size_t n, int bit, unsigned *zeros,
-                                  uint32_t *part_words, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+                                  uint32_t *part_words, const Workspace &ws, cudaStream_t s)
 {
     const unsigned parts = static_cast<unsigned>(split_part_words(n));
-    unsigned blocks = static_cast<unsigned>(ws.num_sms);
-    const unsigned need = (parts + 31) / 32;
-    if (blocks > need) blocks = need;
-    const unsigned chunk = (parts + blocks - 1) / blocks;
-    blocks = (parts + chunk - 1) / chunk;
-    uint32_t *sums = ws.tile_sums;
-    DevState *st = ws.state;
-    void *args[] = {const_cast<uint32_t **>(&keys), &n, &bit, const_cast<unsigned *>(&parts),
-                    const_cast<unsigned *>(&chunk), &part_words, &sums, &zeros, &st, &spin_limit};
-    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(&split_count_kernel), dim3(blocks),
-                                                dim3(kSplitCountThreads), args, 0, s);
+    const unsigned chunk = split_count_chunk(parts, kSplitCountThreads / 32, ws.num_sms);
+    cudaError_t e = launch_split_count<kSplitCountThreads, kSplitStageParts, kSplitStages>(keys, n, bit, part_words,
+                                                                                          zeros, chunk, ws, s);
     if (e != cudaSuccess) return e;
+    const uint32_t *carry = ws.tile_sums + kSplitMaxCountBlocks;
     const unsigned wblocks = (parts + kSplitWriteWarps - 1) / kSplitWriteWarps;
-    if (reinterpret_cast<uintptr_t>(out) % 16 == 0)
-        split_write_kernel<true><<<wblocks, kSplitWriteWarps * 32, 0, s>>>(keys, out, n, bit, parts, part_words, zeros);
-    else
-        split_write_kernel<false><<<wblocks, kSplitWriteWarps * 32, 0, s>>>(keys, out, n, bit, parts, part_words, zeros);
-    return cudaGetLastError();
+    return reinterpret_cast<uintptr_t>(out) % 16 == 0
+               ? launch_dependent(split_write_kernel<true>, wblocks, kSplitWriteWarps * 32, s, keys, out, n, bit, parts,
+                                  chunk, part_words, carry, zeros)
+               : launch_dependent(split_write_kernel<false>, wblocks, kSplitWriteWarps * 32, s, keys, out, n, bit,
+                                  parts, chunk, part_words, carry, zeros);
 }
 
 cudaError_t launch_split(const uint32_t *keys, uint32_t *out, size_t n, int bit, const unsigned *zeros,
