@@ -105,6 +105,14 @@ cudaError_t launch_compact_gt(const int32_t *in, int32_t threshold, int32_t *out
 cudaError_t launch_bracket(const int32_t *in, int32_t *out, int32_t *result, size_t n, int carry,
                            const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
+// Scan of at most kClusterMaxN elements by one thread-block cluster (8
+// blocks of 8,192 elements at most), combining the block totals through
+// distributed shared memory; any 4-byte alignment.  The default below
+// kClusterMaxN + 1 elements.
+constexpr size_t kClusterMaxN = size_t(1) << 16;
+cudaError_t launch_scan_cluster(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
+                                bool aligned, cudaStream_t s);
+
 // Scan of an input that fits in L2: one cooperative launch, one block per SM
 // (16-byte-aligned in/out).
 cudaError_t launch_scan_l2_resident(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,

@@ -260,6 +260,9 @@ cudaError_t dispatch_dir(const void *in, void *out, size_t n, bool inclusive, bo
 cudaError_t launch_scan(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
                         bool aligned, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
 {
+    // small inputs: one thread-block cluster (scan_cluster.cu)
+    if (carry == kCarryDefault && n <= kClusterMaxN)
+        return launch_scan_cluster(type, op, inclusive, in, out, n, aligned, s);
     // inputs that fit in L2: one cooperative launch (scan_l2res.cu)
     if (aligned && (carry == kCarryL2Resident ||
                     (carry == kCarryDefault && n >= kL2ResidentMinN && n <= kL2ResidentMaxN)))

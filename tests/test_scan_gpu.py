@@ -82,7 +82,7 @@ def test_in_place(ds, inclusive):
 def test_unaligned_pointers(ds, offset):
     """in/out 4-byte but not 16-byte aligned take the scalar path."""
     from stream_compaction_device_gb300 import workloads as wl
-    for n in (1, 33, TILE + 7, 100_003):
+    for n in (1, 33, TILE + 7, 60_001, 100_003):
         check(ds, wl.random_input(np.int32, n, n, "add"), "add", False, offset=offset)
         check(ds, wl.random_input(np.uint32, n, n, "max"), "max", True, offset=offset)
         check(ds, wl.random_input(np.float32, n, n, "add"), "add", True, offset=offset)
@@ -109,10 +109,12 @@ def test_carry_modes(ds, mode):
 
 
 def test_default_size_boundaries(ds):
-    """Sizes around the default's switches between the one-tile kernel, the
-    L2-resident scan and the pipeline (2^17 and 2^24), ragged chunks included."""
+    """Sizes around the default's switches between the cluster scan, the
+    one-tile kernel, the L2-resident scan and the pipeline (2^16, 2^17 and
+    2^24), ragged blocks and chunks included."""
     from stream_compaction_device_gb300 import workloads as wl
-    for n in ((1 << 17) - 1, 1 << 17, (1 << 17) + 4097, 3 * (1 << 20) + 1, (1 << 24) - 3, 1 << 24, (1 << 24) + 1):
+    for n in (8191, 8192, 8193, 7 * 8192 + 1, (1 << 16) - 1, 1 << 16, (1 << 16) + 1,
+              (1 << 17) - 1, 1 << 17, (1 << 17) + 4097, 3 * (1 << 20) + 1, (1 << 24) - 3, 1 << 24, (1 << 24) + 1):
         check(ds, wl.random_input(np.int32, n, n, "add"), "add", False)
         check(ds, wl.random_input(np.float32, n, n + 1, "add"), "add", True)
         check(ds, wl.random_input(np.uint32, n, n + 2, "max"), "max", False)
