@@ -239,3 +239,39 @@ def test_config_sort_digits(ds):
     k = wl.radix_keys()
     assert np.array_equal(gpu_sort_digits(ds, k), np.sort(k))
     assert ds.device_status() == 0
+
+
+def test_mixed_calls_one_stream(ds):
+    """The two-launch compaction and split, the L2-resident scan and the
+    read-only bracket check share one arrival counter in the stream's device
+    state (last-block carries and grid barriers); interleaved on one stream,
+    every call still gives the oracle's result."""
+    from stream_compaction_device_gb300 import workloads as wl
+    rng = np.random.default_rng(77)
+    nc, n = (1 << 23) + 5, (1 << 21) + 5
+    v = rng.integers(-2**31, 2**31, nc, dtype=np.int32)
+    f = (rng.random(nc) < 0.3).astype(np.uint8)
+    k = rng.integers(0, 2**32, n, dtype=np.uint32)
+    x = wl.random_input(np.int32, n, 4, "add")
+    w = (2 * rng.integers(0, 2, n) - 1).astype(np.int32)
+    ref_c, ref_s, ref_x = oracle.compact(v, f), oracle.split_bit(k, 7)[0], oracle.scan(x, "add", False)
+    ref_w = oracle.scan(w, "add", True)
+    ref_neg, ref_final = int(ref_w.min() < 0), int(ref_w[-1])
+    dv, df, dk, dx, dw = to_dev(v), torch.from_numpy(f).cuda(), to_dev(k), to_dev(x), to_dev(w)
+    out = torch.empty_like(dv)
+    cnt = torch.empty(1, dtype=torch.int32, device="cuda")
+    so, xo = torch.empty_like(dk), torch.empty_like(dx)
+    res = torch.empty(2, dtype=torch.int32, device="cuda")
+    for _ in range(4):
+        ds.compact(dv, df, out=out, count=cnt)
+        ds.split_bit(dk, 7, out=so)
+        ds.scan_exclusive(dx, xo)
+        ds.bracket_scan(dw, result=res, store=False)
+        ds.compact(dv, df, out=out, count=cnt)
+        torch.cuda.synchronize()
+        kk = int(cnt.item())
+        assert kk == ref_c.size and np.array_equal(out[:kk].cpu().numpy(), ref_c)
+        assert np.array_equal(from_dev(so, np.uint32), ref_s)
+        assert np.array_equal(xo.cpu().numpy(), ref_x)
+        assert res.cpu().tolist() == [ref_neg, ref_final]
+    assert ds.device_status() == 0
