@@ -218,8 +218,10 @@ devscan_status devscan_stream_release(cudaStream_t stream);
 /* Inter-block carry strategy for the scans (P1 section 四 describes the
  * three-phase "reduce, scan the block totals, add the offsets" scheme and
  * mentions chaining blocks inside one launch):
- *   0 = default: for 16-byte-aligned in/out the scans take 4 for
- *       2^17 <= n <= 2^24 and 3 above; compaction with flags takes 3 from
+ *   0 = default: scans of n <= 2^16 run in one thread-block cluster (up
+ *       to 8 blocks exchanging their totals through distributed shared
+ *       memory, any alignment); for 16-byte-aligned in/out the scans take 4
+ *       for 2^17 <= n <= 2^24 and 3 above; compaction with flags takes 3 from
  *       n = 2^19 and 4 from 2^23; split_bit_u32 takes 4 from 2^20; the
  *       sorts' splits, the bracket scan and the segmented scan take 3 from
  *       n = 2^19; the bracket check without the scanned array (out == NULL)
@@ -236,8 +238,8 @@ devscan_status devscan_stream_release(cudaStream_t stream);
  *       bracket scan with its array stored use 3); the bracket check alone
  *       takes its one-read cooperative kernel at every size below 2^31, and
  *       compaction with flags and split_bit_u32 their two-launch paths (a
- *       cooperative count and scan of 512-element parts, then a warp per
- *       part writing its runs).
+ *       count of 512-element parts with offsets per chunk of parts and
+ *       carries between chunks, then a warp per part writing its runs).
  * Compaction and the split follow the same choice between 1 and 3 (their
  * pipelined kernels need 16-byte-aligned inputs, and flags too for
  * compaction).  Process-wide; meant for measurement.  Returns
