@@ -336,9 +336,16 @@ devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStrea
     devscan_status st = acquire(stream, tiles, &ws);
     if (st != DEVSCAN_OK) return st;
     unsigned *z = ws.state->zeros;   // z[b] = zero count of bit b
+    const int carry = g_carry_mode.load(std::memory_order_relaxed);
+    if (reinterpret_cast<uintptr_t>(keys) % 16 == 0 && reinterpret_cast<uintptr_t>(tmp) % 16 == 0 &&
+        (carry == kCarryL2Resident || (carry == kCarryDefault && n >= kSortTwoPassMinN))) {
+        void *part_words = nullptr;   // the parts' offsets, then the next pass's part counts
+        st = acquire_extra(stream, sort_part_words(n) * sizeof(uint32_t), &part_words);
+        if (st != DEVSCAN_OK) return st;
+        return from_cuda(launch_sort_two_pass(keys, tmp, n, &z[40], static_cast<uint32_t *>(part_words), ws, stream));
+    }
     if (cudaMemsetAsync(z, 0, 33 * sizeof(unsigned), stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
     if (launch_count_zeros(keys, n, 0, &z[0], ws, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
-    const int carry = g_carry_mode.load(std::memory_order_relaxed);
     uint32_t *src = keys, *dst = tmp;
     for (int bit = 0; bit < 32; ++bit) {
         unsigned *next = (bit < 31) ? &z[bit + 1] : nullptr;

@@ -90,6 +90,19 @@ size_t split_part_words(size_t n);
 cudaError_t launch_split_two_pass(const uint32_t *keys, uint32_t *out, size_t n, int bit, unsigned *zeros,
                                   uint32_t *part_words, const Workspace &ws, cudaStream_t s);
 
+// The 32-pass LSD sort from the two-launch split: one zero count of bit 0,
+// then per bit a write launch that also counts the next bit's zeros per
+// 512-key part of its output (at most four global atomics per part) and a
+// small launch turning those counts into the next pass's offsets.  Measured
+// on GB300 at 2^26 keys: 3.65 ms against 4.15 ms for the pipelined splits.  keys and
+// tmp 16-byte aligned; the sorted keys end in `keys`; part_words:
+// sort_part_words(n) words of per-stream scratch; *zeros: a device word.
+// Taken from kSortTwoPassMinN keys (default or carry mode 4).
+constexpr size_t kSortTwoPassMinN = size_t(1) << 20;
+size_t sort_part_words(size_t n);
+cudaError_t launch_sort_two_pass(uint32_t *keys, uint32_t *tmp, size_t n, unsigned *zeros, uint32_t *part_words,
+                                 const Workspace &ws, cudaStream_t s);
+
 // One split pass by bit `bit` given the total zero count *zeros.  When
 // next_zeros is not null, the pass also adds the zero count of bit
 // `bit + 1` into *next_zeros.

@@ -31,10 +31,14 @@ __device__ __forceinline__ unsigned zeros_of(uint4 q, int bit)
 // zeros_at % 4 and the ones from the next 16-byte boundary after them (plus
 // ones_at % 4) in its private `stage` area (kWarpItems + 12 words), and
 // writes both runs out in whole 128-bit chunks where they line up.
-template <int VECS>
+// COUNT_NEXT: the writes also count the keys whose bit next_bit is 0 by the
+// 512-position output part they land in, and add those counts to
+// next_cnt[part] (at most four atomics per part).
+template <int VECS, bool COUNT_NEXT = false>
 __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], const uint32_t (&zmask)[VECS],
                                                  unsigned part_len, size_t zeros_at, size_t ones_at, int lane,
-                                                 uint32_t *stage, uint32_t *out, bool out_aligned, size_t n)
+                                                 uint32_t *stage, uint32_t *out, bool out_aligned, size_t n,
+                                                 int next_bit = 0, uint32_t *next_cnt = nullptr)
 {
     static_assert(VECS == 4, "the four rows' counts share one word");
     uint32_t packed = 0;
@@ -71,7 +75,27 @@ __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], c
         row_base += (tot >> (8 * q)) & 0xffu;
     }
     __syncwarp();
-    if (out_aligned) {
+    if (COUNT_NEXT) {
+        // also count bit next_bit's zeros by the output part they land in
+        uint32_t c[4] = {0u, 0u, 0u, 0u};
+        if (out_aligned) {
+            write_run_direct_count<32>(out, zeros_at, zeros, stage, lane, n, next_bit, c[0], c[1]);
+            write_run_direct_count<32>(out, ones_at, part_len - zeros, stage + o_base, lane, n, next_bit, c[2], c[3]);
+        } else {
+            write_run_scalar_count<32>(out, zeros_at, zeros, stage, 0, lane, n, next_bit, c[0], c[1]);
+            write_run_scalar_count<32>(out, ones_at, part_len - zeros, stage, static_cast<int>(zeros), lane, n,
+                                       next_bit, c[2], c[3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = __reduce_add_sync(kFullMask, c[i]);
+        if (lane == 0) {
+            const size_t zp = zeros_at >> 9, op = ones_at >> 9;
+            if (c[0] != 0) atomicAdd(next_cnt + zp, c[0]);
+            if (c[1] != 0) atomicAdd(next_cnt + zp + 1, c[1]);
+            if (c[2] != 0) atomicAdd(next_cnt + op, c[2]);
+            if (c[3] != 0) atomicAdd(next_cnt + op + 1, c[3]);
+        }
+    } else if (out_aligned) {
         write_run_direct<32>(out, zeros_at, zeros, stage, lane, n);
         write_run_direct<32>(out, ones_at, part_len - zeros, stage + o_base, lane, n);
     } else {

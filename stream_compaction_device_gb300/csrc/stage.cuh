@@ -124,4 +124,71 @@ __device__ __forceinline__ void write_run_direct(uint32_t *__restrict__ out, siz
     }
 }
 
+// write_run_direct that also counts the run's keys whose bit `nb` is 0, by
+// the 512-position output part they land in: c0 for the part of out[g0],
+// c1 for the next one (a run of at most 512 keys spans two parts at most).
+// A 16-byte chunk of out never straddles two parts, so each chunk adds its
+// count to one of the two.
+template <int THREADS>
+__device__ __forceinline__ void write_run_direct_count(uint32_t *__restrict__ out, size_t g0, unsigned cnt,
+                                                       const uint32_t *stage, int tid, size_t limit, int nb,
+                                                       uint32_t &c0, uint32_t &c1)
+{
+    if (cnt == 0 || g0 >= limit) return;
+    const unsigned a = static_cast<unsigned>(g0 & 3);
+    const unsigned end = a + cnt;
+    const unsigned chunks = (end + 3) >> 2;
+    uint4 *dst = reinterpret_cast<uint4 *>(out) + (g0 >> 2);
+    const uint4 *src = reinterpret_cast<const uint4 *>(stage);
+    const size_t room = limit - (g0 - a);
+    const size_t first_part = g0 >> 9;
+    for (unsigned k = tid; k < chunks; k += THREADS) {
+        const uint4 v = src[k];
+        const unsigned w0 = 4 * k;
+        const uint32_t zero4 = (((v.x >> nb) & 1u) | (((v.y >> nb) & 1u) << 1) | (((v.z >> nb) & 1u) << 2) |
+                                (((v.w >> nb) & 1u) << 3)) ^ 0xfu;
+        uint32_t valid;
+        if (w0 >= a && w0 + 4 <= end && w0 + 4 <= room) {
+            st_stream(dst + k, v);
+            valid = 0xfu;
+        } else {
+            uint32_t *o = reinterpret_cast<uint32_t *>(dst + k);
+            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+            valid = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const unsigned w = w0 + j;
+                if (w >= a && w < end && w < room) {
+                    o[j] = vv[j];
+                    valid |= 1u << j;
+                }
+            }
+        }
+        const uint32_t z = static_cast<uint32_t>(__popc(zero4 & valid));
+        if (((g0 - a + w0) >> 9) == first_part)
+            c0 += z;
+        else
+            c1 += z;
+    }
+}
+
+// write_run_scalar with the same count as write_run_direct_count.
+template <int THREADS>
+__device__ __forceinline__ void write_run_scalar_count(uint32_t *__restrict__ out, size_t g0, unsigned cnt,
+                                                       const uint32_t *stage, int s0, int tid, size_t limit, int nb,
+                                                       uint32_t &c0, uint32_t &c1)
+{
+    const size_t first_part = g0 >> 9;
+    for (unsigned e = tid; e < cnt; e += THREADS) {
+        if (g0 + e >= limit) continue;
+        const uint32_t k = stage[s0 + static_cast<int>(e)];
+        out[g0 + e] = k;
+        const uint32_t z = ((k >> nb) & 1u) ^ 1u;
+        if (((g0 + e) >> 9) == first_part)
+            c0 += z;
+        else
+            c1 += z;
+    }
+}
+
 }  // namespace devscan
