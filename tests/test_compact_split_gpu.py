@@ -275,3 +275,20 @@ def test_mixed_calls_one_stream(ds):
         assert np.array_equal(xo.cpu().numpy(), ref_x)
         assert res.cpu().tolist() == [ref_neg, ref_final]
     assert ds.device_status() == 0
+
+
+def test_default_two_launch_boundaries(ds):
+    """Around the default's switch to the two-launch split and sort (2^20
+    keys) and to the two-launch compaction (2^23 elements), aligned and not."""
+    ds.set_carry_mode("default")
+    rng = np.random.default_rng(8)
+    for n in ((1 << 20) - 1, 1 << 20, (1 << 20) + 3):
+        k = rng.integers(0, 2**32, n, dtype=np.uint32)
+        assert np.array_equal(gpu_split(ds, k, 23), oracle.split_bit(k, 23)[0]), n
+        assert np.array_equal(gpu_split(ds, k, 0, koff=1, ooff=2), oracle.split_bit(k, 0)[0]), n
+        assert np.array_equal(gpu_sort(ds, k), np.sort(k)), n
+    for n in ((1 << 23) - 1, (1 << 23) + 1):
+        v = rng.integers(-2**31, 2**31, n, dtype=np.int32)
+        f = (rng.random(n) < 0.05).astype(np.uint8)
+        check_compact(ds, v, f)
+        check_compact(ds, v, f, ooff=1)
