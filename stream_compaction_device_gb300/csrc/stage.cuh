@@ -102,15 +102,16 @@ __device__ __forceinline__ void write_run_direct(uint32_t *__restrict__ out, siz
 {
     if (cnt == 0 || g0 >= limit) return;   // (a start past the end only follows a timed-out wait)
     const unsigned a = static_cast<unsigned>(g0 & 3);
-    const unsigned end = a + cnt;   // run occupies words [a, end) of the staged chunks
-    const unsigned chunks = (end + 3) >> 2;
+    const size_t room = limit - (g0 - a);   // words of out from the first chunk's start
+    const unsigned end = a + cnt;
+    const unsigned stop = room < end ? static_cast<unsigned>(room) : end;   // words [a, stop) are written
+    const unsigned chunks = (stop + 3) >> 2;
     uint4 *dst = reinterpret_cast<uint4 *>(out) + (g0 >> 2);
     const uint4 *src = reinterpret_cast<const uint4 *>(stage);
-    const size_t room = limit - (g0 - a);   // words of out from the first chunk's start
     for (unsigned k = tid; k < chunks; k += THREADS) {
         const uint4 v = src[k];
         const unsigned w0 = 4 * k;
-        if (w0 >= a && w0 + 4 <= end && w0 + 4 <= room) {
+        if (w0 >= a && w0 + 4 <= stop) {
             st_stream(dst + k, v);
         } else {
             uint32_t *o = reinterpret_cast<uint32_t *>(dst + k);
@@ -118,7 +119,7 @@ __device__ __forceinline__ void write_run_direct(uint32_t *__restrict__ out, siz
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const unsigned w = w0 + j;
-                if (w >= a && w < end && w < room) o[j] = vv[j];
+                if (w >= a && w < stop) o[j] = vv[j];
             }
         }
     }
@@ -136,36 +137,35 @@ __device__ __forceinline__ void write_run_direct_count(uint32_t *__restrict__ ou
 {
     if (cnt == 0 || g0 >= limit) return;
     const unsigned a = static_cast<unsigned>(g0 & 3);
+    const size_t room = limit - (g0 - a);
     const unsigned end = a + cnt;
-    const unsigned chunks = (end + 3) >> 2;
+    const unsigned stop = room < end ? static_cast<unsigned>(room) : end;
+    const unsigned chunks = (stop + 3) >> 2;
+    // staged word w lands at g0 - a + w: the next part starts at word `next`
+    const unsigned next = 512u - static_cast<unsigned>((g0 - a) & 511u);
     uint4 *dst = reinterpret_cast<uint4 *>(out) + (g0 >> 2);
     const uint4 *src = reinterpret_cast<const uint4 *>(stage);
-    const size_t room = limit - (g0 - a);
-    const size_t first_part = g0 >> 9;
     for (unsigned k = tid; k < chunks; k += THREADS) {
         const uint4 v = src[k];
         const unsigned w0 = 4 * k;
-        const uint32_t zero4 = (((v.x >> nb) & 1u) | (((v.y >> nb) & 1u) << 1) | (((v.z >> nb) & 1u) << 2) |
-                                (((v.w >> nb) & 1u) << 3)) ^ 0xfu;
-        uint32_t valid;
-        if (w0 >= a && w0 + 4 <= end && w0 + 4 <= room) {
+        uint32_t z;
+        if (w0 >= a && w0 + 4 <= stop) {
             st_stream(dst + k, v);
-            valid = 0xfu;
+            z = 4u - (((v.x >> nb) & 1u) + ((v.y >> nb) & 1u) + ((v.z >> nb) & 1u) + ((v.w >> nb) & 1u));
         } else {
             uint32_t *o = reinterpret_cast<uint32_t *>(dst + k);
             const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-            valid = 0;
+            z = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const unsigned w = w0 + j;
-                if (w >= a && w < end && w < room) {
+                if (w >= a && w < stop) {
                     o[j] = vv[j];
-                    valid |= 1u << j;
+                    z += ((vv[j] >> nb) & 1u) ^ 1u;
                 }
             }
         }
-        const uint32_t z = static_cast<uint32_t>(__popc(zero4 & valid));
-        if (((g0 - a + w0) >> 9) == first_part)
+        if (w0 < next)
             c0 += z;
         else
             c1 += z;
