@@ -8,7 +8,7 @@
 // counts (small inputs); the persistent two-pass pipeline (pipeline_l2.cuh
 // with CompactPolicy) where the predicate scan, the carry, the staged scatter
 // and the count happen in one launch; and, for large inputs with flags, two
-// launches -- a cooperative count and scan of 512-element parts, then a warp
+// launches -- a count of 512-element parts with their offsets, then a warp
 // per part writing its run -- which no tile chain slows down.
 #include <atomic>
 

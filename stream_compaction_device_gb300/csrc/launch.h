@@ -65,8 +65,9 @@ cudaError_t launch_stalled_wait(const Workspace &ws, unsigned spin_limit, cudaSt
 // part_words: compact_part_words(n) words of per-stream scratch for the
 // two-launch path (taken, for 16-byte-aligned values and flags, from
 // kCompactTwoPassMinN elements and in carry mode 4), or null.  Measured on
-// GB300: it beats the pipeline from 2^24 (1% kept: 59 against 75 us at 2^26;
-// 50% and 99%: level or ahead) and loses below 2^23 to its second launch.
+// GB300: it beats the pipeline from 2^23 (at 2^26: 54 against 74 us at 1%
+// kept, 82 against 85 at 50%, 103 against 106 at 99%) and loses below to its
+// second launch.
 constexpr size_t kCompactTwoPassMinN = size_t(1) << 23;
 size_t compact_part_words(size_t n);
 cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out, int32_t *count, size_t n,
@@ -83,7 +84,7 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
 // part_words: split_part_words(n) words of per-stream scratch.  Taken for
 // 16-byte-aligned keys from kSplitTwoPassMinN keys and in carry mode 4;
 // measured on GB300 it beats the count pass plus the pipelined split at every
-// size from 2^20 (138 against 170 us at 2^26).  A sort's passes keep the
+// size from 2^20 (139 against 170 us at 2^26).  A sort's passes keep the
 // pipeline, which counts the next bit's zeros as it goes.
 constexpr size_t kSplitTwoPassMinN = size_t(1) << 20;
 size_t split_part_words(size_t n);
