@@ -125,6 +125,11 @@ devscan_status segmented_scan_exclusive_f32(const float *in, const uint8_t *head
  *   count  : device int32, written with the number kept (0 when n == 0).
  *   n      : at most INT32_MAX, else DEVSCAN_ERR_INVALID.
  *   out must not overlap in or flags (DEVSCAN_ERR_INVALID).
+ * From 2^23 elements (in and flags 16-byte aligned) it runs in two launches:
+ * a count of every 512-element part (keep mask, count, offset), then a warp
+ * per part writing its kept values; 18 words per 512 elements of per-stream
+ * scratch are allocated stream-ordered on first use (DEVSCAN_ERR_NOMEM if
+ * that fails).  Smaller or unaligned inputs take a single-pass kernel.
  * ------------------------------------------------------------------------- */
 devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out,
                            int32_t *count, size_t n, cudaStream_t stream);
@@ -168,16 +173,25 @@ devscan_status bracket_scan_i32(const int32_t *in, int32_t *out, int32_t *result
  *   keys, out : device uint32[n], not overlapping (DEVSCAN_ERR_INVALID);
  *   bit       : 0..31, else DEVSCAN_ERR_INVALID;
  *   n         : at most INT32_MAX, else DEVSCAN_ERR_INVALID.
- * Runs a zero-count pass, then the single-pass split.
+ * From 2^20 keys (keys 16-byte aligned): a launch counting every 512-key
+ * part's zeros into part offsets and Z, then a warp per part writing its two
+ * runs; one word per 512 keys of per-stream scratch is allocated
+ * stream-ordered on first use (DEVSCAN_ERR_NOMEM if that fails).  Below, a
+ * zero-count pass, then the single-pass split.
  * ------------------------------------------------------------------------- */
 devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_t n,
                              cudaStream_t stream);
 
 /* Least-significant-bit-first radix sort of uint32 keys by 32 one-bit splits
- * (P1 section 一: one bit per round; each round's core is a scan).  The zero
- * count of each bit is the same in every pass (a permutation keeps it), so
- * pass b counts the zeros of bit b+1 while it scatters and one count pass
- * runs before pass 0.
+ * (P1 section 一: one bit per round; each round's core is a scan).  Pass b
+ * counts the zeros of bit b+1 while it scatters, and one count pass runs
+ * before pass 0.  From 2^20 keys (keys and tmp 16-byte aligned) each pass
+ * is the two-launch split, whose write launch counts bit b+1's zeros per
+ * 512-key part of its output, plus a small launch turning those counts into
+ * the next pass's offsets; 2 words per 512 keys of per-stream scratch are
+ * allocated stream-ordered on first use (DEVSCAN_ERR_NOMEM if that fails).
+ * Otherwise each pass is the pipelined (or one-tile) split, which needs only
+ * the total zero count of bit b+1.
  *
  *   keys : device uint32[n]; sorted ascending in place on return (stream order);
  *   tmp  : device uint32[n] scratch owned by the caller, not overlapping keys;
