@@ -524,6 +524,12 @@ def run_op(args):
         keys = torch.from_numpy(wl.radix_keys(n).view(np.int32)).cuda()
         out = torch.empty_like(keys)
         fn = lambda: ds.split_bit(keys, 17, out)
+    elif args.op == "sort32":
+        keys = torch.from_numpy(wl.radix_keys(n).view(np.int32)).cuda()
+        work, tmp = torch.empty_like(keys), torch.empty_like(keys)
+        def fn():
+            work.copy_(keys)
+            ds.radix_sort(work, tmp)
     else:   # digit_sort
         keys = torch.from_numpy(wl.radix_keys(n).view(np.int32)).cuda()
         work, tmp = torch.empty_like(keys), torch.empty_like(keys)
@@ -557,7 +563,7 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
-    p.add_argument("--op", choices=["scan", "compact50", "segscan", "bracket_check", "split", "digit_sort"],
+    p.add_argument("--op", choices=["scan", "compact50", "segscan", "bracket_check", "split", "sort32", "digit_sort"],
                    default="scan", help="scan: the benchmark; the others run one call repeatedly for profiling")
     args = p.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":

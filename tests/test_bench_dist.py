@@ -56,7 +56,7 @@ def test_reference_arm_line(capsys):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("op", ["compact50", "segscan", "bracket_check", "split", "digit_sort"])
+@pytest.mark.parametrize("op", ["compact50", "segscan", "bracket_check", "split", "sort32", "digit_sort"])
 def test_single_op_mode(capsys, op):
     """``bench.py --op``: one library call repeated for a profiler, its own line."""
     import json
