@@ -270,6 +270,9 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
 {
     constexpr int kStage = kSplitPart + 12;   // the zeros, the ones from the next 16-byte boundary, a spare chunk
     __shared__ __align__(16) uint32_t s_stage[kSplitWriteWarps][kStage];
+    // a sort's next offsets launch may start once every block has begun: it
+    // waits for this grid to finish before it reads the counts
+    allow_dependent_launch();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned p = blockIdx.x * kSplitWriteWarps + warp;
     if (p >= parts) return;   // the whole warp: no barrier follows
@@ -323,6 +326,11 @@ part_offsets_kernel(uint32_t *__restrict__ cnt, unsigned parts, unsigned chunk, 
 {
     static_assert(THREADS >= static_cast<int>(kSplitMaxCountBlocks), "the last block scans one chunk total per thread");
     __shared__ uint32_t s_w[THREADS / 32];
+    // launched as a programmatic dependent of the previous pass's write
+    // launch: wait for its counts (and its keys) to be complete before this
+    // grid lets the next write launch start, as that one reads those keys
+    // before its own wait
+    wait_primary_grid();
     allow_dependent_launch();
     const int tid = threadIdx.x;
     const unsigned p0 = blockIdx.x * chunk, p1 = p0 + chunk < parts ? p0 + chunk : parts;
@@ -428,9 +436,8 @@ cudaError_t launch_sort_two_pass(uint32_t *keys, uint32_t *tmp, size_t n, unsign
         if (e != cudaSuccess) return e;
         if (bit < 31) {
             const unsigned blocks = (parts + chunk - 1) / chunk;
-            part_offsets_kernel<kSortOffsetThreads><<<blocks, kSortOffsetThreads, 0, s>>>(
-                cnt, parts, chunk, off, ws.tile_sums, ws.tile_sums + kSplitMaxCountBlocks, zeros, ws.state);
-            e = cudaGetLastError();
+            e = launch_dependent(part_offsets_kernel<kSortOffsetThreads>, blocks, kSortOffsetThreads, s, cnt, parts,
+                                 chunk, off, ws.tile_sums, ws.tile_sums + kSplitMaxCountBlocks, zeros, ws.state);
             if (e != cudaSuccess) return e;
         }
         src = dst;
