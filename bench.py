@@ -22,19 +22,17 @@ is needed between steps.  Prints one JSON line:
              events (device time per call), except the rows that flush L2
 
 ``--impl reference`` times the CPU oracle instead (the reference arm): each
-step is the oracle's serial exclusive scan of a 2^22-element sample of the
-same workload.  With ``--gpus N`` > 1 (launched by torchrun) every rank runs
+step is the oracle's serial exclusive scan of the same 2^28-element
+workload, on one host core.  With ``--gpus N`` > 1 (launched by torchrun) every rank runs
 an independent replica on its own GPU (the scan needs no exchange between
 replicas); ``scaling`` is "weak".
 """
 from __future__ import annotations
 
 import argparse
-import datetime as _dt
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -46,7 +44,6 @@ if ROOT not in sys.path:
 
 METRIC = "int32 exclusive scan Gelem/s & HBM GB/s (% peak) at N=2^28; compaction Gelem/s"
 N_HEADLINE = 1 << 28
-REF_SAMPLE = 1 << 22
 FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the pipelined
 # scan kernel at N = 2^28 (one-pass ncu capture of this benchmark's own
@@ -103,53 +100,104 @@ def barrier(world):
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
-class ClockSampler:
-    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+class _Nvml:
+    """The few NVML queries the clock record needs, through ctypes (the GPU
+    hosts have the driver's libnvidia-ml but not every Python wrapper).
+    Reads only: no setting of the GPU is changed."""
+    SM_CLOCK = 1   # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        uuid = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+        except Exception:
+            pass
+        rc = 1
+        if uuid:
+            rc = self.lib.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(self.dev))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.dev))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_mhz = self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.SM_CLOCK)
+
+    def _uint(self, fn, *args):
+        v = self.c.c_uint()
+        return v.value if fn(self.dev, *args, self.c.byref(v)) == 0 else None
+
+    def sample(self):
+        r = self.c.c_ulonglong()
+        reasons = r.value if self.reasons_fn(self.dev, self.c.byref(r)) == 0 else 0
+        mw = self._uint(self.lib.nvmlDeviceGetPowerUsage)
+        return (time.perf_counter(), self._uint(self.lib.nvmlDeviceGetClockInfo, self.SM_CLOCK), self.max_mhz,
+                None if mw is None else mw / 1e3, sorted(n for bit, n in self.REASONS.items() if reasons & bit))
+
+
+class ClockSampler:
+    """SM clock, power and throttle reasons sampled every ``period_s`` on a
+    background thread while the timed region runs (NVML through ctypes; the
+    bench's timed regions last milliseconds, below nvidia-smi's polling
+    interval).  ``stop`` summarises the samples taken between the marks t0
+    and t1; with none inside, ``sm_mhz`` is null and ``why_null`` says so."""
+
+    def __init__(self, gpu_index: int, period_s: float = 0.0005):
         self.gpu = gpu_index
-        self.proc = None
+        self.period = period_s
+        self.samples = []
         self.t0 = self.t1 = None
+        self.thread = None
+        self.error = None
 
     def start(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            time.sleep(0.6)
-        except OSError:
-            self.proc = None
+            self.nvml = _Nvml(self.gpu)
+        except (OSError, AttributeError) as e:
+            self.error = f"NVML unavailable: {e}"
+            return
+        self.halt = threading.Event()
+
+        def run():
+            while not self.halt.is_set():
+                self.samples.append(self.nvml.sample())
+                time.sleep(self.period)
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+        time.sleep(0.05)
 
     def mark(self, which):
-        setattr(self, which, _dt.datetime.now())
+        setattr(self, which, time.perf_counter())
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        time.sleep(0.25)
-        self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
-        rows = []
-        for line in out.splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
-            except ValueError:
-                continue
-            rows.append((ts, parts))
-        inside = [p for ts, p in rows if self.t0 and self.t1 and self.t0 <= ts <= self.t1]
-        use = inside if inside else [p for _, p in rows]
-        mhz = [float(p[2]) for p in use if p[2].replace(".", "").isdigit()]
-        mx = [float(p[3]) for p in use if p[3].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for p in use for i in range(4) if p[6 + i] == "Active"})
-        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
-                "power_w_max": max((float(p[4]) for p in use if p[4].replace(".", "").isdigit()), default=None)}
+        if self.thread is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "why_null": self.error or "sampler not started"}
+        self.halt.set()
+        self.thread.join(5)
+        inside = [s for s in self.samples if self.t0 is not None and self.t1 is not None and self.t0 <= s[0] <= self.t1]
+        out = {"samples": len(self.samples), "samples_in_timed_region": len(inside), "source": "nvml",
+               "period_ms": self.period * 1e3,
+               "timed_region_ms": None if self.t0 is None or self.t1 is None else round((self.t1 - self.t0) * 1e3, 3)}
+        if not inside:
+            out.update(sm_mhz=None, sm_max_mhz=self.nvml.max_mhz, reasons=[],
+                       why_null="no clock sample fell inside the timed region")
+            return out
+        mhz = [s[1] for s in inside if s[1] is not None]
+        out.update(sm_mhz=statistics.median(mhz) if mhz else None, sm_min_mhz=min(mhz) if mhz else None,
+                   sm_max_mhz=self.nvml.max_mhz, reasons=sorted({r for s in inside for r in s[4]}),
+                   power_w_max=max((s[3] for s in inside if s[3] is not None), default=None))
+        return out
 
 
 # ---------------------------------------------------------------------------
@@ -339,10 +387,14 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
     import torch
     out = {}
     reps = args.extra_reps
-    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    # L2 flush between calls of the rows that fit in L2: a read of 256 MiB (a
+    # sum into one scalar) replaces every line with a clean one, so no
+    # write-back of dirty lines lands inside the next timed call
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    flush_acc = torch.empty((), dtype=torch.float32, device="cuda")
 
     def flush():
-        flush_buf.zero_()
+        torch.sum(flush_buf, dim=0, out=flush_acc)
 
     def row(n_elems, ms, nbytes):
         gbs = nbytes / (ms / 1e3) / 1e9
@@ -469,16 +521,16 @@ def run_reference(args):
     import oracle
     from stream_compaction_device_gb300 import workloads as wl
     n = args.n
-    x = wl.brackets(n)[:REF_SAMPLE].copy()
+    x = wl.brackets(n)
     for _ in range(args.warmup):
         oracle.scan(x, "add", False)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle.scan(x, "add", False)
     el = time.perf_counter() - t0
-    value = REF_SAMPLE * args.steps / el / 1e9
-    sample = (f"serial oracle exclusive add-scan of the first 2^22 elements of the 2^{n.bit_length() - 1}"
-              f"-element workload per step, {args.steps} steps")
+    value = n * args.steps / el / 1e9
+    sample = (f"serial oracle exclusive add-scan of the whole 2^{n.bit_length() - 1}-element workload per step, "
+              f"{args.steps} steps, one thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Gelem/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
@@ -511,6 +563,10 @@ def run_op(args):
         f = torch.from_numpy(wl.predicate_flags(v, wl.threshold_for(0.5))).cuda()
         out, cnt = torch.empty_like(dv), torch.empty(1, dtype=torch.int32, device="cuda")
         fn = lambda: ds.compact(dv, f, out, cnt)
+    elif args.op == "f32scan":
+        x = torch.from_numpy(wl.unit_floats(n)).cuda()
+        out = torch.empty_like(x)
+        fn = lambda: ds.scan_inclusive(x, out)
     elif args.op == "segscan":
         sv, sh = wl.segmented(n)
         dv, dh = torch.from_numpy(sv).cuda(), torch.from_numpy(sh).cuda()
@@ -563,7 +619,8 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
-    p.add_argument("--op", choices=["scan", "compact50", "segscan", "bracket_check", "split", "sort32", "digit_sort"],
+    p.add_argument("--op", choices=["scan", "f32scan", "compact50", "segscan", "bracket_check", "split", "sort32",
+                                    "digit_sort"],
                    default="scan", help="scan: the benchmark; the others run one call repeatedly for profiling")
     args = p.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":

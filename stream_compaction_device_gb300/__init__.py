@@ -240,12 +240,14 @@ def device_status(stream=None) -> int:
 
 
 def set_carry_mode(mode: str) -> None:
-    """'default', 'lookback' (one tile per block), 'rts' (reduce-then-scan),
-    'pipelined' (persistent warp-specialised single pass) or 'l2' (the
-    cooperative forms: the L2-resident scan, the one-read bracket check, the
-    two-launch compaction with flags and split), process-wide."""
+    """Measurement hook (``devscan_measure_set_carry_mode``): 'default',
+    'lookback' (one tile per block), 'rts' (reduce-then-scan), 'pipelined'
+    (persistent warp-specialised single pass) or 'l2' (the cooperative forms:
+    the L2-resident scan, the one-read bracket check, the two-launch
+    compaction with flags and split).  Applies to the calling thread's later
+    calls only."""
     code = {"default": 0, "lookback": 1, "rts": 2, "pipelined": 3, "l2": 4}[mode]
-    _lib.check(load().devscan_set_carry_mode(code), "devscan_set_carry_mode")
+    _lib.check(load().devscan_measure_set_carry_mode(code), "devscan_measure_set_carry_mode")
 
 
 def stream_release(stream=None) -> None:

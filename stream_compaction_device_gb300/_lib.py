@@ -70,8 +70,8 @@ def load() -> ctypes.CDLL:
         lib.devscan_status_string.restype = ctypes.c_char_p
         lib.devscan_stream_release.argtypes = [vp]
         lib.devscan_stream_release.restype = i
-        lib.devscan_set_carry_mode.argtypes = [i]
-        lib.devscan_set_carry_mode.restype = i
+        lib.devscan_measure_set_carry_mode.argtypes = [i]
+        lib.devscan_measure_set_carry_mode.restype = i
         lib.devscan_selftest_stalled_wait.argtypes = [u, vp]
         lib.devscan_selftest_stalled_wait.restype = i
         lib.scan_exclusive_i32_noalloc.argtypes = [vp, vp, sz, i, vp]

@@ -8,6 +8,7 @@
 #include <utility>
 
 #include "../../include/devscan.h"
+#include "../../include/devscan_measure.h"
 #include "core.cuh"
 #include "launch.h"
 
@@ -19,7 +20,17 @@ namespace {
 // predecessor tile only has to load and reduce its own data).
 constexpr unsigned kSpinLimit = 1u << 21;
 
-std::atomic<int> g_carry_mode{kCarryDefault};
+// Largest tile count a workspace may hold: its capacity doubles from 1,024
+// in 64-bit arithmetic up to this power of two, so no size can wrap it.
+constexpr size_t kMaxTiles = size_t(1) << 31;
+constexpr size_t kMaxScanN = kMaxTiles * kScanTile;
+
+// The inter-block carry strategy of the calling thread's calls (kCarry*),
+// set only through devscan_measure_set_carry_mode (include/devscan_measure.h):
+// one thread choosing a path for a measurement leaves every other thread's
+// calls on the default.
+thread_local int t_carry_mode = kCarryDefault;
+int carry_mode() { return t_carry_mode; }
 
 struct Slot {
     void *base = nullptr;
@@ -61,10 +72,12 @@ devscan_status acquire(cudaStream_t stream, unsigned tiles, Workspace *out)
             return DEVSCAN_ERR_CUDA;
         sms = g_num_sms.emplace(dev, count).first;
     }
+    if (tiles > kMaxTiles) return DEVSCAN_ERR_INVALID;
     Slot &slot = g_slots[{dev, reinterpret_cast<uintptr_t>(stream)}];
     if (slot.base == nullptr || slot.ws.capacity < tiles) {
-        unsigned capacity = 1024;
-        while (capacity < tiles) capacity *= 2;
+        size_t cap = 1024;
+        while (cap < tiles) cap *= 2;   // at most kMaxTiles = 2^31
+        const unsigned capacity = static_cast<unsigned>(cap);
         const size_t bytes = layout_bytes(capacity);
         if (slot.base != nullptr) {
             if (cudaFreeAsync(slot.base, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
@@ -134,14 +147,13 @@ devscan_status scan_common(ElemType type, bool inclusive, const void *in, void *
     if (in == nullptr || out == nullptr) return DEVSCAN_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(in) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
         return DEVSCAN_ERR_INVALID;
-    const size_t max_n = static_cast<size_t>(0xffffffffu) * kScanTile;
-    if (n > max_n) return DEVSCAN_ERR_INVALID;
+    if (n > kMaxScanN) return DEVSCAN_ERR_INVALID;
     const unsigned tiles = tiles_for(n, kScanTile);
     Workspace ws;
     const devscan_status st = acquire(stream, tiles, &ws);
     if (st != DEVSCAN_OK) return st;
     const bool aligned = reinterpret_cast<uintptr_t>(in) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0;
-    const int carry = g_carry_mode.load(std::memory_order_relaxed);
+    const int carry = carry_mode();
     return from_cuda(launch_scan(type, static_cast<int>(op), inclusive, in, out, n, aligned, carry, ws,
                                  kSpinLimit, stream));
 }
@@ -155,13 +167,13 @@ devscan_status segscan_common(ElemType type, bool inclusive, const void *in, con
     if (in == nullptr || heads == nullptr || out == nullptr) return DEVSCAN_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(in) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
         return DEVSCAN_ERR_INVALID;
-    if (n > static_cast<size_t>(0xffffffffu) * kScanTile) return DEVSCAN_ERR_INVALID;
+    if (n > kMaxScanN) return DEVSCAN_ERR_INVALID;
     if (overlaps(heads, n, out, n * 4) || (in != out && overlaps(in, n * 4, out, n * 4))) return DEVSCAN_ERR_INVALID;
     Workspace ws;
     const devscan_status st = acquire(stream, tiles_for(n, kScanTile), &ws);
     if (st != DEVSCAN_OK) return st;
     return from_cuda(launch_segscan(type, static_cast<int>(op), inclusive, in, heads, out, n,
-                                    g_carry_mode.load(std::memory_order_relaxed), ws, kSpinLimit, stream));
+                                    carry_mode(), ws, kSpinLimit, stream));
 }
 
 }  // namespace
@@ -246,7 +258,7 @@ devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out
     Workspace ws;
     devscan_status st = acquire(stream, tiles, &ws);
     if (st != DEVSCAN_OK) return st;
-    const int carry = g_carry_mode.load(std::memory_order_relaxed);
+    const int carry = carry_mode();
     void *part_words = nullptr;   // the two-launch path's part counts and offsets
     if (carry == kCarryL2Resident || (carry == kCarryDefault && n >= kCompactTwoPassMinN)) {
         st = acquire_extra(stream, compact_part_words(n) * sizeof(uint32_t), &part_words);
@@ -272,14 +284,14 @@ devscan_status compact_gt_i32(const int32_t *in, int32_t threshold, int32_t *out
     Workspace ws;
     const devscan_status st = acquire(stream, tiles_for(n, kCompactTile), &ws);
     if (st != DEVSCAN_OK) return st;
-    return from_cuda(launch_compact_gt(in, threshold, out, count, n, g_carry_mode.load(std::memory_order_relaxed),
+    return from_cuda(launch_compact_gt(in, threshold, out, count, n, carry_mode(),
                                        ws, kSpinLimit, stream));
 }
 
 devscan_status bracket_scan_i32(const int32_t *in, int32_t *out, int32_t *result, size_t n, cudaStream_t stream)
 {
     if (result == nullptr || reinterpret_cast<uintptr_t>(result) % 4 != 0) return DEVSCAN_ERR_INVALID;
-    if (n > static_cast<size_t>(0xffffffffu) * kScanTile) return DEVSCAN_ERR_INVALID;
+    if (n > kMaxScanN) return DEVSCAN_ERR_INVALID;
     if (n > 0) {
         if (in == nullptr || reinterpret_cast<uintptr_t>(in) % 4 != 0) return DEVSCAN_ERR_INVALID;
         if (out != nullptr && reinterpret_cast<uintptr_t>(out) % 4 != 0) return DEVSCAN_ERR_INVALID;
@@ -291,7 +303,7 @@ devscan_status bracket_scan_i32(const int32_t *in, int32_t *out, int32_t *result
         const devscan_status st = acquire(stream, tiles_for(n, kScanTile), &ws);
         if (st != DEVSCAN_OK) return st;
     }
-    return from_cuda(launch_bracket(in, out, result, n, g_carry_mode.load(std::memory_order_relaxed), ws,
+    return from_cuda(launch_bracket(in, out, result, n, carry_mode(), ws,
                                     kSpinLimit, stream));
 }
 
@@ -309,7 +321,7 @@ devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_
     devscan_status st = acquire(stream, tiles, &ws);
     if (st != DEVSCAN_OK) return st;
     unsigned *z = &ws.state->zeros[40];
-    const int carry = g_carry_mode.load(std::memory_order_relaxed);
+    const int carry = carry_mode();
     if (reinterpret_cast<uintptr_t>(keys) % 16 == 0 &&
         (carry == kCarryL2Resident || (carry == kCarryDefault && n >= kSplitTwoPassMinN))) {
         void *part_words = nullptr;   // the parts' zero offsets
@@ -336,7 +348,7 @@ devscan_status radix_sort_u32(uint32_t *keys, uint32_t *tmp, size_t n, cudaStrea
     devscan_status st = acquire(stream, tiles, &ws);
     if (st != DEVSCAN_OK) return st;
     unsigned *z = ws.state->zeros;   // z[b] = zero count of bit b
-    const int carry = g_carry_mode.load(std::memory_order_relaxed);
+    const int carry = carry_mode();
     if (reinterpret_cast<uintptr_t>(keys) % 16 == 0 && reinterpret_cast<uintptr_t>(tmp) % 16 == 0 &&
         (carry == kCarryL2Resident || (carry == kCarryDefault && n >= kSortTwoPassMinN))) {
         void *part_words = nullptr;   // the parts' offsets, then the next pass's part counts
@@ -432,12 +444,12 @@ devscan_status devscan_stream_release(cudaStream_t stream)
     return from_cuda(cudaFreeAsync(base, stream));
 }
 
-devscan_status devscan_set_carry_mode(int mode)
+devscan_status devscan_measure_set_carry_mode(int mode)
 {
     if (mode != kCarryDefault && mode != kCarryLookback && mode != kCarryReduceThenScan && mode != kCarryPipelined &&
         mode != kCarryL2Resident)
         return DEVSCAN_ERR_INVALID;
-    g_carry_mode.store(mode, std::memory_order_relaxed);
+    t_carry_mode = mode;
     return DEVSCAN_OK;
 }
 

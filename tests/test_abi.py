@@ -1,7 +1,8 @@
 """The C-ABI library builds, loads and exports every entry point that
-include/devscan.h declares; host-side argument validation rejects bad calls
+include/*.h declares; host-side argument validation rejects bad calls
 before any CUDA work (no GPU needed: none of these calls reaches a kernel)."""
 import ctypes
+import glob
 import os
 import re
 
@@ -9,7 +10,7 @@ import pytest
 
 from conftest import ROOT
 
-HEADER = os.path.join(ROOT, "include", "devscan.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -21,13 +22,18 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER, encoding="utf-8").read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:devscan_status|const char \*)\s*(\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    for header in HEADERS:
+        text = open(header, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:devscan_status|const char \*)\s*(\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
+    assert [os.path.basename(h) for h in HEADERS] == ["devscan.h", "devscan_measure.h"]
     names = declared_functions()
+    assert "devscan_measure_set_carry_mode" in names
     for want in ("scan_inclusive_i32", "scan_exclusive_f32", "compact_i32", "split_bit_u32",
                  "radix_sort_u32", "devscan_device_status", "devscan_status_string"):
         assert want in names
@@ -73,8 +79,8 @@ def test_validation_without_device_work(lib):
     assert lib.split_bit_u32(None, None, 3, 0, None) == OK
     assert lib.radix_sort_u32(fake, fake, 10, None) == ERR_INVALID
     assert lib.radix_sort_u32(None, None, 0, None) == OK
-    assert lib.devscan_set_carry_mode(9) == ERR_INVALID
-    assert lib.devscan_set_carry_mode(0) == OK
+    assert lib.devscan_measure_set_carry_mode(9) == ERR_INVALID
+    assert lib.devscan_measure_set_carry_mode(0) == OK
     assert lib.devscan_selftest_stalled_wait(0, None) == ERR_INVALID
 
 

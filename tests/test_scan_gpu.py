@@ -108,6 +108,20 @@ def test_carry_modes(ds, mode):
         ds.set_carry_mode("default")
 
 
+def test_reduce_then_scan_at_full_size(ds):
+    """The reduce-then-scan carry at 2^28 elements, the size the benchmark
+    times it at (65,536 tile totals scanned by one block)."""
+    from stream_compaction_device_gb300 import workloads as wl
+    x = wl.brackets()
+    ds.set_carry_mode("rts")
+    try:
+        got = gpu_scan(ds, x, "add", False)
+    finally:
+        ds.set_carry_mode("default")
+    assert np.array_equal(got, oracle.scan(x, "add", False))
+    assert ds.device_status() == 0
+
+
 def test_default_size_boundaries(ds):
     """Sizes around the default's switches between the cluster scan, the
     one-tile kernel, the L2-resident scan and the pipeline (2^16, 2^17 and
