@@ -15,7 +15,8 @@ is needed between steps.  Prints one JSON line:
              download overlaps the next one's upload
   cpu_baseline  the serial CPU oracle on the host cores (1 thread)
   extra      the inclusive / max / xor sweep, the bracket check and bracket
-             scan and the segmented scan at N = 2^28; compaction (flags and
+             scan, the segmented scan, the fold and one rank's share of the
+             sharded scan at N = 2^28; compaction (flags and
              fused predicate), the split, the 32-pass and the 8-bit radix
              sorts at N = 2^26; fp32 add at N = 2^24; N = 65,536 latency; the
              reduce-then-scan carry.  Back-to-back calls between one pair of
@@ -418,6 +419,15 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
     med, _ = time_events(lambda: ds.bracket_scan(d_in, out=d_out, result=res), reps, 3)
     out["bracket_scan_2^28_mostly_negative"] = row(n, med, 8 * n)
     d_in.neg_()
+    # the fold alone (one read, 4 B per element), and one rank's device work
+    # in the sharded scan (its total, the fold of the gathered totals, the
+    # scan from the carry: 12 B per element); the exchange between ranks is
+    # not part of this single-GPU row
+    tot = torch.empty(1, dtype=torch.int32, device="cuda")
+    med, _ = time_events(lambda: ds.reduce(d_in, out=tot), reps, 3)
+    out["reduce_i32_add_2^28"] = row(n, med, 4 * n)
+    med, _ = time_events(lambda: ds.sharded_scan(d_in, d_out), reps, 3)
+    out["sharded_scan_one_rank_2^28"] = row(n, med, 12 * n)
     del d_in
     xm = torch.from_numpy(wl.max_values(n)).cuda()
     med, _ = time_events(lambda: ds.scan_inclusive(xm, d_out, op="max"), reps, 3)

@@ -86,6 +86,53 @@ devscan_status scan_exclusive_f32(const float *in, float *out, size_t n,
                                   devscan_op op, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Scans with a carry-in, and the fold of an array: the pieces of a scan whose
+ * input is split into contiguous shards, one per device (P1 section 四 and
+ * P2 section 3.2: reduce each part, scan the part totals, give every part
+ * its offset -- here the parts are shards instead of blocks).  Shard r of P:
+ *   1. reduce_T(shard_r, n_r, op, &total_r)      its own total;
+ *   2. the P totals are exchanged (an all-gather of P scalars, outside this
+ *      library: each device keeps the array totals[0 .. P) in its memory);
+ *   3. reduce_T(totals, r, op, &carry_r)         the fold of the earlier
+ *      shards' totals (the identity for r == 0);
+ *   4. scan_*_carry_T(shard_r, out_r, n_r, op, &carry_r)   its scan.
+ * The concatenated out_r then equal the scan of the whole array.
+ *
+ * scan_{inclusive,exclusive}_carry_T: the scans above with
+ *   out[i] = carry ⊕ (scan of in)[i], carry = *carry_in,
+ * i.e. the scan of the array that carry_in's value would precede; exclusive
+ * out[0] is the carry itself.
+ *   carry_in : device pointer to one T, 4-byte aligned, read on the stream
+ *              (so it may be written by earlier work on the same stream); it
+ *              must not overlap out (DEVSCAN_ERR_INVALID); NULL means the
+ *              identity (the plain scan).
+ * Other arguments, paths, limits and errors as the scans above.  fp32 add
+ * adds the carry in fp32 (one more rounding per element).
+ *
+ * reduce_T: *total = in[0] ⊕ in[1] ⊕ ... ⊕ in[n-1], the identity of ⊕ when
+ * n == 0.  One read of the input (4 bytes per element), one launch; fp32
+ * add is folded in a fixed order (the same n and alignment give the same
+ * bits).  in: device T[n], 4-byte aligned (NULL allowed when n == 0);
+ * total: device T, 4-byte aligned, not inside in.  Operators and errors as
+ * the scans.
+ * ------------------------------------------------------------------------- */
+devscan_status scan_inclusive_carry_i32(const int32_t *in, int32_t *out, size_t n, devscan_op op,
+                                        const int32_t *carry_in, cudaStream_t stream);
+devscan_status scan_inclusive_carry_u32(const uint32_t *in, uint32_t *out, size_t n, devscan_op op,
+                                        const uint32_t *carry_in, cudaStream_t stream);
+devscan_status scan_inclusive_carry_f32(const float *in, float *out, size_t n, devscan_op op,
+                                        const float *carry_in, cudaStream_t stream);
+devscan_status scan_exclusive_carry_i32(const int32_t *in, int32_t *out, size_t n, devscan_op op,
+                                        const int32_t *carry_in, cudaStream_t stream);
+devscan_status scan_exclusive_carry_u32(const uint32_t *in, uint32_t *out, size_t n, devscan_op op,
+                                        const uint32_t *carry_in, cudaStream_t stream);
+devscan_status scan_exclusive_carry_f32(const float *in, float *out, size_t n, devscan_op op,
+                                        const float *carry_in, cudaStream_t stream);
+devscan_status reduce_i32(const int32_t *in, size_t n, devscan_op op, int32_t *total, cudaStream_t stream);
+devscan_status reduce_u32(const uint32_t *in, size_t n, devscan_op op, uint32_t *total, cudaStream_t stream);
+devscan_status reduce_f32(const float *in, size_t n, devscan_op op, float *total, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Segmented scans (P2 section 7.2 names the segmented scan for sparse data):
  * heads[i] != 0 starts a new segment at i (element 0 always starts one) and
  * every segment is scanned on its own, the running value returning to the

@@ -14,7 +14,8 @@ import torch
 from . import _lib
 from ._lib import DevscanError, OPS, load
 
-__all__ = ["scan_inclusive", "scan_exclusive", "compact", "split_bit", "radix_sort", "radix_sort_digits", "scan_host",
+__all__ = ["scan_inclusive", "scan_exclusive", "scan_inclusive_carry", "scan_exclusive_carry", "reduce",
+           "sharded_scan", "exchange_totals", "compact", "split_bit", "radix_sort", "radix_sort_digits", "scan_host",
            "compact_greater", "bracket_scan", "segmented_scan_inclusive", "segmented_scan_exclusive",
            "device_status", "set_carry_mode", "stream_release", "selftest_stalled_wait", "DevscanError",
            "load"]
@@ -64,6 +65,91 @@ def scan_exclusive(x: torch.Tensor, out: torch.Tensor | None = None, op: str = "
                    as_uint32: bool = False) -> torch.Tensor:
     """z[i] = x[0] op ... op x[i-1]; z[0] = identity of op."""
     return _scan("exclusive", x, out, op, stream, "u32" if as_uint32 else None)
+
+
+def _carry_scan(direction: str, x: torch.Tensor, carry: torch.Tensor | None, out, op: str, stream,
+                dtype_override=None):
+    _check_cuda(x, "x")
+    suffix = dtype_override or _SUFFIX.get(x.dtype)
+    if suffix is None:
+        raise TypeError(f"unsupported dtype {x.dtype} (int32, uint32, float32)")
+    if carry is not None:
+        _check_cuda(carry, "carry")
+        if carry.dtype != x.dtype or carry.numel() < 1:
+            raise ValueError("carry must be a device tensor of x's dtype holding one element")
+    if out is None:
+        out = torch.empty_like(x)
+    _check_cuda(out, "out")
+    if out.numel() != x.numel() or out.dtype != x.dtype:
+        raise ValueError("out must match x in size and dtype")
+    name = f"scan_{direction}_carry_{suffix}"
+    _lib.check(getattr(load(), name)(x.data_ptr(), out.data_ptr(), x.numel(), OPS[op],
+                                     None if carry is None else carry.data_ptr(), _stream_handle(stream)), name)
+    return out
+
+
+def scan_inclusive_carry(x: torch.Tensor, carry: torch.Tensor | None, out: torch.Tensor | None = None,
+                         op: str = "add", stream=None, as_uint32: bool = False) -> torch.Tensor:
+    """y[i] = carry op x[0] op ... op x[i], ``carry`` a one-element device
+    tensor (None: the identity)."""
+    return _carry_scan("inclusive", x, carry, out, op, stream, "u32" if as_uint32 else None)
+
+
+def scan_exclusive_carry(x: torch.Tensor, carry: torch.Tensor | None, out: torch.Tensor | None = None,
+                         op: str = "add", stream=None, as_uint32: bool = False) -> torch.Tensor:
+    """z[i] = carry op x[0] op ... op x[i-1]; z[0] = carry."""
+    return _carry_scan("exclusive", x, carry, out, op, stream, "u32" if as_uint32 else None)
+
+
+def reduce(x: torch.Tensor, op: str = "add", out: torch.Tensor | None = None, stream=None,
+           as_uint32: bool = False) -> torch.Tensor:
+    """Fold of all of ``x`` under ``op`` into a one-element device tensor
+    (the identity for an empty ``x``)."""
+    _check_cuda(x, "x")
+    suffix = "u32" if as_uint32 else _SUFFIX.get(x.dtype)
+    if suffix is None:
+        raise TypeError(f"unsupported dtype {x.dtype} (int32, uint32, float32)")
+    if out is None:
+        out = torch.empty(1, dtype=x.dtype, device=x.device)
+    _check_cuda(out, "out")
+    if out.dtype != x.dtype or out.numel() < 1:
+        raise ValueError("out must hold one element of x's dtype")
+    name = f"reduce_{suffix}"
+    _lib.check(getattr(load(), name)(x.data_ptr() if x.numel() else None, x.numel(), OPS[op], out.data_ptr(),
+                                     _stream_handle(stream)), name)
+    return out
+
+
+def exchange_totals(total: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather of one total per rank: returns a tensor of ``world_size``
+    elements on ``total``'s device, element r from rank r (the one exchange
+    step of a sharded scan; NCCL for device tensors, gloo for host
+    tensors).  A single process returns ``total`` itself."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return total.reshape(1)
+    world = dist.get_world_size(group)
+    totals = torch.empty(world, dtype=total.dtype, device=total.device)
+    dist.all_gather_into_tensor(totals, total.reshape(1).contiguous(), group=group)
+    return totals
+
+
+def sharded_scan(shard: torch.Tensor, out: torch.Tensor | None = None, inclusive: bool = False, op: str = "add",
+                 group=None, stream=None, as_uint32: bool = False) -> torch.Tensor:
+    """This rank's part of the scan of an array split into contiguous shards,
+    shard r on rank r of ``group`` (in rank order).  The library folds this
+    shard's total, the ranks exchange their totals (one all-gather of one
+    element each), the library folds the totals of the ranks before this
+    one into a carry and scans the shard from it.  Every rank calls it; the
+    ranks' outputs, concatenated in rank order, are the scan of the whole
+    array."""
+    import torch.distributed as dist
+    rank = dist.get_rank(group) if dist.is_available() and dist.is_initialized() else 0
+    total = reduce(shard, op, stream=stream, as_uint32=as_uint32)
+    totals = exchange_totals(total, group)
+    carry = reduce(totals[:rank], op, stream=stream, as_uint32=as_uint32)
+    fn = scan_inclusive_carry if inclusive else scan_exclusive_carry
+    return fn(shard, carry, out, op=op, stream=stream, as_uint32=as_uint32)
 
 
 def _segscan(direction: str, x: torch.Tensor, heads: torch.Tensor, out, op: str, stream, dtype_override=None):

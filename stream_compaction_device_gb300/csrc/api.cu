@@ -139,7 +139,7 @@ bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes)
 }
 
 devscan_status scan_common(ElemType type, bool inclusive, const void *in, void *out, size_t n, devscan_op op,
-                           cudaStream_t stream)
+                           cudaStream_t stream, const void *carry_in = nullptr)
 {
     if (op != DEVSCAN_OP_ADD && op != DEVSCAN_OP_MAX && op != DEVSCAN_OP_XOR) return DEVSCAN_ERR_INVALID;
     if (type == ElemType::F32 && op == DEVSCAN_OP_XOR) return DEVSCAN_ERR_UNSUPPORTED;
@@ -148,6 +148,9 @@ devscan_status scan_common(ElemType type, bool inclusive, const void *in, void *
     if (reinterpret_cast<uintptr_t>(in) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
         return DEVSCAN_ERR_INVALID;
     if (n > kMaxScanN) return DEVSCAN_ERR_INVALID;
+    if (carry_in != nullptr &&
+        (reinterpret_cast<uintptr_t>(carry_in) % 4 != 0 || overlaps(carry_in, 4, out, n * 4)))
+        return DEVSCAN_ERR_INVALID;
     const unsigned tiles = tiles_for(n, kScanTile);
     Workspace ws;
     const devscan_status st = acquire(stream, tiles, &ws);
@@ -155,7 +158,22 @@ devscan_status scan_common(ElemType type, bool inclusive, const void *in, void *
     const bool aligned = reinterpret_cast<uintptr_t>(in) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0;
     const int carry = carry_mode();
     return from_cuda(launch_scan(type, static_cast<int>(op), inclusive, in, out, n, aligned, carry, ws,
-                                 kSpinLimit, stream));
+                                 kSpinLimit, stream, carry_in));
+}
+
+devscan_status reduce_common(ElemType type, const void *in, size_t n, devscan_op op, void *total,
+                             cudaStream_t stream)
+{
+    if (op != DEVSCAN_OP_ADD && op != DEVSCAN_OP_MAX && op != DEVSCAN_OP_XOR) return DEVSCAN_ERR_INVALID;
+    if (type == ElemType::F32 && op == DEVSCAN_OP_XOR) return DEVSCAN_ERR_UNSUPPORTED;
+    if (total == nullptr || reinterpret_cast<uintptr_t>(total) % 4 != 0) return DEVSCAN_ERR_INVALID;
+    if (n > kMaxScanN) return DEVSCAN_ERR_INVALID;
+    if (n > 0 && (in == nullptr || reinterpret_cast<uintptr_t>(in) % 4 != 0 || overlaps(total, 4, in, n * 4)))
+        return DEVSCAN_ERR_INVALID;
+    Workspace ws;
+    const devscan_status st = acquire(stream, 1, &ws);
+    if (st != DEVSCAN_OK) return st;
+    return from_cuda(launch_reduce(type, static_cast<int>(op), in, n, total, ws, stream));
 }
 
 devscan_status segscan_common(ElemType type, bool inclusive, const void *in, const uint8_t *heads, void *out,
@@ -206,6 +224,50 @@ devscan_status scan_exclusive_u32(const uint32_t *in, uint32_t *out, size_t n, d
 devscan_status scan_exclusive_f32(const float *in, float *out, size_t n, devscan_op op, cudaStream_t stream)
 {
     return scan_common(ElemType::F32, false, in, out, n, op, stream);
+}
+
+devscan_status scan_inclusive_carry_i32(const int32_t *in, int32_t *out, size_t n, devscan_op op,
+                                        const int32_t *carry_in, cudaStream_t stream)
+{
+    return scan_common(ElemType::I32, true, in, out, n, op, stream, carry_in);
+}
+devscan_status scan_inclusive_carry_u32(const uint32_t *in, uint32_t *out, size_t n, devscan_op op,
+                                        const uint32_t *carry_in, cudaStream_t stream)
+{
+    return scan_common(ElemType::U32, true, in, out, n, op, stream, carry_in);
+}
+devscan_status scan_inclusive_carry_f32(const float *in, float *out, size_t n, devscan_op op, const float *carry_in,
+                                        cudaStream_t stream)
+{
+    return scan_common(ElemType::F32, true, in, out, n, op, stream, carry_in);
+}
+devscan_status scan_exclusive_carry_i32(const int32_t *in, int32_t *out, size_t n, devscan_op op,
+                                        const int32_t *carry_in, cudaStream_t stream)
+{
+    return scan_common(ElemType::I32, false, in, out, n, op, stream, carry_in);
+}
+devscan_status scan_exclusive_carry_u32(const uint32_t *in, uint32_t *out, size_t n, devscan_op op,
+                                        const uint32_t *carry_in, cudaStream_t stream)
+{
+    return scan_common(ElemType::U32, false, in, out, n, op, stream, carry_in);
+}
+devscan_status scan_exclusive_carry_f32(const float *in, float *out, size_t n, devscan_op op, const float *carry_in,
+                                        cudaStream_t stream)
+{
+    return scan_common(ElemType::F32, false, in, out, n, op, stream, carry_in);
+}
+
+devscan_status reduce_i32(const int32_t *in, size_t n, devscan_op op, int32_t *total, cudaStream_t stream)
+{
+    return reduce_common(ElemType::I32, in, n, op, total, stream);
+}
+devscan_status reduce_u32(const uint32_t *in, size_t n, devscan_op op, uint32_t *total, cudaStream_t stream)
+{
+    return reduce_common(ElemType::U32, in, n, op, total, stream);
+}
+devscan_status reduce_f32(const float *in, size_t n, devscan_op op, float *total, cudaStream_t stream)
+{
+    return reduce_common(ElemType::F32, in, n, op, total, stream);
 }
 
 devscan_status segmented_scan_inclusive_i32(const int32_t *in, const uint8_t *heads, int32_t *out, size_t n,

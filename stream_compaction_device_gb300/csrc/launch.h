@@ -55,8 +55,11 @@ inline unsigned tiles_for(size_t n, int tile)
     return static_cast<unsigned>((n + static_cast<size_t>(tile) - 1) / static_cast<size_t>(tile));
 }
 
+// carry_in: a device element folded in front of the array (tile 0's prefix),
+// or null for the operator's identity.
 cudaError_t launch_scan(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
-                        bool aligned, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+                        bool aligned, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s,
+                        const void *carry_in = nullptr);
 
 cudaError_t launch_stalled_wait(const Workspace &ws, unsigned spin_limit, cudaStream_t s);
 
@@ -125,16 +128,22 @@ cudaError_t launch_bracket(const int32_t *in, int32_t *out, int32_t *result, siz
 // kClusterMaxN + 1 elements.
 constexpr size_t kClusterMaxN = size_t(1) << 16;
 cudaError_t launch_scan_cluster(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
-                                bool aligned, cudaStream_t s);
+                                bool aligned, cudaStream_t s, const void *carry_in = nullptr);
 
 // Scan of an input that fits in L2: one cooperative launch, one block per SM
 // (16-byte-aligned in/out).
 cudaError_t launch_scan_l2_resident(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
-                                   const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+                                   const Workspace &ws, unsigned spin_limit, cudaStream_t s,
+                                   const void *carry_in = nullptr);
 
 // Segmented scan: heads[i] != 0 starts a segment at i.
 cudaError_t launch_segscan(ElemType type, int op, bool inclusive, const void *in, const uint8_t *heads, void *out,
                            size_t n, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+
+// Fold of in[0, n) under `op` into the device element *total (the identity
+// when n == 0); one launch, deterministic order.
+cudaError_t launch_reduce(ElemType type, int op, const void *in, size_t n, void *total, const Workspace &ws,
+                          cudaStream_t s);
 
 // Digit width and passes of the multi-bit LSD radix sort.
 constexpr int kRadixDigitBits = 8, kRadixPasses = 32 / kRadixDigitBits;

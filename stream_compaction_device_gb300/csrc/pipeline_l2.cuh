@@ -170,6 +170,19 @@ template <class P>
 struct PolicyTicketBatch<P, decltype(void(P::kTicketBatch))> {
     static constexpr unsigned value = P::kTicketBatch;
 };
+// kCarryIn: tile 0's prefix is P::carry_prefix(args) -- the fold of
+// whatever precedes the array (a shard's offset in a scan split across
+// devices) -- and tile 0 publishes P::with_carry(args, aggregate) as its
+// inclusive prefix.  Without a carry both leave the values as they were.
+template <class P, class = void>
+struct PolicyCarryIn {
+    static constexpr bool value = false;
+};
+template <class P>
+struct PolicyCarryIn<P, decltype(void(P::kCarryIn))> {
+    static constexpr bool value = P::kCarryIn;
+};
+
 template <class P, class = void>
 struct PolicyScratch {
     static constexpr size_t value = 0;
@@ -486,6 +499,8 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 prefix = lookback2<Op>(op, status, group_status(status, capacity), t, tag, agg, &st->error,
                                        spin_limit, lane, head);
                 if (!head) publish<Op>(status, t, tag, kFlagInclusive, op(prefix, agg), lane);
+            } else if constexpr (PolicyCarryIn<P>::value) {
+                prefix = P::carry_prefix(args);
             }
             if (lane == 0) {
                 ctrl->rec_prefix[r] = to_bits(prefix);
@@ -569,8 +584,13 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
                 }
                 // publish first; a record (and so a look-back warp) is only
                 // claimed for the time the prefix takes to resolve
+                // tile 0 publishes its inclusive prefix: the carry-in (if
+                // any) folded with its aggregate
+                S pub = agg;
+                if constexpr (PolicyCarryIn<P>::value)
+                    if (t == 0) pub = P::with_carry(args, agg);
                 st_status(status + t, pack_status(tag, (t == 0 || head) ? kFlagInclusive : kFlagAggregate,
-                                                  to_bits(agg)));
+                                                  to_bits(pub)));
                 if (P::kHasExtra) P::after_reduce(args, t, ex);
                 if constexpr (PolicyAggregateAware<P>::value) P::on_aggregate(args, t, agg);
                 if (kr > 0) freed = mbar_wait(&ctrl->rec_free[r], (kr - 1) & 1u, wait_limit);
@@ -664,11 +684,15 @@ struct ScanPolicy {
     static constexpr int kParts = PARTS ? NS_ : 0;   // one part per consume warp
     static constexpr bool kWarpIndependent = PARTS;
     static constexpr unsigned kTicketBatch = TB;
+    static constexpr bool kCarryIn = true;
     struct Args {
         const S *in;
         S *out;
         size_t n;
+        const S *carry = nullptr;   // device word folded in front of the array, or null (identity)
     };
+    __device__ static S carry_prefix(const Args &a) { return a.carry != nullptr ? *a.carry : Op::identity(); }
+    __device__ static S with_carry(const Args &a, S v) { return a.carry != nullptr ? Op()(*a.carry, v) : v; }
     __device__ static unsigned tile_len(const Args &a, unsigned t)
     {
         const size_t rem = a.n - static_cast<size_t>(t) * kTile;

@@ -166,14 +166,14 @@ namespace {
 
 template <class Op, bool INCLUSIVE, bool ALIGNED>
 cudaError_t launch_lookback(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,
-                            cudaStream_t s)
+                            cudaStream_t s, const void *carry_in)
 {
     using S = typename Op::S;
     constexpr int THREADS = kScanThreads, VECS = kScanVecs;
     const unsigned tiles = tiles_for(n, kScanTile);
     scan_lookback_kernel<Op, THREADS, VECS, INCLUSIVE, ALIGNED, kUseTickets><<<tiles, THREADS, 0, s>>>(
         static_cast<const S *>(in), static_cast<S *>(out), n, tiles, ws.status, ws.state, ws.capacity,
-        spin_limit);
+        spin_limit, NoEpilogue::Args{}, static_cast<const S *>(carry_in));
     return cudaGetLastError();
 }
 
@@ -196,7 +196,7 @@ constexpr size_t kL2ResidentMinN = size_t(1) << 17, kL2ResidentMaxN = size_t(1) 
 
 template <class Op, bool INCLUSIVE>
 cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,
-                             cudaStream_t s)
+                             cudaStream_t s, const void *carry_in)
 {
     using S = typename Op::S;
     using P = ScanPolicy<Op, INCLUSIVE, 16, 4, 4, 2, 4, 10, kL2EvictLast, kL2EvictFirst, true, 1, true, 2>;
@@ -214,7 +214,7 @@ cudaError_t launch_pipelined(const void *in, void *out, size_t n, const Workspac
     }
     const unsigned tiles = tiles_for(n, P::kTile);
     const unsigned grid = tiles < static_cast<unsigned>(ws.num_sms) ? tiles : static_cast<unsigned>(ws.num_sms);
-    typename P::Args args{static_cast<const S *>(in), static_cast<S *>(out), n};
+    typename P::Args args{static_cast<const S *>(in), static_cast<S *>(out), n, static_cast<const S *>(carry_in)};
     kernel<<<grid, G::kThreads, G::kSmemBytes, s>>>(args, tiles, ws.status, ws.state, ws.capacity, spin_limit,
                                                     kWaitLimit);
     return cudaGetLastError();
@@ -236,49 +236,51 @@ cudaError_t launch_rts(const void *in, void *out, size_t n, const Workspace &ws,
 
 template <class Op, bool INCLUSIVE>
 cudaError_t dispatch_op(const void *in, void *out, size_t n, bool aligned, int carry, const Workspace &ws,
-                        unsigned spin_limit, cudaStream_t s)
+                        unsigned spin_limit, cudaStream_t s, const void *carry_in)
 {
-    if (carry == kCarryReduceThenScan && aligned) return launch_rts<Op, INCLUSIVE>(in, out, n, ws, s);
+    // reduce-then-scan has no carry-in: a scan with one takes the look-back
+    if (carry == kCarryReduceThenScan && aligned && carry_in == nullptr) return launch_rts<Op, INCLUSIVE>(in, out, n, ws, s);
     // up to 2^19 elements the pipeline's fill latency outweighs its
     // bandwidth: one tile per block is faster there (measured on GB300)
     const bool pipelined = aligned && (carry == kCarryPipelined || (carry == kCarryDefault && n >= kPipelineMinN));
-    if (pipelined) return launch_pipelined<Op, INCLUSIVE>(in, out, n, ws, spin_limit, s);
-    if (aligned) return launch_lookback<Op, INCLUSIVE, true>(in, out, n, ws, spin_limit, s);
-    return launch_lookback<Op, INCLUSIVE, false>(in, out, n, ws, spin_limit, s);
+    if (pipelined) return launch_pipelined<Op, INCLUSIVE>(in, out, n, ws, spin_limit, s, carry_in);
+    if (aligned) return launch_lookback<Op, INCLUSIVE, true>(in, out, n, ws, spin_limit, s, carry_in);
+    return launch_lookback<Op, INCLUSIVE, false>(in, out, n, ws, spin_limit, s, carry_in);
 }
 
 template <class Op>
 cudaError_t dispatch_dir(const void *in, void *out, size_t n, bool inclusive, bool aligned, int carry,
-                         const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+                         const Workspace &ws, unsigned spin_limit, cudaStream_t s, const void *carry_in)
 {
-    return inclusive ? dispatch_op<Op, true>(in, out, n, aligned, carry, ws, spin_limit, s)
-                     : dispatch_op<Op, false>(in, out, n, aligned, carry, ws, spin_limit, s);
+    return inclusive ? dispatch_op<Op, true>(in, out, n, aligned, carry, ws, spin_limit, s, carry_in)
+                     : dispatch_op<Op, false>(in, out, n, aligned, carry, ws, spin_limit, s, carry_in);
 }
 
 }  // namespace
 
 cudaError_t launch_scan(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
-                        bool aligned, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+                        bool aligned, int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s,
+                        const void *carry_in)
 {
     // small inputs: one thread-block cluster (scan_cluster.cu)
     if (carry == kCarryDefault && n <= kClusterMaxN)
-        return launch_scan_cluster(type, op, inclusive, in, out, n, aligned, s);
+        return launch_scan_cluster(type, op, inclusive, in, out, n, aligned, s, carry_in);
     // inputs that fit in L2: one cooperative launch (scan_l2res.cu)
     if (aligned && (carry == kCarryL2Resident ||
                     (carry == kCarryDefault && n >= kL2ResidentMinN && n <= kL2ResidentMaxN)))
-        return launch_scan_l2_resident(type, op, inclusive, in, out, n, ws, spin_limit, s);
+        return launch_scan_l2_resident(type, op, inclusive, in, out, n, ws, spin_limit, s, carry_in);
     switch (type) {
     case ElemType::I32:
-        if (op == kOpAdd) return dispatch_dir<AddU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
-        if (op == kOpMax) return dispatch_dir<MaxI32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
-        return dispatch_dir<XorU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+        if (op == kOpAdd) return dispatch_dir<AddU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s, carry_in);
+        if (op == kOpMax) return dispatch_dir<MaxI32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s, carry_in);
+        return dispatch_dir<XorU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s, carry_in);
     case ElemType::U32:
-        if (op == kOpAdd) return dispatch_dir<AddU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
-        if (op == kOpMax) return dispatch_dir<MaxU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
-        return dispatch_dir<XorU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+        if (op == kOpAdd) return dispatch_dir<AddU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s, carry_in);
+        if (op == kOpMax) return dispatch_dir<MaxU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s, carry_in);
+        return dispatch_dir<XorU32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s, carry_in);
     case ElemType::F32:
-        if (op == kOpAdd) return dispatch_dir<AddF32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
-        return dispatch_dir<MaxF32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s);
+        if (op == kOpAdd) return dispatch_dir<AddF32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s, carry_in);
+        return dispatch_dir<MaxF32>(in, out, n, inclusive, aligned, carry, ws, spin_limit, s, carry_in);
     }
     return cudaErrorInvalidValue;
 }

@@ -51,7 +51,8 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(const void *p, unsigned rank)
 
 template <class Op, bool INCLUSIVE, bool ALIGNED>
 __global__ void __launch_bounds__(kClusterThreads, 1)
-scan_cluster_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n)
+scan_cluster_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,
+                    const typename Op::S *carry_in)
 {
     using S = typename Op::S;
     constexpr int NWARPS = kClusterThreads / 32, VECS = kClusterVecs;
@@ -90,7 +91,13 @@ scan_cluster_kernel(const typename Op::S *__restrict__ in, typename Op::S *__res
             if (lane >= d) v = op(u, v);
         }
         const S prefix = __shfl_sync(kFullMask, v, rank > 0 ? rank - 1 : 0);
-        if (lane == 0) s_prefix = rank > 0 ? prefix : Op::identity();
+        if (lane == 0) {
+            // a carry-in (the fold of whatever precedes the array) goes in front
+            if (carry_in != nullptr)
+                s_prefix = rank > 0 ? op(*carry_in, prefix) : *carry_in;
+            else
+                s_prefix = rank > 0 ? prefix : Op::identity();
+        }
     }
     cluster_sync();   // the later blocks have read s_total; s_prefix is visible block-wide
 
@@ -114,7 +121,7 @@ scan_cluster_kernel(const typename Op::S *__restrict__ in, typename Op::S *__res
 }
 
 template <class Op, bool INCLUSIVE, bool ALIGNED>
-cudaError_t launch_cluster(const void *in, void *out, size_t n, cudaStream_t s)
+cudaError_t launch_cluster(const void *in, void *out, size_t n, cudaStream_t s, const void *carry_in)
 {
     using S = typename Op::S;
     const unsigned blocks = static_cast<unsigned>((n + kClusterTile - 1) / kClusterTile);
@@ -131,15 +138,16 @@ cudaError_t launch_cluster(const void *in, void *out, size_t n, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, scan_cluster_kernel<Op, INCLUSIVE, ALIGNED>, static_cast<const S *>(in),
-                              static_cast<S *>(out), n);
+                              static_cast<S *>(out), n, static_cast<const S *>(carry_in));
 }
 
 template <class Op>
-cudaError_t dispatch(const void *in, void *out, size_t n, bool inclusive, bool aligned, cudaStream_t s)
+cudaError_t dispatch(const void *in, void *out, size_t n, bool inclusive, bool aligned, cudaStream_t s,
+                     const void *c)
 {
     if (inclusive)
-        return aligned ? launch_cluster<Op, true, true>(in, out, n, s) : launch_cluster<Op, true, false>(in, out, n, s);
-    return aligned ? launch_cluster<Op, false, true>(in, out, n, s) : launch_cluster<Op, false, false>(in, out, n, s);
+        return aligned ? launch_cluster<Op, true, true>(in, out, n, s, c) : launch_cluster<Op, true, false>(in, out, n, s, c);
+    return aligned ? launch_cluster<Op, false, true>(in, out, n, s, c) : launch_cluster<Op, false, false>(in, out, n, s, c);
 }
 
 }  // namespace
@@ -148,21 +156,21 @@ static_assert(kClusterMaxN == static_cast<size_t>(kClusterBlocks) * kClusterTile
               "the small-scan limit is one portable cluster of tiles");
 
 cudaError_t launch_scan_cluster(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
-                                bool aligned, cudaStream_t s)
+                                bool aligned, cudaStream_t s, const void *carry_in)
 {
     if (n == 0 || n > kClusterMaxN) return cudaErrorInvalidValue;
     switch (type) {
     case ElemType::I32:
-        if (op == kOpAdd) return dispatch<AddU32>(in, out, n, inclusive, aligned, s);
-        if (op == kOpMax) return dispatch<MaxI32>(in, out, n, inclusive, aligned, s);
-        return dispatch<XorU32>(in, out, n, inclusive, aligned, s);
+        if (op == kOpAdd) return dispatch<AddU32>(in, out, n, inclusive, aligned, s, carry_in);
+        if (op == kOpMax) return dispatch<MaxI32>(in, out, n, inclusive, aligned, s, carry_in);
+        return dispatch<XorU32>(in, out, n, inclusive, aligned, s, carry_in);
     case ElemType::U32:
-        if (op == kOpAdd) return dispatch<AddU32>(in, out, n, inclusive, aligned, s);
-        if (op == kOpMax) return dispatch<MaxU32>(in, out, n, inclusive, aligned, s);
-        return dispatch<XorU32>(in, out, n, inclusive, aligned, s);
+        if (op == kOpAdd) return dispatch<AddU32>(in, out, n, inclusive, aligned, s, carry_in);
+        if (op == kOpMax) return dispatch<MaxU32>(in, out, n, inclusive, aligned, s, carry_in);
+        return dispatch<XorU32>(in, out, n, inclusive, aligned, s, carry_in);
     case ElemType::F32:
-        if (op == kOpAdd) return dispatch<AddF32>(in, out, n, inclusive, aligned, s);
-        return dispatch<MaxF32>(in, out, n, inclusive, aligned, s);
+        if (op == kOpAdd) return dispatch<AddF32>(in, out, n, inclusive, aligned, s, carry_in);
+        return dispatch<MaxF32>(in, out, n, inclusive, aligned, s, carry_in);
     }
     return cudaErrorInvalidValue;
 }

@@ -23,12 +23,15 @@ struct NoEpilogue {
 // per SM the register allocation must allow; EPI: per-tile epilogue (it sees
 // the scanned rows, whether the tile is the last one, and the tile's
 // inclusive prefix).  With an active epilogue a null `out` skips the store.
+// carry_in: a device word that seeds tile 0's prefix (the fold of whatever
+// precedes the array), or null for the identity.
 template <class Op, int THREADS, int VECS, bool INCLUSIVE, bool ALIGNED, bool TICKETS,
           int LB = kLookbackPerLane, int MINB = 1, bool TWO_LEVEL = false, class EPI = NoEpilogue>
 __global__ void __launch_bounds__(THREADS, MINB)
 scan_lookback_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,
                      unsigned num_tiles, unsigned long long *status, DevState *st, unsigned capacity,
-                     unsigned spin_limit, typename EPI::Args epi = typename EPI::Args{})
+                     unsigned spin_limit, typename EPI::Args epi = typename EPI::Args{},
+                     const typename Op::S *carry_in = nullptr)
 {
     using S = typename Op::S;
     constexpr int NWARPS = THREADS / 32;
@@ -73,7 +76,9 @@ scan_lookback_kernel(const typename Op::S *__restrict__ in, typename Op::S *__re
         const unsigned tag = __shfl_sync(kFullMask, lane == 0 ? read_tag(st) : 0u, 0);
         S prefix = Op::identity();
         if (tile == 0) {
-            publish<Op>(status, tile, tag, kFlagInclusive, tile_total, lane);
+            if (carry_in != nullptr) prefix = *carry_in;
+            publish<Op>(status, tile, tag, kFlagInclusive, carry_in != nullptr ? op(prefix, tile_total) : tile_total,
+                        lane);
         } else {
             publish<Op>(status, tile, tag, kFlagAggregate, tile_total, lane);
             if (TWO_LEVEL)

@@ -30,7 +30,8 @@ namespace {
 template <class Op, bool INCLUSIVE, int THREADS, int VECS>
 __global__ void __launch_bounds__(THREADS, 1)
 l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *__restrict__ out, size_t n,
-                        size_t chunk, typename Op::S *__restrict__ block_sums, DevState *st, unsigned spin_limit)
+                        size_t chunk, typename Op::S *__restrict__ block_sums, DevState *st, unsigned spin_limit,
+                        const typename Op::S *carry_in)
 {
     using S = typename Op::S;
     constexpr int NWARPS = THREADS / 32;
@@ -90,7 +91,7 @@ l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *_
             for (unsigned b = lane; b < blockIdx.x; b += 32) v = op(v, __ldcg(block_sums + b));   // through L2
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) v = op(v, __shfl_xor_sync(kFullMask, v, d));
-        if (lane == 0) s_carry = v;
+        if (lane == 0) s_carry = carry_in != nullptr ? op(*carry_in, v) : v;
     }
     __syncthreads();
     S carry;
@@ -137,7 +138,7 @@ l2_resident_scan_kernel(const typename Op::S *__restrict__ in, typename Op::S *_
 
 template <class Op, bool INCLUSIVE, int VECS>
 cudaError_t launch_l2res(const void *in, void *out, size_t n, const Workspace &ws, unsigned spin_limit,
-                         cudaStream_t s)
+                         cudaStream_t s, const void *carry_in)
 {
     using S = typename Op::S;
     constexpr int THREADS = 1024;
@@ -150,40 +151,41 @@ cudaError_t launch_l2res(const void *in, void *out, size_t n, const Workspace &w
     S *sout = static_cast<S *>(out);
     S *sums = reinterpret_cast<S *>(ws.tile_sums);
     DevState *st = ws.state;
-    void *args[] = {&sin, &sout, &n, const_cast<size_t *>(&chunk), &sums, &st, &spin_limit};
+    const S *carry = static_cast<const S *>(carry_in);
+    void *args[] = {&sin, &sout, &n, const_cast<size_t *>(&chunk), &sums, &st, &spin_limit, &carry};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(&l2_resident_scan_kernel<Op, INCLUSIVE, THREADS, VECS>),
                                        dim3(static_cast<unsigned>(blocks)), dim3(THREADS), args, 0, s);
 }
 
 template <class Op>
 cudaError_t launch_l2res_dir(bool inclusive, const void *in, void *out, size_t n, const Workspace &ws,
-                             unsigned spin_limit, cudaStream_t s)
+                             unsigned spin_limit, cudaStream_t s, const void *carry_in)
 {
     // small inputs take 4,096-element chunk units so that more blocks share them
     if (n >= (size_t(1) << 21))
-        return inclusive ? launch_l2res<Op, true, 2>(in, out, n, ws, spin_limit, s)
-                         : launch_l2res<Op, false, 2>(in, out, n, ws, spin_limit, s);
-    return inclusive ? launch_l2res<Op, true, 1>(in, out, n, ws, spin_limit, s)
-                     : launch_l2res<Op, false, 1>(in, out, n, ws, spin_limit, s);
+        return inclusive ? launch_l2res<Op, true, 2>(in, out, n, ws, spin_limit, s, carry_in)
+                         : launch_l2res<Op, false, 2>(in, out, n, ws, spin_limit, s, carry_in);
+    return inclusive ? launch_l2res<Op, true, 1>(in, out, n, ws, spin_limit, s, carry_in)
+                     : launch_l2res<Op, false, 1>(in, out, n, ws, spin_limit, s, carry_in);
 }
 
 }  // namespace
 
 cudaError_t launch_scan_l2_resident(ElemType type, int op, bool inclusive, const void *in, void *out, size_t n,
-                                   const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+                                   const Workspace &ws, unsigned spin_limit, cudaStream_t s, const void *carry_in)
 {
     switch (type) {
     case ElemType::I32:
-        if (op == kOpAdd) return launch_l2res_dir<AddU32>(inclusive, in, out, n, ws, spin_limit, s);
-        if (op == kOpMax) return launch_l2res_dir<MaxI32>(inclusive, in, out, n, ws, spin_limit, s);
-        return launch_l2res_dir<XorU32>(inclusive, in, out, n, ws, spin_limit, s);
+        if (op == kOpAdd) return launch_l2res_dir<AddU32>(inclusive, in, out, n, ws, spin_limit, s, carry_in);
+        if (op == kOpMax) return launch_l2res_dir<MaxI32>(inclusive, in, out, n, ws, spin_limit, s, carry_in);
+        return launch_l2res_dir<XorU32>(inclusive, in, out, n, ws, spin_limit, s, carry_in);
     case ElemType::U32:
-        if (op == kOpAdd) return launch_l2res_dir<AddU32>(inclusive, in, out, n, ws, spin_limit, s);
-        if (op == kOpMax) return launch_l2res_dir<MaxU32>(inclusive, in, out, n, ws, spin_limit, s);
-        return launch_l2res_dir<XorU32>(inclusive, in, out, n, ws, spin_limit, s);
+        if (op == kOpAdd) return launch_l2res_dir<AddU32>(inclusive, in, out, n, ws, spin_limit, s, carry_in);
+        if (op == kOpMax) return launch_l2res_dir<MaxU32>(inclusive, in, out, n, ws, spin_limit, s, carry_in);
+        return launch_l2res_dir<XorU32>(inclusive, in, out, n, ws, spin_limit, s, carry_in);
     case ElemType::F32:
-        if (op == kOpAdd) return launch_l2res_dir<AddF32>(inclusive, in, out, n, ws, spin_limit, s);
-        return launch_l2res_dir<MaxF32>(inclusive, in, out, n, ws, spin_limit, s);
+        if (op == kOpAdd) return launch_l2res_dir<AddF32>(inclusive, in, out, n, ws, spin_limit, s, carry_in);
+        return launch_l2res_dir<MaxF32>(inclusive, in, out, n, ws, spin_limit, s, carry_in);
     }
     return cudaErrorInvalidValue;
 }
