@@ -21,6 +21,8 @@ is needed between steps.  Prints one JSON line:
              sorts at N = 2^26; fp32 add at N = 2^24; N = 65,536 latency; the
              reduce-then-scan carry.  Back-to-back calls between one pair of
              events (device time per call), except the rows that flush L2
+             (a read of 256 MiB before each call; per-call events, 10%-trimmed
+             mean of at least 200 calls)
 
 ``--impl reference`` times the CPU oracle instead (the reference arm): each
 step is the oracle's serial exclusive scan of the same 2^28-element
@@ -206,7 +208,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def time_events(fn, reps, warmup, flush=None):
     """Per-call milliseconds of fn() with CUDA events on the current stream,
-    as (median, mean).  Without ``flush`` the calls run back to back between
+    as (median, mean; with ``flush``: the 10%-trimmed mean).  Without ``flush`` the calls run back to back between
     one pair of events, as the headline steps do, so the host's launch
     overhead overlaps the device work and the result is the device time per
     call (median and mean are then the same number).  With ``flush`` (run
@@ -237,8 +239,9 @@ def time_events(fn, reps, warmup, flush=None):
         b.record()
         pairs.append((a, b))
     torch.cuda.synchronize()
-    times = [a.elapsed_time(b) for a, b in pairs]
-    return statistics.median(times), statistics.fmean(times)
+    times = sorted(a.elapsed_time(b) for a, b in pairs)
+    k = len(times) // 10   # the 10%-trimmed mean: the event timer ticks in steps of about 2 us, so a
+    return statistics.median(times), statistics.fmean(times[k:len(times) - k])   # single median snaps to a tick
 
 
 def cpu_oracle_rate(x: np.ndarray, budget_s: float):
@@ -507,17 +510,19 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
     xf = torch.from_numpy(wl.unit_floats()).cuda()
     yf = torch.empty_like(xf)
     nf = xf.numel()
-    med, _ = time_events(lambda: ds.scan_inclusive(xf, yf), reps, 3, flush=flush)
-    out["f32_add_inclusive_2^24"] = row(nf, med, 8 * nf)
-    med, _ = time_events(lambda: ds.scan_exclusive(xf, yf), reps, 3, flush=flush)
-    out["f32_add_exclusive_2^24"] = row(nf, med, 8 * nf)
+    # per-call events snap to the timer's ~2 us ticks: many calls, trimmed mean
+    flushed_reps = max(reps, 200)
+    _, mean = time_events(lambda: ds.scan_inclusive(xf, yf), flushed_reps, 3, flush=flush)
+    out["f32_add_inclusive_2^24"] = row(nf, mean, 8 * nf)
+    _, mean = time_events(lambda: ds.scan_exclusive(xf, yf), flushed_reps, 3, flush=flush)
+    out["f32_add_exclusive_2^24"] = row(nf, mean, 8 * nf)
     del xf, yf
 
     # N = 65,536 latency (launch-bound)
     xs = torch.from_numpy(wl.small_digits()).cuda()
     ys = torch.empty_like(xs)
-    med, _ = time_events(lambda: ds.scan_exclusive(xs, ys), reps, 3, flush=flush)
-    out["i32_add_exclusive_65536"] = row(xs.numel(), med, 8 * xs.numel())
+    _, mean = time_events(lambda: ds.scan_exclusive(xs, ys), flushed_reps, 3, flush=flush)
+    out["i32_add_exclusive_65536"] = row(xs.numel(), mean, 8 * xs.numel())
     return out
 
 
