@@ -14,6 +14,7 @@ is needed between steps.  Prints one JSON line:
              every step; steps alternate between two streams, so one step's
              download overlaps the next one's upload
   cpu_baseline  the serial CPU oracle on the host cores (1 thread)
+  cpu_baseline_mt  the blocked three-phase scan on every host core
   extra      the inclusive / max / xor sweep, the bracket check and bracket
              scan, the segmented scan, the fold and one rank's share of the
              sharded scan at N = 2^28; compaction (flags and
@@ -244,6 +245,22 @@ def time_events(fn, reps, warmup, flush=None):
     return statistics.median(times), statistics.fmean(times[k:len(times) - k])   # single median snaps to a tick
 
 
+def cpu_mt_rate(x: np.ndarray, budget_s: float):
+    """Multithreaded CPU baseline (blocked three-phase scan on every host
+    core) throughput in Gelem/s, repeated until ``budget_s`` seconds pass;
+    returns (rate, runs, seconds, threads used)."""
+    import oracle
+    _, used = oracle.mt_scan_exclusive_add(x[:1 << 16])
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _, used = oracle.mt_scan_exclusive_add(x)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s and reps >= 2:
+            break
+    return x.size * reps / el / 1e9, reps, el, used
+
+
 def cpu_oracle_rate(x: np.ndarray, budget_s: float):
     """Serial oracle exclusive add-scan throughput (Gelem/s) on repeated runs
     over ``x`` until ``budget_s`` seconds of CPU work have been spent."""
@@ -352,12 +369,16 @@ def run_ours(args):
     if not args.no_extras and rank == 0:
         extra = run_extras(args, ds, wl, d_in, d_out, peak)
 
-    cpu = None
+    cpu = cpu_mt = None
     if rank == 0 and world >= 1 and not args.no_cpu:
         rate, reps, el = cpu_oracle_rate(x_host, args.cpu_budget)
         cpu = {"value": round(rate, 4), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
                "sample": f"serial oracle exclusive add-scan of the full 2^{n.bit_length() - 1}-element "
                          f"workload, {reps} runs, {el:.1f} s"}
+        rate, reps, el, used = cpu_mt_rate(x_host, args.cpu_budget / 2)
+        cpu_mt = {"value": round(rate, 4), "unit": "Gelem/s", "cores": used, "kind": "blocked three-phase, threads",
+                  "sample": f"multithreaded blocked exclusive add-scan of the full 2^{n.bit_length() - 1}-element "
+                            f"workload on {used} host threads, {reps} runs, {el:.1f} s"}
 
     if rank == 0:
         line = {
@@ -375,7 +396,7 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4), "traffic": SCAN_TRAFFIC_BYTES,
                          "kernel": "pipeline_l2_kernel<ScanPolicy<AddU32,exclusive,16,4,4,2,4,10,prefetch 1,parts,2 tiles per ticket>>",
                          "algorithmic_bytes_per_launch": alg_bytes, "peak_kind": peak_kind},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
+            "cpu_baseline": cpu, "cpu_baseline_mt": cpu_mt, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
             "clocks": clock_info, "parity_sampled": parity_ok, "extra": extra,
         }
         print(json.dumps(line), flush=True)
@@ -477,6 +498,18 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
         comp_gt[f"{int(sel * 100)}%"] = r
     out["compaction_2^26"] = comp
     out["compaction_gt_fused_2^26"] = comp_gt
+    # the fused predicate's two-launch form (measurement hook)
+    comp_gt2 = {}
+    ds.set_carry_mode("l2")
+    for sel in wl.SELECTIVITIES:
+        t = wl.threshold_for(sel)
+        med, _ = time_events(lambda: ds.compact_greater(dv, t, dout, cnt), reps, 3)
+        k = int(cnt.item())
+        r = row(nc, med, 4 * nc + 4 * k + 4)
+        r["kept"] = k
+        comp_gt2[f"{int(sel * 100)}%"] = r
+    ds.set_carry_mode(args.carry)
+    out["compaction_gt_fused_two_launch_2^26"] = comp_gt2
 
     # split and radix sort at N = 2^26
     keys = torch.from_numpy(wl.radix_keys(nc).view(np.int32)).cuda()

@@ -31,6 +31,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
+_MT_SRC = os.path.join(_HERE, "mt_baseline.c")   # the multithreaded CPU baseline (not the oracle)
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 OPS = {"add": 0, "max": 1, "xor": 2}
@@ -42,11 +43,11 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile ``oracle.c`` into ``liboracle.so`` with gcc (no -ffast-math)."""
     stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+             or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC), os.path.getmtime(_MT_SRC)))
     if force or stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall",
-               "-Wextra", "-o", tmp, _SRC, "-lm"]
+        cmd = ["gcc", "-O2", "-std=c11", "-D_POSIX_C_SOURCE=200809L", "-fPIC", "-shared", "-pthread", "-Wall",
+               "-Wextra", "-o", tmp, _SRC, _MT_SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -80,6 +81,8 @@ def _load():
         lib.oracle_sort_lsd_u32.restype = None
         lib.oracle_bracket_flags.argtypes = [vp, sz, ctypes.POINTER(i), ctypes.POINTER(i)]
         lib.oracle_bracket_flags.restype = None
+        lib.mt_scan_excl_add_i32.argtypes = [vp, vp, sz, i]
+        lib.mt_scan_excl_add_i32.restype = i
         _lib = lib
         return lib
 
@@ -217,3 +220,14 @@ def identity(op: str, dtype) -> float | int:
     if dtype == np.uint32:
         return 0
     return float("-inf")
+
+
+def mt_scan_exclusive_add(x, threads: int | None = None) -> tuple[np.ndarray, int]:
+    """The multithreaded CPU baseline (``mt_baseline.c``, not the oracle):
+    blocked three-phase int32 exclusive add-scan on up to ``threads`` host
+    threads (default: every core).  Returns (scan, threads used)."""
+    x = _contig(x, np.int32)
+    y = np.empty_like(x)
+    t = threads if threads is not None else (os.cpu_count() or 1)
+    used = _load().mt_scan_excl_add_i32(_ptr(x), _ptr(y), x.size, int(t))
+    return y, int(used)

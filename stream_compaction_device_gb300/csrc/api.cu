@@ -344,10 +344,16 @@ devscan_status compact_gt_i32(const int32_t *in, int32_t threshold, int32_t *out
     }
     if (n == 0) return from_cuda(cudaMemsetAsync(count, 0, sizeof(int32_t), stream));
     Workspace ws;
-    const devscan_status st = acquire(stream, tiles_for(n, kCompactTile), &ws);
+    devscan_status st = acquire(stream, tiles_for(n, kCompactTile), &ws);
     if (st != DEVSCAN_OK) return st;
-    return from_cuda(launch_compact_gt(in, threshold, out, count, n, carry_mode(),
-                                       ws, kSpinLimit, stream));
+    const int carry = carry_mode();
+    void *part_words = nullptr;   // the two-launch path's part masks, counts and offsets
+    if (carry == kCarryL2Resident) {
+        st = acquire_extra(stream, compact_part_words(n) * sizeof(uint32_t), &part_words);
+        if (st != DEVSCAN_OK) return st;
+    }
+    return from_cuda(launch_compact_gt(in, threshold, out, count, n, carry, ws, kSpinLimit, stream,
+                                       static_cast<uint32_t *>(part_words)));
 }
 
 devscan_status bracket_scan_i32(const int32_t *in, int32_t *out, int32_t *result, size_t n, cudaStream_t stream)

@@ -164,12 +164,14 @@ constexpr unsigned kMaxCountBlocks = 512;   // chunk totals and carries share th
 // of SP parts (dynamic shared memory), the ragged last part of the input
 // takes plain loads.  The last block writes carry[b] = kept elements of the
 // chunks before b, and *count (block_sums: one word per block).
-template <int THREADS, int SP, int NSTG>
+// GT: the predicate is values[i] > threshold (signed) and `flags` points at
+// the int32 values (parts of 2,048 bytes); otherwise flags[i] != 0.
+template <int THREADS, int SP, int NSTG, bool GT = false>
 __global__ void __launch_bounds__(THREADS, 1)
 compact_count_kernel(const uint8_t *__restrict__ flags, size_t n, unsigned parts, unsigned chunk,
                      uint32_t *__restrict__ mask, uint32_t *__restrict__ cnt, uint32_t *__restrict__ off,
                      uint32_t *__restrict__ block_sums, uint32_t *__restrict__ carry, int32_t *__restrict__ count,
-                     DevState *st)
+                     DevState *st, int32_t threshold = 0)
 {
     static_assert(THREADS >= static_cast<int>(kMaxCountBlocks), "the last block scans one chunk total per thread");
     constexpr int NW = THREADS / 32;
@@ -189,18 +191,41 @@ compact_count_kernel(const uint8_t *__restrict__ flags, size_t n, unsigned parts
         const uint32_t c = __reduce_add_sync(kFullMask, static_cast<uint32_t>(__popc(m16)));
         if (lane == 0) cnt[p] = c;
     };
-    const bool streamed = stream_parts<kPartElems, SP, NSTG>(
-        flags, p0, q1, s_ring, s_full, kCountWaitLimit, [&](unsigned p, const uint8_t *part) {
-            const uint4 q = reinterpret_cast<const uint4 *>(part)[lane];
-            part_done(p, nonzero_byte_mask(q.x) | (nonzero_byte_mask(q.y) << 4) | (nonzero_byte_mask(q.z) << 8) |
-                             (nonzero_byte_mask(q.w) << 12));
-        });
+    bool streamed;
+    if constexpr (GT) {
+        // lane L evaluates values 16 L .. 16 L + 15 of the part
+        streamed = stream_parts<kPartElems * 4, SP, NSTG>(
+            flags, p0, q1, s_ring, s_full, kCountWaitLimit, [&](unsigned p, const uint8_t *part) {
+                const uint4 *v4 = reinterpret_cast<const uint4 *>(part) + 4 * lane;
+                uint32_t m16 = 0;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 q = v4[g];
+                    m16 |= (static_cast<uint32_t>(static_cast<int32_t>(q.x) > threshold) |
+                            (static_cast<uint32_t>(static_cast<int32_t>(q.y) > threshold) << 1) |
+                            (static_cast<uint32_t>(static_cast<int32_t>(q.z) > threshold) << 2) |
+                            (static_cast<uint32_t>(static_cast<int32_t>(q.w) > threshold) << 3))
+                           << (4 * g);
+                }
+                part_done(p, m16);
+            });
+    } else {
+        streamed = stream_parts<kPartElems, SP, NSTG>(
+            flags, p0, q1, s_ring, s_full, kCountWaitLimit, [&](unsigned p, const uint8_t *part) {
+                const uint4 q = reinterpret_cast<const uint4 *>(part)[lane];
+                part_done(p, nonzero_byte_mask(q.x) | (nonzero_byte_mask(q.y) << 4) | (nonzero_byte_mask(q.z) << 8) |
+                                 (nonzero_byte_mask(q.w) << 12));
+            });
+    }
     if (!streamed && tid == 0) atomicOr(&st->error, kErrTimeout);
     for (unsigned p = q1 + warp; p < p1; p += NW) {   // the input's ragged last part
         const size_t e = static_cast<size_t>(p) * kPartElems + 16u * lane;
         uint32_t m16 = 0;
-        for (unsigned j = 0; j < 16; ++j)
-            if (e + j < n && flags[e + j] != 0) m16 |= 1u << j;
+        for (unsigned j = 0; j < 16; ++j) {
+            if (e + j >= n) break;
+            const bool keep = GT ? reinterpret_cast<const int32_t *>(flags)[e + j] > threshold : flags[e + j] != 0;
+            if (keep) m16 |= 1u << j;
+        }
         part_done(p, m16);
     }
     __syncthreads();   // every part's count written
@@ -278,34 +303,42 @@ inline unsigned count_chunk(unsigned parts, unsigned warps, int num_sms)
     return (parts + blocks - 1) / blocks;
 }
 
-// The count launch: THREADS per block, NSTG * SP * 512 bytes of stages.
-// part_words: mask[16 parts] | cnt[parts] | off[parts]; the workspace's tile
-// sums hold the chunk totals (first kMaxCountBlocks words) and carries (next).
-template <int THREADS, int SP, int NSTG>
+// The count launch: THREADS per block, NSTG * SP parts of stages (512 bytes
+// of flags or, GT, 2,048 bytes of values per part).  part_words: mask[16
+// parts] | cnt[parts] | off[parts]; the workspace's tile sums hold the chunk
+// totals (first kMaxCountBlocks words) and carries (next).
+template <int THREADS, int SP, int NSTG, bool GT = false>
 cudaError_t launch_compact_count(const uint8_t *flags, size_t n, uint32_t *part_words, int32_t *count,
-                                 unsigned chunk, const Workspace &ws, cudaStream_t s)
+                                 unsigned chunk, const Workspace &ws, cudaStream_t s, int32_t threshold = 0)
 {
     static std::atomic<unsigned long long> smem_set{0};
-    constexpr int kSmem = NSTG * SP * kPartElems;
-    auto kernel = compact_count_kernel<THREADS, SP, NSTG>;
+    constexpr int kSmem = NSTG * SP * kPartElems * (GT ? 4 : 1);
+    auto kernel = compact_count_kernel<THREADS, SP, NSTG, GT>;
     cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kernel), kSmem, smem_set);
     if (e != cudaSuccess) return e;
     const unsigned parts = static_cast<unsigned>((n + kPartElems - 1) / kPartElems);
     const unsigned blocks = (parts + chunk - 1) / chunk;
     uint32_t *mask = part_words, *cnt = part_words + static_cast<size_t>(parts) * 16, *off = cnt + parts;
     kernel<<<blocks, THREADS, kSmem, s>>>(flags, n, parts, chunk, mask, cnt, off, ws.tile_sums,
-                                          ws.tile_sums + kMaxCountBlocks, count, ws.state);
+                                          ws.tile_sums + kMaxCountBlocks, count, ws.state, threshold);
     return cudaGetLastError();
 }
 
+// The fused predicate's count launch streams the values: 32 parts (64 KB)
+// per stage, three stages.
+constexpr int kGtCountStageParts = 32, kGtCountStages = 3;
+
+// gt: keep in[i] > threshold (the count launch reads the values; flags unused)
 cudaError_t launch_compact_two_pass(const uint32_t *in, const uint8_t *flags, uint32_t *out, int32_t *count,
                                     size_t n, bool out_aligned, uint32_t *part_words, const Workspace &ws,
-                                    cudaStream_t s)
+                                    cudaStream_t s, bool gt = false, int32_t threshold = 0)
 {
     const unsigned parts = static_cast<unsigned>((n + kPartElems - 1) / kPartElems);
     const unsigned chunk = count_chunk(parts, kCountThreads / 32, ws.num_sms);
-    cudaError_t e = launch_compact_count<kCountThreads, kCountStageParts, kCountStages>(flags, n, part_words, count,
-                                                                                        chunk, ws, s);
+    cudaError_t e = gt ? launch_compact_count<kCountThreads, kGtCountStageParts, kGtCountStages, true>(
+                             reinterpret_cast<const uint8_t *>(in), n, part_words, count, chunk, ws, s, threshold)
+                       : launch_compact_count<kCountThreads, kCountStageParts, kCountStages>(flags, n, part_words,
+                                                                                           count, chunk, ws, s);
     if (e != cudaSuccess) return e;
     const uint32_t *mask = part_words, *off = part_words + static_cast<size_t>(parts) * 17;
     const uint32_t *carry = ws.tile_sums + kMaxCountBlocks;
@@ -393,12 +426,15 @@ cudaError_t set_pipeline_smem(void (*kernel)(typename P::Args, unsigned, unsigne
 }
 
 cudaError_t launch_compact_gt(const int32_t *in, int32_t threshold, int32_t *out, int32_t *count, size_t n,
-                              int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s)
+                              int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s,
+                              uint32_t *part_words)
 {
     const bool out_aligned = reinterpret_cast<uintptr_t>(out) % 16 == 0;
     const bool in_aligned = reinterpret_cast<uintptr_t>(in) % 16 == 0;
     const uint32_t *vin = reinterpret_cast<const uint32_t *>(in);
     uint32_t *vout = reinterpret_cast<uint32_t *>(out);
+    if (in_aligned && part_words != nullptr && carry == kCarryL2Resident)
+        return launch_compact_two_pass(vin, nullptr, vout, count, n, out_aligned, part_words, ws, s, true, threshold);
     const bool pipelined =
         in_aligned && (carry == kCarryPipelined || (carry != kCarryLookback && n >= kCompactPipelineMinN));
     if (pipelined) {

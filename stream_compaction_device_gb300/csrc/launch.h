@@ -115,8 +115,11 @@ cudaError_t launch_split(const uint32_t *keys, uint32_t *out, size_t n, int bit,
 
 // Compaction keeping in[i] when in[i] > threshold (signed), predicate
 // evaluated in the kernel.
+// part_words (compact_part_words(n) words, or null): the two-launch form,
+// taken in carry mode 4 for 16-byte-aligned values.
 cudaError_t launch_compact_gt(const int32_t *in, int32_t threshold, int32_t *out, int32_t *count, size_t n,
-                              int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s);
+                              int carry, const Workspace &ws, unsigned spin_limit, cudaStream_t s,
+                              uint32_t *part_words = nullptr);
 // Inclusive int32 add-scan (stored when out != nullptr) with the bracket
 // answers in result[0..1]; clears result first (stream-ordered).
 cudaError_t launch_bracket(const int32_t *in, int32_t *out, int32_t *result, size_t n, int carry,

@@ -23,7 +23,7 @@ def ds():
     return m
 
 
-@pytest.fixture(params=["lookback", "pipelined"])
+@pytest.fixture(params=["lookback", "pipelined", "l2"])
 def mode(request, ds):
     ds.set_carry_mode(request.param)
     yield request.param
@@ -88,6 +88,22 @@ def test_config_compact_gt(ds, sel):
     from stream_compaction_device_gb300 import workloads as wl
     v = wl.compaction_values()
     check_compact_gt(ds, v, wl.threshold_for(sel))
+    assert ds.device_status() == 0
+
+
+@pytest.mark.parametrize("sel", [0.0, 0.01, 0.50, 0.99, 1.0])
+def test_config_compact_gt_two_launch(ds, sel):
+    """The two-launch form (a count of every 512-element part from the
+    values, then a warp per part) on the 2^26 workload, and with nothing or
+    everything kept."""
+    from stream_compaction_device_gb300 import workloads as wl
+    v = wl.compaction_values()
+    t = {0.0: I32_MAX, 1.0: I32_MIN}.get(sel)
+    ds.set_carry_mode("l2")
+    try:
+        check_compact_gt(ds, v, wl.threshold_for(sel) if t is None else t)
+    finally:
+        ds.set_carry_mode("default")
     assert ds.device_status() == 0
 
 
