@@ -6,8 +6,8 @@
 //
 // One pass over digit p (bits 8p .. 8p+7):
 //   1. radix_hist_kernel: every tile of 8,192 keys counts its 256 digit
-//      values and stores them digit-major: hist[d * tiles + tile] (a block
-//      of 1,024 threads counts two tiles);
+//      values and stores them digit-major: hist[d * tiles + tile] (two
+//      persistent 1,024-thread blocks per SM walk the tiles);
 //   2. an exclusive add-scan of that array (the library's own scan; at 2^26
 //      keys it is 2M counts, which the L2-resident scan takes) turns it into
 //      every (digit, tile) run's first output position: all keys of smaller
@@ -20,6 +20,8 @@
 //      contiguous run.
 // Traffic: 12 bytes per key per pass (count read, scatter read and write),
 // 48 per key for the sort, against 260 for the 32 one-bit splits.
+#include <algorithm>
+
 #include "core.cuh"
 #include "launch.h"
 
@@ -59,59 +61,71 @@ __device__ __forceinline__ unsigned lanemask_lt()
 }
 
 // hist[d * tiles + tile] = number of keys of the tile whose digit is d.  The
-// count does not depend on the order, so each thread takes kHistKeys
-// consecutive keys of each of the block's kHistTiles tiles, all its 128-bit
-// loads issued before the first count; one shared counter row per
-// kHistCopyWarps warps and tile.  Measured at 2^26 keys: 61 us against 70 us
-// for one 512-thread block per tile.
-constexpr int kHistThreads = 1024, kHistTiles = 2, kHistCopyWarps = 4;
-constexpr int kHistKeys = kSortTile / kHistThreads;   // 8
-__global__ void __launch_bounds__(kHistThreads)
+// count does not depend on the order of the keys, so the loads are plain
+// coalesced 128-bit loads.  The kernel is persistent: block b counts tiles b,
+// b + G, b + 2G, ... (G blocks, two per SM), and the next tile's keys are
+// loading while the current tile is counted.  Shared-memory atomics go to one
+// row of 256 counters per four warps; two sets of rows alternate, so one
+// barrier per tile separates a tile's counting from the write-out (and
+// clearing) of the tile before it.  Measured at 2^26 keys: 51.5 us per pass
+// against 61 us for two tiles per block without the prefetch.
+constexpr int kHistThreads = 1024, kHistBlocksPerSm = 2;
+constexpr int kHistVecs = kSortTile / kHistThreads / 4;   // 16-byte loads per thread per tile (2)
+__global__ void __launch_bounds__(kHistThreads, kHistBlocksPerSm)
 radix_hist_kernel(const uint32_t *__restrict__ keys, size_t n, int shift, unsigned tiles, uint32_t *__restrict__ hist,
                   bool aligned)
 {
-    constexpr int COPIES = kHistThreads / 32 / kHistCopyWarps;
-    __shared__ uint32_t s_h[kHistTiles][COPIES][kSortBuckets];   // 16 KB
+    constexpr int COPIES = kHistThreads / 32 / 4;
+    __shared__ uint32_t s_h[2][COPIES][kSortBuckets];   // 16 KB
     const int tid = threadIdx.x, warp = tid >> 5;
-    const unsigned t0 = blockIdx.x * kHistTiles;
-    for (int i = tid; i < kHistTiles * COPIES * kSortBuckets; i += kHistThreads) (&s_h[0][0][0])[i] = 0;
-    uint4 q[kHistTiles][kHistKeys / 4];
-    bool vec[kHistTiles];
+    for (int i = tid; i < 2 * COPIES * kSortBuckets; i += kHistThreads) (&s_h[0][0][0])[i] = 0;
+    const unsigned G = gridDim.x;
+    // keys of the tile being counted (cur) and of the next one (nxt); zeros
+    // for tiles that take the scalar path or do not exist
+    uint4 cur[kHistVecs], nxt[kHistVecs];
+    auto load = [&](unsigned t, uint4 (&r)[kHistVecs]) {
+        const size_t base = static_cast<size_t>(t) * kSortTile;
+        const bool vec = t < tiles && aligned && base + kSortTile <= n;
 #pragma unroll
-    for (int t = 0; t < kHistTiles; ++t) {
-        const size_t e0 = static_cast<size_t>(t0 + t) * kSortTile + static_cast<size_t>(tid) * kHistKeys;
-        vec[t] = aligned && e0 + kHistKeys <= n;
+        for (int v = 0; v < kHistVecs; ++v)
+            r[v] = vec ? __ldcs(reinterpret_cast<const uint4 *>(keys + base) + v * kHistThreads + tid)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    };
+    load(blockIdx.x, cur);
+    __syncthreads();   // the counters are clear
+    int buf = 0;
+    for (unsigned t = blockIdx.x; t < tiles; t += G) {
+        load(t + G, nxt);
+        const size_t base = static_cast<size_t>(t) * kSortTile;
+        uint32_t *h = s_h[buf][warp / 4];
+        if (aligned && base + kSortTile <= n) {
 #pragma unroll
-        for (int v = 0; v < kHistKeys / 4; ++v)
-            q[t][v] = vec[t] ? __ldcs(reinterpret_cast<const uint4 *>(keys + e0) + v) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int t = 0; t < kHistTiles; ++t) {
-        if (t0 + t >= tiles) break;   // block-uniform
-        uint32_t *h = s_h[t][warp / kHistCopyWarps];
-        if (vec[t]) {
-#pragma unroll
-            for (int v = 0; v < kHistKeys / 4; ++v) {
-                atomicAdd(&h[digit_of(q[t][v].x, shift)], 1u);
-                atomicAdd(&h[digit_of(q[t][v].y, shift)], 1u);
-                atomicAdd(&h[digit_of(q[t][v].z, shift)], 1u);
-                atomicAdd(&h[digit_of(q[t][v].w, shift)], 1u);
+            for (int v = 0; v < kHistVecs; ++v) {
+                atomicAdd(&h[digit_of(cur[v].x, shift)], 1u);
+                atomicAdd(&h[digit_of(cur[v].y, shift)], 1u);
+                atomicAdd(&h[digit_of(cur[v].z, shift)], 1u);
+                atomicAdd(&h[digit_of(cur[v].w, shift)], 1u);
             }
-        } else {
-            const size_t e0 = static_cast<size_t>(t0 + t) * kSortTile + static_cast<size_t>(tid) * kHistKeys;
-            for (int j = 0; j < kHistKeys; ++j)
-                if (e0 + j < n) atomicAdd(&h[digit_of(keys[e0 + j], shift)], 1u);
+        } else {   // the ragged last tile, or keys that are not 16-byte aligned
+            for (int v = 0; v < kHistVecs; ++v)
+                for (int j = 0; j < 4; ++j) {
+                    const size_t e = base + static_cast<size_t>(v * kHistThreads + tid) * 4 + j;
+                    if (e < n) atomicAdd(&h[digit_of(keys[e], shift)], 1u);
+                }
         }
-    }
-    __syncthreads();
-    for (int i = tid; i < kHistTiles * kSortBuckets; i += kHistThreads) {
-        const int t = i / kSortBuckets, d = i % kSortBuckets;
-        if (t0 + t >= tiles) continue;
-        uint32_t c = 0;
 #pragma unroll
-        for (int w = 0; w < COPIES; ++w) c += s_h[t][w][d];
-        hist[static_cast<size_t>(d) * tiles + t0 + t] = c;
+        for (int v = 0; v < kHistVecs; ++v) cur[v] = nxt[v];
+        __syncthreads();   // tile t counted; the other set was written out and cleared before this barrier
+        if (tid < kSortBuckets) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int w = 0; w < COPIES; ++w) {
+                c += s_h[buf][w][tid];
+                s_h[buf][w][tid] = 0;
+            }
+            hist[static_cast<size_t>(tid) * tiles + t] = c;
+        }
+        buf ^= 1;
     }
 }
 
@@ -244,8 +258,8 @@ cudaError_t launch_radix_pass(const uint32_t *src, uint32_t *dst, size_t n, int 
     const unsigned tiles = tiles_for(n, kSortTile);
     const int shift = kRadixDigitBits * pass;
     const bool aligned = reinterpret_cast<uintptr_t>(src) % 16 == 0;
-    radix_hist_kernel<<<(tiles + kHistTiles - 1) / kHistTiles, kHistThreads, 0, s>>>(src, n, shift, tiles, hist,
-                                                                                      aligned);
+    const unsigned hist_blocks = std::min(tiles, static_cast<unsigned>(kHistBlocksPerSm * ws.num_sms));
+    radix_hist_kernel<<<hist_blocks, kHistThreads, 0, s>>>(src, n, shift, tiles, hist, aligned);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = launch_scan(ElemType::U32, kOpAdd, false, hist, hist, static_cast<size_t>(tiles) * kSortBuckets,
