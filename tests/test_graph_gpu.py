@@ -1,8 +1,10 @@
 """The library's calls inside a CUDA graph: after one warm-up on the
 capturing stream (which sets up that stream's workspace and scratch), a
 capture of scans (cluster, L2-resident and pipelined sizes), the two-launch
-compaction, the standalone split and the 32-pass sort replays with new
-inputs and matches the CPU oracle each time.  The kernels keep their
+compaction, the standalone split, the 32-pass sort, the 8-bit digit sort and
+one shard's calls of the sharded scan (its fold, the fold of the gathered
+totals, its scan from that carry) replays with new inputs and matches the
+CPU oracle each time.  The kernels keep their
 look-back tags, tickets and arrival counters in device memory, so a replay
 needs no host-side state."""
 import numpy as np
@@ -44,6 +46,9 @@ def test_graph_capture_and_replay(ds):
     ys, ym, yb = torch.empty_like(xs), torch.empty_like(xm), torch.empty_like(xb)
     out, cnt = torch.empty_like(v), torch.empty(1, dtype=torch.int32, device="cuda")
     ko, work, tmp = torch.empty_like(k), torch.empty_like(k), torch.empty_like(k)
+    work2 = torch.empty_like(k)
+    totals = torch.empty(3, dtype=torch.int32, device="cuda")
+    carry, ysh = torch.empty(1, dtype=torch.int32, device="cuda"), torch.empty_like(xs)
 
     def run():
         ds.scan_exclusive(xs, ys)                       # one thread-block cluster
@@ -53,6 +58,12 @@ def test_graph_capture_and_replay(ds):
         ds.split_bit(k, 9, out=ko)
         work.copy_(k)
         ds.radix_sort(work, tmp)
+        work2.copy_(k)
+        ds.radix_sort_digits(work2, tmp)
+        # shard 2 of 3 of an array whose other shards' totals sit in totals[0:2]
+        ds.reduce(xs, out=totals[2:3])
+        ds.reduce(totals[:2], out=carry)
+        ds.scan_inclusive_carry(xs, carry, ysh)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -69,6 +80,8 @@ def test_graph_capture_and_replay(ds):
         for dst, src in ((xs, h["xs"]), (xm, h["xm"]), (xb, h["xb"]), (v, h["v"]), (k, h["k"])):
             dst.copy_(to_dev(src))
         f.copy_(torch.from_numpy(h["f"]).cuda())
+        t01 = rng.integers(-10**6, 10**6, 2, dtype=np.int32)
+        totals[:2].copy_(torch.from_numpy(t01).cuda())
         torch.cuda.synchronize()
         g.replay()
         torch.cuda.synchronize()
@@ -82,5 +95,9 @@ def test_graph_capture_and_replay(ds):
         assert kk == ref_c.size and np.array_equal(out[:kk].cpu().numpy(), ref_c)
         assert np.array_equal(from_dev(ko, np.uint32), oracle.split_bit(h["k"], 9)[0])
         assert np.array_equal(from_dev(work, np.uint32), np.sort(h["k"]))
+        assert np.array_equal(from_dev(work2, np.uint32), np.sort(h["k"]))
+        assert int(totals[2].item()) == int(oracle.scan(h["xs"], "add", True)[-1])
+        shard = oracle.scan(np.concatenate([t01, h["xs"]]), "add", True)[2:]
+        assert np.array_equal(ysh.cpu().numpy(), shard)
     assert ds.device_status(s) == 0
     ds.stream_release(s)

@@ -169,3 +169,20 @@ def test_sharded_scan_single_process(ds):
     x = wl.random_input(np.int32, 300_001, 9, "add")
     got = from_dev(ds.sharded_scan(to_dev(x), inclusive=True), np.int32)
     assert np.array_equal(got, oracle.scan(x, "add", True))
+
+
+def test_sharded_scan_through_a_one_rank_nccl_group(ds, tmp_path):
+    """exchange_totals and sharded_scan through torch.distributed with NCCL
+    (one rank: every call of this run has one GPU), against the oracle."""
+    import torch.distributed as dist
+    from stream_compaction_device_gb300 import workloads as wl
+    dist.init_process_group("nccl", init_method=f"file://{tmp_path / 'store'}", rank=0, world_size=1)
+    try:
+        t = torch.tensor([42], dtype=torch.int32, device="cuda")
+        assert ds.exchange_totals(t).tolist() == [42]
+        for op in ("add", "max", "xor"):
+            x = wl.random_input(np.int32, 1_000_003, 17, op)
+            got = from_dev(ds.sharded_scan(to_dev(x), op=op), np.int32)
+            assert np.array_equal(got, oracle.scan(x, op, False)), op
+    finally:
+        dist.destroy_process_group()
