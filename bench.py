@@ -9,8 +9,9 @@ is needed between steps.  Prints one JSON line:
   value      whole-job Gelem/s (all ranks' elements / max-over-ranks time)
   roofline   the scan kernel's algorithmic bytes (2 * N * 4 per launch) over
              its CUDA-event duration, against the measured HBM copy peak
-  e2e        the same scan from pinned host memory through scan_host:
-             host-to-device copy, scan, device-to-host copy of the result,
+  e2e        the same scan from pinned host memory through the library's
+             host entry (scan_exclusive_host_i32: host-to-device copy, scan,
+             device-to-host copy of the result, all queued by the library),
              every step; steps alternate between two streams, so one step's
              download overlaps the next one's upload
   cpu_baseline  the serial CPU oracle on the host cores (1 thread)

@@ -86,6 +86,47 @@ devscan_status scan_exclusive_f32(const float *in, float *out, size_t n,
                                   devscan_op op, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Scans of host arrays: the host-side entry to the scans above, for callers
+ * whose data lives in host memory (P2 section 5.3: the copies and the scan
+ * are ordered on a CUDA stream, so work on two streams overlaps one's
+ * transfers with the other's; the scan itself is P1 section 一).  In order on
+ * `stream`:
+ *   1. h_in[0 .. n) is copied into d_in (host to device);
+ *   2. d_in is scanned into d_out by the device scan above (same operators,
+ *      identities, paths and accuracy);
+ *   3. d_out is copied into h_out[0 .. n) (device to host).
+ * The call returns once the three steps are queued; h_out holds the result
+ * when the stream has reached this point (synchronise the stream, or record
+ * an event after the call).
+ *
+ *   h_in, h_out : host arrays of n elements; they may be the same array.
+ *                 Page-locked (pinned) memory makes the copies asynchronous;
+ *                 with pageable memory CUDA stages them and they are slower.
+ *                 The caller keeps both valid and untouched until the
+ *                 stream has reached this point.
+ *   d_in, d_out : device arrays of n elements owned by the caller (the call
+ *                 allocates no array of n elements); d_out may equal d_in;
+ *                 otherwise they must not overlap (DEVSCAN_ERR_INVALID).
+ *                 16-byte aligned buffers take the vectorised paths.
+ * Other arguments and errors as the scans; a failed copy returns
+ * DEVSCAN_ERR_CUDA.  Traffic: n * sizeof(T) bytes over the host link in each
+ * direction, plus the scan's 2 * n * sizeof(T) bytes of device memory.
+ * Calls on two streams overlap one call's download with the other's upload.
+ * ------------------------------------------------------------------------- */
+devscan_status scan_inclusive_host_i32(const int32_t *h_in, int32_t *h_out, size_t n, devscan_op op,
+                                       int32_t *d_in, int32_t *d_out, cudaStream_t stream);
+devscan_status scan_inclusive_host_u32(const uint32_t *h_in, uint32_t *h_out, size_t n, devscan_op op,
+                                       uint32_t *d_in, uint32_t *d_out, cudaStream_t stream);
+devscan_status scan_inclusive_host_f32(const float *h_in, float *h_out, size_t n, devscan_op op,
+                                       float *d_in, float *d_out, cudaStream_t stream);
+devscan_status scan_exclusive_host_i32(const int32_t *h_in, int32_t *h_out, size_t n, devscan_op op,
+                                       int32_t *d_in, int32_t *d_out, cudaStream_t stream);
+devscan_status scan_exclusive_host_u32(const uint32_t *h_in, uint32_t *h_out, size_t n, devscan_op op,
+                                       uint32_t *d_in, uint32_t *d_out, cudaStream_t stream);
+devscan_status scan_exclusive_host_f32(const float *h_in, float *h_out, size_t n, devscan_op op,
+                                       float *d_in, float *d_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Scans with a carry-in, and the fold of an array: the pieces of a scan whose
  * input is split into contiguous shards, one per device (P1 section 四 and
  * P2 section 3.2: reduce each part, scan the part totals, give every part

@@ -4,8 +4,8 @@ radix one-bit split as hand-written sm_103a CUDA kernels behind a C ABI.
 The functions below take CUDA tensors (PyTorch is used for device memory
 and streams only), pass their device pointers and the current CUDA stream
 to ``libdevscan.so`` and return.  All work is asynchronous on that stream.
-``scan_host`` is the one host-buffer entry: it copies a pinned host array
-to the device, scans it and copies the result back.
+``scan_host`` is the host-buffer entry: the library copies a pinned host
+array to the device, scans it and copies the result back.
 """
 from __future__ import annotations
 
@@ -293,28 +293,40 @@ def radix_sort_digits(keys: torch.Tensor, tmp: torch.Tensor | None = None, strea
 
 def scan_host(x_host: torch.Tensor, inclusive: bool = False, op: str = "add", device="cuda",
               stream=None, out_host: torch.Tensor | None = None, work=None,
-              synchronize: bool = True) -> torch.Tensor:
-    """Scan a host array end to end: host-to-device copy, device scan,
-    device-to-host copy, all ordered on ``stream``.  Pinned host tensors make
-    the copies asynchronous.  ``work`` may pass preallocated (device input,
-    device output) tensors.  With ``synchronize`` (the default) it returns
-    once the result is in ``out_host``; without, it returns at once and the
-    result is there when ``stream`` has reached this point, so calls on two
-    streams overlap one call's download with the next one's upload."""
+              synchronize: bool = True, as_uint32: bool = False) -> torch.Tensor:
+    """Scan a host array end to end through the library's host entry
+    (``scan_{inclusive,exclusive}_host_T``): host-to-device copy, device
+    scan, device-to-host copy, all queued by the library on ``stream``.
+    Pinned host tensors make the copies asynchronous.  ``work`` may pass
+    preallocated (device input, device output) tensors.  With
+    ``synchronize`` (the default) it returns once the result is in
+    ``out_host``; without, it returns at once and the result is there when
+    ``stream`` has reached this point, so calls on two streams overlap one
+    call's download with the next one's upload."""
     if x_host.is_cuda:
         raise ValueError("x_host must be a host tensor")
+    if not x_host.is_contiguous():
+        raise ValueError("x_host must be contiguous")
+    suffix = "u32" if as_uint32 else _SUFFIX.get(x_host.dtype)
+    if suffix is None:
+        raise TypeError(f"unsupported dtype {x_host.dtype} (int32, uint32, float32)")
     s = stream if stream is not None else torch.cuda.current_stream()
-    with torch.cuda.stream(s):
-        if work is None:
-            d_in = torch.empty(x_host.shape, dtype=x_host.dtype, device=device)
-            d_out = torch.empty_like(d_in)
-        else:
-            d_in, d_out = work
-        d_in.copy_(x_host, non_blocking=True)
-        (scan_inclusive if inclusive else scan_exclusive)(d_in, d_out, op=op, stream=s)
-        if out_host is None:
-            out_host = torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=x_host.is_pinned())
-        out_host.copy_(d_out, non_blocking=True)
+    if work is None:
+        d_in = torch.empty(x_host.shape, dtype=x_host.dtype, device=device)
+        d_out = torch.empty_like(d_in)
+    else:
+        d_in, d_out = work
+        _check_cuda(d_in, "work[0]")
+        _check_cuda(d_out, "work[1]")
+        if d_in.numel() < x_host.numel() or d_out.numel() < x_host.numel():
+            raise ValueError("work tensors are smaller than x_host")
+    if out_host is None:
+        out_host = torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=x_host.is_pinned())
+    if out_host.is_cuda or out_host.numel() != x_host.numel() or out_host.dtype != x_host.dtype:
+        raise ValueError("out_host must be a host tensor matching x_host")
+    name = f"scan_{'inclusive' if inclusive else 'exclusive'}_host_{suffix}"
+    _lib.check(getattr(load(), name)(x_host.data_ptr(), out_host.data_ptr(), x_host.numel(), OPS[op],
+                                     d_in.data_ptr(), d_out.data_ptr(), _stream_handle(s)), name)
     if synchronize:
         s.synchronize()
     return out_host

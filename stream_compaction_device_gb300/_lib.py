@@ -19,6 +19,7 @@ STATUS = {0: "DEVSCAN_OK", 1: "DEVSCAN_ERR_INVALID", 2: "DEVSCAN_ERR_UNSUPPORTED
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NOMEM = range(6)
 
 SCAN_SYMBOLS = [f"scan_{d}_{t}" for d in ("inclusive", "exclusive") for t in ("i32", "u32", "f32")]
+HOST_SCAN_SYMBOLS = tuple(f"scan_{d}_host_{t}" for d in ("inclusive", "exclusive") for t in ("i32", "u32", "f32"))
 CARRY_SCAN_SYMBOLS = tuple(f"scan_{d}_carry_{t}" for d in ("inclusive", "exclusive") for t in ("i32", "u32", "f32"))
 REDUCE_SYMBOLS = ("reduce_i32", "reduce_u32", "reduce_f32")
 SEGSCAN_SYMBOLS = tuple(f"segmented_scan_{d}_{t}" for d in ("inclusive", "exclusive")
@@ -49,6 +50,10 @@ def load() -> ctypes.CDLL:
         for name in SCAN_SYMBOLS:
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, sz, i, vp]
+            fn.restype = i
+        for name in HOST_SCAN_SYMBOLS:
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, sz, i, vp, vp, vp]
             fn.restype = i
         for name in CARRY_SCAN_SYMBOLS:
             fn = getattr(lib, name)

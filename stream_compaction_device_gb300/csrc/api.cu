@@ -161,6 +161,25 @@ devscan_status scan_common(ElemType type, bool inclusive, const void *in, void *
                                  kSpinLimit, stream, carry_in));
 }
 
+// Host arrays in, host array out: the input is copied into the caller's
+// device buffer, scanned there into the second device buffer, and the result
+// copied back, all ordered on `stream`.
+devscan_status scan_host_common(ElemType type, bool inclusive, const void *h_in, void *h_out, size_t n,
+                                devscan_op op, void *d_in, void *d_out, cudaStream_t stream)
+{
+    if (op != DEVSCAN_OP_ADD && op != DEVSCAN_OP_MAX && op != DEVSCAN_OP_XOR) return DEVSCAN_ERR_INVALID;
+    if (type == ElemType::F32 && op == DEVSCAN_OP_XOR) return DEVSCAN_ERR_UNSUPPORTED;
+    if (n == 0) return DEVSCAN_OK;
+    if (h_in == nullptr || h_out == nullptr || d_in == nullptr || d_out == nullptr) return DEVSCAN_ERR_INVALID;
+    if (n > kMaxScanN) return DEVSCAN_ERR_INVALID;
+    const size_t bytes = n * 4;
+    if (overlaps(d_in, bytes, d_out, bytes) && d_in != d_out) return DEVSCAN_ERR_INVALID;
+    if (cudaMemcpyAsync(d_in, h_in, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return DEVSCAN_ERR_CUDA;
+    const devscan_status st = scan_common(type, inclusive, d_in, d_out, n, op, stream);
+    if (st != DEVSCAN_OK) return st;
+    return from_cuda(cudaMemcpyAsync(h_out, d_out, bytes, cudaMemcpyDeviceToHost, stream));
+}
+
 devscan_status reduce_common(ElemType type, const void *in, size_t n, devscan_op op, void *total,
                              cudaStream_t stream)
 {
@@ -255,6 +274,37 @@ devscan_status scan_exclusive_carry_f32(const float *in, float *out, size_t n, d
                                         cudaStream_t stream)
 {
     return scan_common(ElemType::F32, false, in, out, n, op, stream, carry_in);
+}
+
+devscan_status scan_inclusive_host_i32(const int32_t *h_in, int32_t *h_out, size_t n, devscan_op op, int32_t *d_in,
+                                       int32_t *d_out, cudaStream_t stream)
+{
+    return scan_host_common(ElemType::I32, true, h_in, h_out, n, op, d_in, d_out, stream);
+}
+devscan_status scan_inclusive_host_u32(const uint32_t *h_in, uint32_t *h_out, size_t n, devscan_op op,
+                                       uint32_t *d_in, uint32_t *d_out, cudaStream_t stream)
+{
+    return scan_host_common(ElemType::U32, true, h_in, h_out, n, op, d_in, d_out, stream);
+}
+devscan_status scan_inclusive_host_f32(const float *h_in, float *h_out, size_t n, devscan_op op, float *d_in,
+                                       float *d_out, cudaStream_t stream)
+{
+    return scan_host_common(ElemType::F32, true, h_in, h_out, n, op, d_in, d_out, stream);
+}
+devscan_status scan_exclusive_host_i32(const int32_t *h_in, int32_t *h_out, size_t n, devscan_op op, int32_t *d_in,
+                                       int32_t *d_out, cudaStream_t stream)
+{
+    return scan_host_common(ElemType::I32, false, h_in, h_out, n, op, d_in, d_out, stream);
+}
+devscan_status scan_exclusive_host_u32(const uint32_t *h_in, uint32_t *h_out, size_t n, devscan_op op,
+                                       uint32_t *d_in, uint32_t *d_out, cudaStream_t stream)
+{
+    return scan_host_common(ElemType::U32, false, h_in, h_out, n, op, d_in, d_out, stream);
+}
+devscan_status scan_exclusive_host_f32(const float *h_in, float *h_out, size_t n, devscan_op op, float *d_in,
+                                       float *d_out, cudaStream_t stream)
+{
+    return scan_host_common(ElemType::F32, false, h_in, h_out, n, op, d_in, d_out, stream);
 }
 
 devscan_status reduce_i32(const int32_t *in, size_t n, devscan_op op, int32_t *total, cudaStream_t stream)

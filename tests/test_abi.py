@@ -79,6 +79,12 @@ def test_validation_without_device_work(lib):
     assert lib.split_bit_u32(None, None, 3, 0, None) == OK
     assert lib.radix_sort_u32(fake, fake, 10, None) == ERR_INVALID
     assert lib.radix_sort_u32(None, None, 0, None) == OK
+    for name in ("scan_inclusive_host_i32", "scan_exclusive_host_f32"):
+        fn = getattr(lib, name)
+        assert fn(None, fake, 10, 0, fake, ctypes.c_void_p(1 << 20), None) == ERR_INVALID   # null host input
+        assert fn(fake, fake, 10, 0, fake, ctypes.c_void_p(4096 + 8), None) == ERR_INVALID  # device buffers overlap
+        assert fn(None, None, 0, 0, None, None, None) == OK                                # n == 0
+    assert lib.scan_inclusive_host_f32(fake, fake, 10, 2, fake, fake, None) == ERR_UNSUPPORTED
     assert lib.devscan_measure_set_carry_mode(9) == ERR_INVALID
     assert lib.devscan_measure_set_carry_mode(0) == OK
     assert lib.devscan_selftest_stalled_wait(0, None) == ERR_INVALID

@@ -214,3 +214,35 @@ def test_config_sweep_xor(ds):
     from stream_compaction_device_gb300 import workloads as wl
     x = wl.xor_values()
     assert np.array_equal(gpu_scan(ds, x, "xor", True), oracle.scan(x, "xor", True))
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_entry(ds, pinned):
+    """scan_{inclusive,exclusive}_host_T: host array in, host array out, the
+    copies and the scan queued by the library on one stream; in place on
+    the host and on the device too."""
+    from stream_compaction_device_gb300 import workloads as wl
+    for dtype, op in CASES:
+        for n in (1, 4097, 1_000_003):
+            x = wl.random_input(dtype, n, n + 5, op)
+            hx = torch.from_numpy(x.view(np.int32) if dtype == np.uint32 else x)
+            if pinned:
+                hx = hx.pin_memory()
+            for inclusive in (True, False):
+                got = ds.scan_host(hx, inclusive=inclusive, op=op, as_uint32=dtype == np.uint32).numpy()
+                got = got.view(np.uint32) if dtype == np.uint32 else got
+                ref = oracle.scan(x, op, inclusive)
+                if dtype == np.float32 and op == "add":
+                    assert_f32_within(got, ref, oracle.abs_prefix(x), f"host n={n}")
+                elif dtype == np.float32:
+                    assert np.array_equal(got.astype(np.float64), ref)
+                else:
+                    assert np.array_equal(got, ref), (dtype, op, n, inclusive)
+    # in place: one host array, one device buffer
+    x = wl.random_input(np.int32, 300_001, 3, "add")
+    h = torch.from_numpy(x.copy())
+    if pinned:
+        h = h.pin_memory()
+    d = torch.empty(x.size, dtype=torch.int32, device="cuda")
+    ds.scan_host(h, inclusive=False, out_host=h, work=(d, d))
+    assert np.array_equal(h.numpy(), oracle.scan(x, "add", False))
