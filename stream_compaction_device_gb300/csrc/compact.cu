@@ -154,6 +154,7 @@ compact_kernel(const uint32_t *__restrict__ in, const uint8_t *__restrict__ flag
 constexpr int kPartElems = 512;
 constexpr unsigned kSparseKept = 32;
 constexpr int kCountThreads = 1024, kCountStageParts = 128, kCountStages = 3, kWriteWarps = 8, kWriteMinBlocks = 1;
+constexpr int kWritePartsPerWarp = 4;
 constexpr unsigned kCountWaitLimit = 1u << 18;
 constexpr unsigned kMaxCountBlocks = 512;   // chunk totals and carries share the workspace's tile sums
 
@@ -164,14 +165,38 @@ constexpr unsigned kMaxCountBlocks = 512;   // chunk totals and carries share th
 // of SP parts (dynamic shared memory), the ragged last part of the input
 // takes plain loads.  The last block writes carry[b] = kept elements of the
 // chunks before b, and *count (block_sums: one word per block).
-// GT: the predicate is values[i] > threshold (signed) and `flags` points at
-// the int32 values (parts of 2,048 bytes); otherwise flags[i] != 0.
-template <int THREADS, int SP, int NSTG, bool GT = false>
+// The parts' offsets within the block's chunk [p0, p1), THREADS parts at a
+// time: off[p] = counts of the chunk's parts before p.  Then the last block
+// to arrive writes carry[b] = counts of the chunks before b for every block
+// b, and *count.  Called by every thread of every block, after the block's
+// counts are written.
+template <int THREADS>
+__device__ void chunk_offsets(const uint32_t *__restrict__ cnt, uint32_t *__restrict__ off, unsigned p0, unsigned p1,
+                              uint32_t *__restrict__ block_sums, uint32_t *__restrict__ carry, int32_t *count,
+                              DevState *st, uint32_t *s_w)
+{
+    const int tid = threadIdx.x;
+    uint32_t run = 0;
+    for (unsigned base = p0; base < p1; base += THREADS) {
+        const unsigned p = base + tid;
+        const uint32_t c = p < p1 ? cnt[p] : 0u;
+        uint32_t total;
+        const uint32_t excl = block_excl_scan<THREADS>(c, s_w, tid, total);
+        if (p < p1) off[p] = run + excl;
+        run += total;
+        __syncthreads();   // s_w is read before the next round writes it
+    }
+    uint32_t all;
+    if (last_block_carries<THREADS>(run, block_sums, carry, st, s_w, all) && tid == 0)
+        *count = static_cast<int32_t>(all);
+}
+
+template <int THREADS, int SP, int NSTG>
 __global__ void __launch_bounds__(THREADS, 1)
 compact_count_kernel(const uint8_t *__restrict__ flags, size_t n, unsigned parts, unsigned chunk,
                      uint32_t *__restrict__ mask, uint32_t *__restrict__ cnt, uint32_t *__restrict__ off,
                      uint32_t *__restrict__ block_sums, uint32_t *__restrict__ carry, int32_t *__restrict__ count,
-                     DevState *st, int32_t threshold = 0)
+                     DevState *st)
 {
     static_assert(THREADS >= static_cast<int>(kMaxCountBlocks), "the last block scans one chunk total per thread");
     constexpr int NW = THREADS / 32;
@@ -191,104 +216,203 @@ compact_count_kernel(const uint8_t *__restrict__ flags, size_t n, unsigned parts
         const uint32_t c = __reduce_add_sync(kFullMask, static_cast<uint32_t>(__popc(m16)));
         if (lane == 0) cnt[p] = c;
     };
-    bool streamed;
-    if constexpr (GT) {
-        // lane L evaluates values 16 L .. 16 L + 15 of the part
-        streamed = stream_parts<kPartElems * 4, SP, NSTG>(
-            flags, p0, q1, s_ring, s_full, kCountWaitLimit, [&](unsigned p, const uint8_t *part) {
-                const uint4 *v4 = reinterpret_cast<const uint4 *>(part) + 4 * lane;
-                uint32_t m16 = 0;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint4 q = v4[g];
-                    m16 |= (static_cast<uint32_t>(static_cast<int32_t>(q.x) > threshold) |
-                            (static_cast<uint32_t>(static_cast<int32_t>(q.y) > threshold) << 1) |
-                            (static_cast<uint32_t>(static_cast<int32_t>(q.z) > threshold) << 2) |
-                            (static_cast<uint32_t>(static_cast<int32_t>(q.w) > threshold) << 3))
-                           << (4 * g);
-                }
-                part_done(p, m16);
-            });
-    } else {
-        streamed = stream_parts<kPartElems, SP, NSTG>(
-            flags, p0, q1, s_ring, s_full, kCountWaitLimit, [&](unsigned p, const uint8_t *part) {
-                const uint4 q = reinterpret_cast<const uint4 *>(part)[lane];
-                part_done(p, nonzero_byte_mask(q.x) | (nonzero_byte_mask(q.y) << 4) | (nonzero_byte_mask(q.z) << 8) |
-                                 (nonzero_byte_mask(q.w) << 12));
-            });
-    }
+    const bool streamed = stream_parts<kPartElems, SP, NSTG>(
+        flags, p0, q1, s_ring, s_full, kCountWaitLimit, [&](unsigned p, const uint8_t *part) {
+            const uint4 q = reinterpret_cast<const uint4 *>(part)[lane];
+            part_done(p, nonzero_byte_mask(q.x) | (nonzero_byte_mask(q.y) << 4) | (nonzero_byte_mask(q.z) << 8) |
+                             (nonzero_byte_mask(q.w) << 12));
+        });
     if (!streamed && tid == 0) atomicOr(&st->error, kErrTimeout);
     for (unsigned p = q1 + warp; p < p1; p += NW) {   // the input's ragged last part
         const size_t e = static_cast<size_t>(p) * kPartElems + 16u * lane;
         uint32_t m16 = 0;
-        for (unsigned j = 0; j < 16; ++j) {
-            if (e + j >= n) break;
-            const bool keep = GT ? reinterpret_cast<const int32_t *>(flags)[e + j] > threshold : flags[e + j] != 0;
-            if (keep) m16 |= 1u << j;
-        }
+        for (unsigned j = 0; j < 16; ++j)
+            if (e + j < n && flags[e + j] != 0) m16 |= 1u << j;
         part_done(p, m16);
     }
     __syncthreads();   // every part's count written
 
-    // phase 2: the parts' offsets within the chunk, THREADS parts at a time
-    uint32_t run = 0;
-    for (unsigned base = p0; base < p1; base += THREADS) {
-        const unsigned p = base + tid;
-        const uint32_t c = p < p1 ? cnt[p] : 0u;
-        uint32_t total;
-        const uint32_t excl = block_excl_scan<THREADS>(c, s_w, tid, total);
-        if (p < p1) off[p] = run + excl;
-        run += total;
-        __syncthreads();   // s_w is read before the next round writes it
-    }
-    uint32_t all;
-    if (last_block_carries<THREADS>(run, block_sums, carry, st, s_w, all) && tid == 0)
-        *count = static_cast<int32_t>(all);
+    // phase 2: the parts' offsets within the chunk; the last block's carries
+    chunk_offsets<THREADS>(cnt, off, p0, p1, block_sums, carry, count, st, s_w);
 }
 
-// Warp w of block b writes part b * kWriteWarps + w.  Lane L's row q holds
-// elements 128 q + 4 L .. + 3 of the part: mask word 4 q + L / 8, bits
-// 4 (L % 8) .. + 3.  The part's kept count comes from its mask, so the mask,
-// offset and carry loads go out together and the values follow them.
+// The fused predicate's count launch: keep values[i] > threshold (signed).
+// Block b takes the chunk of parts [b * chunk, (b + 1) * chunk); warp w takes
+// its parts w, w + NW, ... two at a time, so each lane has eight 128-bit
+// loads in flight (their lines marked to stay in L2, where the write launch's
+// dense parts find them).  In a part, lane L reads the 16-byte chunks L,
+// L + 32, L + 64 and L + 96: row q gives it the 4-bit keep mask of elements
+// 128 q + 4 L .. + 3, which lies in the part's mask word 4 q + L / 8 at bit
+// 4 (L % 8); an OR over the 8 lanes of each group gathers the word.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 1)
+compact_gt_count_kernel(const uint32_t *__restrict__ in, int32_t threshold, size_t n, unsigned parts,
+                        unsigned chunk, uint32_t *__restrict__ mask, uint32_t *__restrict__ cnt,
+                        uint32_t *__restrict__ off, uint32_t *__restrict__ block_sums, uint32_t *__restrict__ carry,
+                        int32_t *__restrict__ count, DevState *st)
+{
+    static_assert(THREADS >= static_cast<int>(kMaxCountBlocks), "the last block scans one chunk total per thread");
+    constexpr int NW = THREADS / 32;
+    __shared__ uint32_t s_w[NW];
+    allow_dependent_launch();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned p0 = blockIdx.x * chunk, p1 = p0 + chunk < parts ? p0 + chunk : parts;
+    const unsigned whole = static_cast<unsigned>(n / kPartElems);
+    const unsigned q1 = p1 < whole ? p1 : (p0 > whole ? p0 : whole);   // [p0, q1): whole parts
+    const uint64_t keep_pol = policy_evict_last();
+
+    auto load_part = [&](unsigned p, uint4 (&v)[4]) {
+        const uint4 *v4 = reinterpret_cast<const uint4 *>(in + static_cast<size_t>(p) * kPartElems);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = ld_keep(v4 + q * 32 + lane, keep_pol);
+    };
+    auto nibbles = [&](const uint4 (&v)[4], uint32_t (&nib)[4]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) nib[q] = greater_mask(v[q].x, v[q].y, v[q].z, v[q].w, threshold);
+    };
+    auto part_done = [&](unsigned p, const uint32_t (&nib)[4]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t w = nib[q] << (4 * (lane & 7));
+            w |= __shfl_xor_sync(kFullMask, w, 1);
+            w |= __shfl_xor_sync(kFullMask, w, 2);
+            w |= __shfl_xor_sync(kFullMask, w, 4);
+            if ((lane & 7) == 0) mask[static_cast<size_t>(p) * 16 + 4 * q + (lane >> 3)] = w;
+        }
+        const uint32_t c = __reduce_add_sync(
+            kFullMask, static_cast<uint32_t>(__popc(nib[0] | (nib[1] << 4) | (nib[2] << 8) | (nib[3] << 12))));
+        if (lane == 0) cnt[p] = c;
+    };
+    unsigned p = p0 + warp;
+    for (; p + NW < q1; p += 2 * NW) {   // two whole parts per round
+        uint4 a[4], b[4];
+        load_part(p, a);
+        load_part(p + NW, b);
+        uint32_t na[4], nb[4];
+        nibbles(a, na);
+        nibbles(b, nb);
+        part_done(p, na);
+        part_done(p + NW, nb);
+    }
+    for (; p < q1; p += NW) {
+        uint4 a[4];
+        load_part(p, a);
+        uint32_t na[4];
+        nibbles(a, na);
+        part_done(p, na);
+    }
+    for (p = q1 + warp; p < p1; p += NW) {   // the input's ragged last part
+        const size_t base = static_cast<size_t>(p) * kPartElems;
+        uint32_t na[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const size_t e = base + static_cast<size_t>((q * 32 + lane) * 4 + j);
+                if (e < n && static_cast<int32_t>(in[e]) > threshold) m |= 1u << j;
+            }
+            na[q] = m;
+        }
+        part_done(p, na);
+    }
+    __syncthreads();   // every part's count written
+
+    chunk_offsets<THREADS>(cnt, off, p0, p1, block_sums, carry, count, st, s_w);
+}
+
+// Warp w of block b writes the kWritePartsPerWarp consecutive parts from
+// (b * kWriteWarps + w) * kWritePartsPerWarp.  Lanes 0 .. 15 take the 16 mask
+// words of each part (bit i of word w: element 32 w + i), and each part's
+// output offset is its offset within its chunk plus the chunk's carry.
+//   - A part that keeps at most kSparseKept elements takes the sparse path:
+//     its kept indices are listed in order in shared memory, lane i loads the
+//     i-th kept value and stores it at the part's offset + i.  The loads of
+//     all the warp's sparse parts are in flight together, so at low
+//     selectivity a part costs one round trip to its values after its mask,
+//     shared with the warp's other parts.
+//   - A denser part loads all its values (lane L, row q: elements
+//     128 q + 4 L .. + 3, whose keep bits are the nibble of mask word
+//     4 q + L / 8), ranks them, stages them in phase with their destination
+//     and writes one run (compact_write_warp); those parts go one after
+//     another.
 template <bool OUT_ALIGNED, int MIN_BLOCKS>
 __global__ void __launch_bounds__(kWriteWarps * 32, MIN_BLOCKS)
 compact_write_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, size_t n, unsigned parts,
                      unsigned chunk, const uint32_t *__restrict__ mask, const uint32_t *__restrict__ off,
                      const uint32_t *__restrict__ carry)
 {
+    constexpr int PPW = kWritePartsPerWarp;
     __shared__ __align__(16) uint32_t s_stage[kWriteWarps][kPartElems + 4];
+    __shared__ uint16_t s_list[kWriteWarps][PPW][kSparseKept];
     wait_primary_grid();   // the count launch's masks, offsets and carries
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned p = blockIdx.x * kWriteWarps + warp;
-    if (p >= parts) return;   // the whole warp: no barrier follows
-    const uint32_t *mw = mask + static_cast<size_t>(p) * 16;
-    uint32_t x[4][4], keep[4];
+    const unsigned p0 = (blockIdx.x * kWriteWarps + warp) * PPW;
+    if (p0 >= parts) return;   // the whole warp: no block barrier follows
+    uint32_t word[PPW], o[PPW], c[PPW];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) keep[q] = (mw[4 * q + (lane >> 3)] >> (4 * (lane & 7))) & 0xfu;
-    const uint32_t o = off[p] + carry[p / chunk];
-    const uint32_t c = __reduce_add_sync(kFullMask, static_cast<uint32_t>(__popc(keep[0] | (keep[1] << 4) |
-                                                                                   (keep[2] << 8) | (keep[3] << 12))));
-    if (c == 0) return;
-    const size_t b = static_cast<size_t>(p) * kPartElems;
-    if (b + kPartElems <= n) {
-        const uint4 *v4 = reinterpret_cast<const uint4 *>(in + b);
+    for (int k = 0; k < PPW; ++k) {
+        const unsigned p = p0 + k;
+        word[k] = (p < parts && lane < 16) ? mask[static_cast<size_t>(p) * 16 + lane] : 0u;
+        o[k] = p < parts ? off[p] + carry[p / chunk] : 0u;
+    }
+    // counts, and the sparse parts' kept indices in order
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 u = make_uint4(0u, 0u, 0u, 0u);
-            if (c > kSparseKept || keep[q] != 0) u = __ldcs(v4 + q * 32 + lane);
-            x[q][0] = u.x;
-            x[q][1] = u.y;
-            x[q][2] = u.z;
-            x[q][3] = u.w;
+    for (int k = 0; k < PPW; ++k) {
+        const uint32_t pc = static_cast<uint32_t>(__popc(word[k]));
+        c[k] = __reduce_add_sync(kFullMask, pc);
+        if (c[k] != 0 && c[k] <= kSparseKept) {   // (warp-uniform)
+            uint32_t r = pc;
+#pragma unroll
+            for (int d = 1; d < 16; d <<= 1) {
+                const uint32_t u = __shfl_up_sync(kFullMask, r, d);
+                if (lane >= d) r += u;
+            }
+            r -= pc;   // kept elements in the words before this lane's
+            uint32_t w = word[k];
+            while (w != 0) {
+                s_list[warp][k][r++] = static_cast<uint16_t>(32 * lane + (__ffs(w) - 1));
+                w &= w - 1;
+            }
         }
-    } else {
+    }
+    __syncwarp();
+    uint32_t v[PPW];
+#pragma unroll
+    for (int k = 0; k < PPW; ++k)
+        if (c[k] <= kSparseKept && static_cast<uint32_t>(lane) < c[k])
+            v[k] = __ldcs(in + static_cast<size_t>(p0 + k) * kPartElems + s_list[warp][k][lane]);
+#pragma unroll
+    for (int k = 0; k < PPW; ++k)
+        if (c[k] <= kSparseKept && static_cast<uint32_t>(lane) < c[k]) out[static_cast<size_t>(o[k]) + lane] = v[k];
+    // dense parts, one after another
+#pragma unroll
+    for (int k = 0; k < PPW; ++k) {
+        if (c[k] <= kSparseKept) continue;   // (warp-uniform)
+        uint32_t x[4][4], keep[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
+            keep[q] = (__shfl_sync(kFullMask, word[k], 4 * q + (lane >> 3)) >> (4 * (lane & 7))) & 0xfu;
+        const size_t b = static_cast<size_t>(p0 + k) * kPartElems;
+        if (b + kPartElems <= n) {
+            const uint4 *v4 = reinterpret_cast<const uint4 *>(in + b);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                x[q][j] = ((keep[q] >> j) & 1u) ? in[b + static_cast<size_t>((q * 32 + lane) * 4 + j)] : 0u;
+            for (int q = 0; q < 4; ++q) {
+                const uint4 u = __ldcs(v4 + q * 32 + lane);
+                x[q][0] = u.x;
+                x[q][1] = u.y;
+                x[q][2] = u.z;
+                x[q][3] = u.w;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    x[q][j] = ((keep[q] >> j) & 1u) ? in[b + static_cast<size_t>((q * 32 + lane) * 4 + j)] : 0u;
+        }
+        compact_write_warp<4>(x, keep, o[k], lane, s_stage[warp], out, OUT_ALIGNED, n);
     }
-    compact_write_warp<4>(x, keep, o, lane, s_stage[warp], out, OUT_ALIGNED, n);
 }
 
 size_t compact_part_words(size_t n) { return 18 * ((n + kPartElems - 1) / kPartElems); }   // mask, count, offset
@@ -303,30 +427,38 @@ inline unsigned count_chunk(unsigned parts, unsigned warps, int num_sms)
     return (parts + blocks - 1) / blocks;
 }
 
-// The count launch: THREADS per block, NSTG * SP parts of stages (512 bytes
-// of flags or, GT, 2,048 bytes of values per part).  part_words: mask[16
-// parts] | cnt[parts] | off[parts]; the workspace's tile sums hold the chunk
-// totals (first kMaxCountBlocks words) and carries (next).
-template <int THREADS, int SP, int NSTG, bool GT = false>
+// The count launch: THREADS per block, NSTG * SP * 512 bytes of stages.
+// part_words: mask[16 parts] | cnt[parts] | off[parts]; the workspace's tile
+// sums hold the chunk totals (first kMaxCountBlocks words) and carries (next).
+template <int THREADS, int SP, int NSTG>
 cudaError_t launch_compact_count(const uint8_t *flags, size_t n, uint32_t *part_words, int32_t *count,
-                                 unsigned chunk, const Workspace &ws, cudaStream_t s, int32_t threshold = 0)
+                                 unsigned chunk, const Workspace &ws, cudaStream_t s)
 {
     static std::atomic<unsigned long long> smem_set{0};
-    constexpr int kSmem = NSTG * SP * kPartElems * (GT ? 4 : 1);
-    auto kernel = compact_count_kernel<THREADS, SP, NSTG, GT>;
+    constexpr int kSmem = NSTG * SP * kPartElems;
+    auto kernel = compact_count_kernel<THREADS, SP, NSTG>;
     cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kernel), kSmem, smem_set);
     if (e != cudaSuccess) return e;
     const unsigned parts = static_cast<unsigned>((n + kPartElems - 1) / kPartElems);
     const unsigned blocks = (parts + chunk - 1) / chunk;
     uint32_t *mask = part_words, *cnt = part_words + static_cast<size_t>(parts) * 16, *off = cnt + parts;
     kernel<<<blocks, THREADS, kSmem, s>>>(flags, n, parts, chunk, mask, cnt, off, ws.tile_sums,
-                                          ws.tile_sums + kMaxCountBlocks, count, ws.state, threshold);
+                                          ws.tile_sums + kMaxCountBlocks, count, ws.state);
     return cudaGetLastError();
 }
 
-// The fused predicate's count launch streams the values: 32 parts (64 KB)
-// per stage, three stages.
-constexpr int kGtCountStageParts = 32, kGtCountStages = 3;
+// The fused predicate's count launch (the same layout of part_words).
+cudaError_t launch_compact_gt_count(const uint32_t *in, int32_t threshold, size_t n, uint32_t *part_words,
+                                    int32_t *count, unsigned chunk, const Workspace &ws, cudaStream_t s)
+{
+    const unsigned parts = static_cast<unsigned>((n + kPartElems - 1) / kPartElems);
+    const unsigned blocks = (parts + chunk - 1) / chunk;
+    uint32_t *mask = part_words, *cnt = part_words + static_cast<size_t>(parts) * 16, *off = cnt + parts;
+    compact_gt_count_kernel<kCountThreads><<<blocks, kCountThreads, 0, s>>>(
+        in, threshold, n, parts, chunk, mask, cnt, off, ws.tile_sums, ws.tile_sums + kMaxCountBlocks, count,
+        ws.state);
+    return cudaGetLastError();
+}
 
 // gt: keep in[i] > threshold (the count launch reads the values; flags unused)
 cudaError_t launch_compact_two_pass(const uint32_t *in, const uint8_t *flags, uint32_t *out, int32_t *count,
@@ -335,14 +467,13 @@ cudaError_t launch_compact_two_pass(const uint32_t *in, const uint8_t *flags, ui
 {
     const unsigned parts = static_cast<unsigned>((n + kPartElems - 1) / kPartElems);
     const unsigned chunk = count_chunk(parts, kCountThreads / 32, ws.num_sms);
-    cudaError_t e = gt ? launch_compact_count<kCountThreads, kGtCountStageParts, kGtCountStages, true>(
-                             reinterpret_cast<const uint8_t *>(in), n, part_words, count, chunk, ws, s, threshold)
+    cudaError_t e = gt ? launch_compact_gt_count(in, threshold, n, part_words, count, chunk, ws, s)
                        : launch_compact_count<kCountThreads, kCountStageParts, kCountStages>(flags, n, part_words,
                                                                                            count, chunk, ws, s);
     if (e != cudaSuccess) return e;
     const uint32_t *mask = part_words, *off = part_words + static_cast<size_t>(parts) * 17;
     const uint32_t *carry = ws.tile_sums + kMaxCountBlocks;
-    const unsigned wblocks = (parts + kWriteWarps - 1) / kWriteWarps;
+    const unsigned wblocks = (parts + kWriteWarps * kWritePartsPerWarp - 1) / (kWriteWarps * kWritePartsPerWarp);
     return out_aligned ? launch_dependent(compact_write_kernel<true, kWriteMinBlocks>, wblocks, kWriteWarps * 32, s, in,
                                           out, n, parts, chunk, mask, off, carry)
                        : launch_dependent(compact_write_kernel<false, kWriteMinBlocks>, wblocks, kWriteWarps * 32, s,
