@@ -339,7 +339,7 @@ compact_gt_count_kernel(const uint32_t *__restrict__ in, int32_t threshold, size
 template <bool OUT_ALIGNED, int MIN_BLOCKS>
 __global__ void __launch_bounds__(kWriteWarps * 32, MIN_BLOCKS)
 compact_write_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, size_t n, unsigned parts,
-                     unsigned chunk, const uint32_t *__restrict__ mask, const uint32_t *__restrict__ off,
+                     ChunkDiv chunk, const uint32_t *__restrict__ mask, const uint32_t *__restrict__ off,
                      const uint32_t *__restrict__ carry)
 {
     constexpr int PPW = kWritePartsPerWarp;
@@ -354,7 +354,7 @@ compact_write_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out
     for (int k = 0; k < PPW; ++k) {
         const unsigned p = p0 + k;
         word[k] = (p < parts && lane < 16) ? mask[static_cast<size_t>(p) * 16 + lane] : 0u;
-        o[k] = p < parts ? off[p] + carry[p / chunk] : 0u;
+        o[k] = p < parts ? off[p] + carry[chunk.of(p)] : 0u;
     }
     // counts, and the sparse parts' kept indices in order
 #pragma unroll
@@ -474,10 +474,11 @@ cudaError_t launch_compact_two_pass(const uint32_t *in, const uint8_t *flags, ui
     const uint32_t *mask = part_words, *off = part_words + static_cast<size_t>(parts) * 17;
     const uint32_t *carry = ws.tile_sums + kMaxCountBlocks;
     const unsigned wblocks = (parts + kWriteWarps * kWritePartsPerWarp - 1) / (kWriteWarps * kWritePartsPerWarp);
+    const ChunkDiv cd = chunk_div(chunk, parts);
     return out_aligned ? launch_dependent(compact_write_kernel<true, kWriteMinBlocks>, wblocks, kWriteWarps * 32, s, in,
-                                          out, n, parts, chunk, mask, off, carry)
+                                          out, n, parts, cd, mask, off, carry)
                        : launch_dependent(compact_write_kernel<false, kWriteMinBlocks>, wblocks, kWriteWarps * 32, s,
-                                          in, out, n, parts, chunk, mask, off, carry);
+                                          in, out, n, parts, cd, mask, off, carry);
 }
 
 // Ring depths measured on GB300 at 2^26: flags pass A (8 KB per tile) with

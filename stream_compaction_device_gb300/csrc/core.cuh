@@ -137,6 +137,35 @@ __device__ __forceinline__ void st_status(unsigned long long *p, unsigned long l
 }
 
 // ---------------------------------------------------------------------------
+// Bit `nb` of the four words of v, gathered with byte permutes: byte nb / 8 of
+// each word moves into one word (byte j from word j), whose bits nb % 8,
+// 8 + nb % 8, ... then hold the four bits.  `sel` = byte_sel(nb), nbb = nb % 8.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ uint32_t byte_sel(int nb)
+{
+    const uint32_t b = static_cast<uint32_t>(nb) >> 3;
+    return b | ((4u + b) << 4);
+}
+__device__ __forceinline__ uint32_t bytes_at_bit(const uint4 &v, uint32_t sel)
+{
+    const uint32_t lo = __byte_perm(v.x, v.y, sel), hi = __byte_perm(v.z, v.w, sel);
+    return __byte_perm(lo, hi, 0x5410);
+}
+// how many of the four words have bit nb set
+__device__ __forceinline__ uint32_t ones_at_bit(const uint4 &v, uint32_t sel, int nbb)
+{
+    return static_cast<uint32_t>(__popc((bytes_at_bit(v, sel) >> nbb) & 0x01010101u));
+}
+// bit j set when word j has bit nb set: the four bits at 0, 8, 16 and 24 land
+// on bits 21 .. 24 of one product (1 + 2^7 + 2^14 + 2^21 has no two terms on
+// one bit)
+__device__ __forceinline__ uint32_t nibble_at_bit(const uint4 &v, uint32_t sel, int nbb)
+{
+    const uint32_t t = (bytes_at_bit(v, sel) >> nbb) & 0x01010101u;
+    return ((t * 0x00204081u) >> 21) & 0xfu;
+}
+
+// ---------------------------------------------------------------------------
 // Streaming global memory access (each element is read once and written once).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }

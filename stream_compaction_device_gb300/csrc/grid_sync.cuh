@@ -142,6 +142,30 @@ __device__ bool last_block_carries(uint32_t block_total, uint32_t *block_sums, u
     return true;
 }
 
+// floor(p / d) for the part indices of a launch without a division
+// sequence: (p * m) >> 40 with m = ceil(2^40 / d).  With m d = 2^40 + r,
+// 0 <= r < d, the product's extra term p r / 2^40 stays below 1 when
+// p d < 2^40, so the floor is exact; the host passes m = 0 (divide) when it
+// cannot promise that for every part index p < parts, or when p m could
+// overflow 64 bits.
+struct ChunkDiv {
+    unsigned d;
+    unsigned long long m;
+    __device__ __forceinline__ unsigned of(unsigned p) const
+    {
+        return m != 0 ? static_cast<unsigned>((static_cast<unsigned long long>(p) * m) >> 40) : p / d;
+    }
+};
+inline ChunkDiv chunk_div(unsigned d, unsigned parts)
+{
+    ChunkDiv c;
+    c.d = d;
+    const unsigned long long pd = static_cast<unsigned long long>(parts) * d;
+    const bool exact = pd < (1ull << 40) && static_cast<unsigned long long>(parts) < (static_cast<unsigned long long>(d) << 23);
+    c.m = exact ? ((1ull << 40) + d - 1) / d : 0ull;
+    return c;
+}
+
 // Programmatic dependent launch: a grid launched after this one with
 // launch_dependent() may start once every block here has called
 // allow_dependent_launch() (or exited); it waits in wait_primary_grid() until

@@ -248,7 +248,9 @@ radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict_
     for (unsigned i = tid; i < len; i += kSortThreads) {
         const uint32_t k = s_keys[i];
         const size_t dst = static_cast<uint32_t>(i + s_delta[digit_of(k, shift)]);
-        if (dst < n) __stcs(keys_out + dst, k);
+        // full tiles: the run starts come from counts of the whole input, so
+        // every destination is below n; the ragged tile keeps the guard
+        if (FULL || dst < n) __stcs(keys_out + dst, k);
     }
 }
 

@@ -265,7 +265,7 @@ split_count_kernel(const uint32_t *__restrict__ keys, size_t n, int bit, unsigne
 template <bool OUT_ALIGNED, bool COUNT_NEXT>
 __global__ void __launch_bounds__(kSplitWriteWarps * 32, 5)
 split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size_t n, int bit, unsigned parts,
-                   unsigned chunk, const uint32_t *__restrict__ off, const uint32_t *__restrict__ carry,
+                   ChunkDiv chunk, const uint32_t *__restrict__ off, const uint32_t *__restrict__ carry,
                    const unsigned *__restrict__ zeros, int next_bit, uint32_t *__restrict__ next_cnt)
 {
     constexpr int kStage = kSplitPart + 12;   // the zeros, the ones from the next 16-byte boundary, a spare chunk
@@ -281,6 +281,7 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
     uint32_t x[4][4], zmask[4];
     if (part_len == static_cast<unsigned>(kSplitPart)) {
         const uint4 *k4 = reinterpret_cast<const uint4 *>(keys + b);
+        const uint32_t sel = byte_sel(bit);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const uint4 u = __ldcs(k4 + q * 32 + lane);
@@ -288,10 +289,7 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
             x[q][1] = u.y;
             x[q][2] = u.z;
             x[q][3] = u.w;
-            uint32_t m = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) m |= ((x[q][j] >> bit) & 1u) << j;
-            zmask[q] = m ^ 0xfu;
+            zmask[q] = nibble_at_bit(u, sel, bit & 7) ^ 0xfu;
         }
     } else {
 #pragma unroll
@@ -307,7 +305,7 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
         }
     }
     wait_primary_grid();   // the count launch's offsets, carries and Z (the keys need no wait)
-    const size_t zeros_at = static_cast<size_t>(off[p]) + carry[p / chunk];
+    const size_t zeros_at = static_cast<size_t>(off[p]) + carry[chunk.of(p)];
     const size_t ones_at = static_cast<size_t>(*zeros) + (b - zeros_at);
     split_write_warp<4, COUNT_NEXT>(x, zmask, part_len, zeros_at, ones_at, lane, s_stage[warp], out, OUT_ALIGNED, n,
                                     next_bit, next_cnt);
@@ -392,16 +390,17 @@ cudaError_t launch_split_write(const uint32_t *keys, uint32_t *out, size_t n, in
     const unsigned parts = static_cast<unsigned>(split_part_words(n));
     const unsigned wblocks = (parts + kSplitWriteWarps - 1) / kSplitWriteWarps;
     const bool aligned = reinterpret_cast<uintptr_t>(out) % 16 == 0;
+    const ChunkDiv cd = chunk_div(chunk, parts);
     constexpr unsigned kThreads = kSplitWriteWarps * 32;
     if (next_cnt != nullptr)
         return aligned ? launch_dependent(split_write_kernel<true, true>, wblocks, kThreads, s, keys, out, n, bit, parts,
-                                          chunk, off, carry, zeros, next_bit, next_cnt)
+                                          cd, off, carry, zeros, next_bit, next_cnt)
                        : launch_dependent(split_write_kernel<false, true>, wblocks, kThreads, s, keys, out, n, bit,
-                                          parts, chunk, off, carry, zeros, next_bit, next_cnt);
+                                          parts, cd, off, carry, zeros, next_bit, next_cnt);
     return aligned ? launch_dependent(split_write_kernel<true, false>, wblocks, kThreads, s, keys, out, n, bit, parts,
-                                      chunk, off, carry, zeros, 0, static_cast<uint32_t *>(nullptr))
+                                      cd, off, carry, zeros, 0, static_cast<uint32_t *>(nullptr))
                    : launch_dependent(split_write_kernel<false, false>, wblocks, kThreads, s, keys, out, n, bit, parts,
-                                      chunk, off, carry, zeros, 0, static_cast<uint32_t *>(nullptr));
+                                      cd, off, carry, zeros, 0, static_cast<uint32_t *>(nullptr));
 }
 
 cudaError_t launch_split_two_pass(const uint32_t *keys, uint32_t *out, size_t n, int bit, unsigned *zeros,

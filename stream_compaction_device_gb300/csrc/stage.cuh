@@ -145,13 +145,15 @@ __device__ __forceinline__ void write_run_direct_count(uint32_t *__restrict__ ou
     const unsigned next = 512u - static_cast<unsigned>((g0 - a) & 511u);
     uint4 *dst = reinterpret_cast<uint4 *>(out) + (g0 >> 2);
     const uint4 *src = reinterpret_cast<const uint4 *>(stage);
+    const uint32_t sel = byte_sel(nb);
+    const int nbb = nb & 7;
     for (unsigned k = tid; k < chunks; k += THREADS) {
         const uint4 v = src[k];
         const unsigned w0 = 4 * k;
         uint32_t z;
         if (w0 >= a && w0 + 4 <= stop) {
             st_stream(dst + k, v);
-            z = 4u - (((v.x >> nb) & 1u) + ((v.y >> nb) & 1u) + ((v.z >> nb) & 1u) + ((v.w >> nb) & 1u));
+            z = 4u - ones_at_bit(v, sel, nbb);
         } else {
             uint32_t *o = reinterpret_cast<uint32_t *>(dst + k);
             const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
