@@ -339,8 +339,7 @@ compact_gt_count_kernel(const uint32_t *__restrict__ in, int32_t threshold, size
 template <bool OUT_ALIGNED, int MIN_BLOCKS>
 __global__ void __launch_bounds__(kWriteWarps * 32, MIN_BLOCKS)
 compact_write_kernel(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, size_t n, unsigned parts,
-                     ChunkDiv chunk, const uint32_t *__restrict__ mask, const uint32_t *__restrict__ off,
-                     const uint32_t *__restrict__ carry)
+                     ChunkDiv chunk, const uint32_t *mask, const uint32_t *off, const uint32_t *carry)
 {
     constexpr int PPW = kWritePartsPerWarp;
     __shared__ __align__(16) uint32_t s_stage[kWriteWarps][kPartElems + 4];

@@ -226,7 +226,12 @@ inline cudaError_t allow_dynamic_smem(const void *kernel, int bytes, std::atomic
 
 // Host side: launch `kernel` on `s` as a programmatic dependent of the grid
 // before it (see allow_dependent_launch); without a wait_primary_grid() call
-// first, the kernel must not read what that grid writes.
+// first, the kernel must not read what that grid writes.  The kernel's
+// pointers to such data carry no __restrict__: the wait orders memory
+// accesses only through its "memory" clobber, and a load through a restrict
+// pointer may be moved above it (seen on GB300: a write-launch variant that
+// read the count launch's total through a restrict pointer right after the
+// wait sometimes got an earlier call's total).
 template <typename... Params, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned threads, cudaStream_t s,
                              Args... args)

@@ -265,8 +265,8 @@ split_count_kernel(const uint32_t *__restrict__ keys, size_t n, int bit, unsigne
 template <bool OUT_ALIGNED, bool COUNT_NEXT>
 __global__ void __launch_bounds__(kSplitWriteWarps * 32, 5)
 split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size_t n, int bit, unsigned parts,
-                   ChunkDiv chunk, const uint32_t *__restrict__ off, const uint32_t *__restrict__ carry,
-                   const unsigned *__restrict__ zeros, int next_bit, uint32_t *__restrict__ next_cnt)
+                   ChunkDiv chunk, const uint32_t *off, const uint32_t *carry, const unsigned *zeros,
+                   int next_bit, uint32_t *__restrict__ next_cnt)
 {
     constexpr int kStage = kSplitPart + 12;   // the zeros, the ones from the next 16-byte boundary, a spare chunk
     __shared__ __align__(16) uint32_t s_stage[kSplitWriteWarps][kStage];
@@ -318,7 +318,7 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
 // next pass's writes.
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, 1)
-part_offsets_kernel(uint32_t *__restrict__ cnt, unsigned parts, unsigned chunk, uint32_t *__restrict__ off,
+part_offsets_kernel(uint32_t *cnt, unsigned parts, unsigned chunk, uint32_t *__restrict__ off,
                     uint32_t *__restrict__ block_sums, uint32_t *__restrict__ carry, unsigned *__restrict__ zeros,
                     DevState *st)
 {
