@@ -49,6 +49,7 @@ if ROOT not in sys.path:
 
 METRIC = "int32 exclusive scan Gelem/s & HBM GB/s (% peak) at N=2^28; compaction Gelem/s"
 N_HEADLINE = 1 << 28
+REF_FULL_STEPS = 600   # whole-array oracle scans the reference arm may run (about 130 s at 2^28)
 FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the pipelined
 # scan kernel at N = 2^28 (one-pass ncu capture of this benchmark's own
@@ -137,6 +138,16 @@ class _Nvml:
             self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
         self.max_mhz = self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.SM_CLOCK)
 
+    def cpu_affinity(self):
+        """The host CPUs NVML names as closest to the device (a set), or
+        None when the query is unavailable."""
+        words = 64
+        mask = (self.c.c_ulong * words)()
+        if self.lib.nvmlDeviceGetCpuAffinity(self.dev, words, mask) != 0:
+            return None
+        bits = self.c.sizeof(self.c.c_ulong) * 8
+        return {w * bits + b for w in range(words) for b in range(bits) if (mask[w] >> b) & 1}
+
     def _uint(self, fn, *args):
         v = self.c.c_uint()
         return v.value if fn(self.dev, *args, self.c.byref(v)) == 0 else None
@@ -147,6 +158,35 @@ class _Nvml:
         mw = self._uint(self.lib.nvmlDeviceGetPowerUsage)
         return (time.perf_counter(), self._uint(self.lib.nvmlDeviceGetClockInfo, self.SM_CLOCK), self.max_mhz,
                 None if mw is None else mw / 1e3, sorted(n for bit, n in self.REASONS.items() if reasons & bit))
+
+
+class HostPlacement:
+    """Binds the calling thread to the host CPUs closest to GPU ``index``
+    (those NVML names, within the CPUs this process may use) until
+    ``restore``; ``info`` records what was found and done."""
+
+    def __init__(self, index: int):
+        self.saved = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+        self.info = {"bound": False}
+        try:
+            near = _Nvml(index).cpu_affinity()
+        except Exception as exc:   # no NVML on this host: leave the placement alone
+            self.info["why"] = f"no NVML CPU affinity ({type(exc).__name__})"
+            return
+        if not near or self.saved is None:
+            self.info["why"] = "NVML gave no CPU affinity"
+            return
+        use = self.saved & near
+        self.info.update({"allowed_cpus": len(self.saved), "gpu_near_cpus": len(near), "both": len(use)})
+        if not use:
+            self.info["why"] = "none of this process's CPUs is near the GPU"
+            return
+        os.sched_setaffinity(0, use)
+        self.info["bound"] = True
+
+    def restore(self):
+        if self.saved is not None and self.info.get("bound"):
+            os.sched_setaffinity(0, self.saved)
 
 
 class ClockSampler:
@@ -345,6 +385,10 @@ def run_ours(args):
         # pinned output buffers), so one step's download overlaps the next
         # step's upload, as a user streaming batches would run it; every step
         # still moves its whole input up and its whole result down
+        # the pinned buffers are first touched from the CPUs closest to the
+        # GPU, so that their pages sit on the GPU's side of the host (a
+        # buffer on the far socket crosses the socket link on every copy)
+        placement = HostPlacement(local)
         h_in = torch.from_numpy(x_host).pin_memory()
         h_outs = [torch.empty_like(h_in).pin_memory() for _ in range(2)]
         streams = [torch.cuda.Stream(), torch.cuda.Stream()]
@@ -363,8 +407,9 @@ def run_ours(args):
         el = time.perf_counter() - t0
         el, u = aggregate(el, float(n) * e2e_steps, world, torch.device("cuda", local))
         e2e = {"value": round(u / el / 1e9, 3), "unit": "Gelem/s", "h2d_bytes_per_step": n * 4,
-               "d2h_bytes_per_step": n * 4, "steps": e2e_steps}
+               "d2h_bytes_per_step": n * 4, "steps": e2e_steps, "host_placement": placement.info}
         del h_in, h_outs, works
+        placement.restore()
 
     extra = None
     if not args.no_extras and rank == 0:
@@ -571,15 +616,26 @@ def run_reference(args):
     from stream_compaction_device_gb300 import workloads as wl
     n = args.n
     x = wl.brackets(n)
+    # each step scans the whole array (about 0.22 s at 2^28 on one core)
+    # unless steps + warm-up would run past REF_FULL_STEPS full scans; then
+    # every step scans the same leading sample, sized to that budget
+    calls = args.steps + args.warmup
+    m = n if calls <= REF_FULL_STEPS else max(4096, (n * REF_FULL_STEPS // calls) // 4096 * 4096)
+    xs = x[:m]
     for _ in range(args.warmup):
-        oracle.scan(x, "add", False)
+        oracle.scan(xs, "add", False)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.scan(x, "add", False)
+        oracle.scan(xs, "add", False)
     el = time.perf_counter() - t0
-    value = n * args.steps / el / 1e9
-    sample = (f"serial oracle exclusive add-scan of the whole 2^{n.bit_length() - 1}-element workload per step, "
-              f"{args.steps} steps, one thread")
+    value = m * args.steps / el / 1e9
+    if m == n:
+        sample = (f"serial oracle exclusive add-scan of the whole 2^{n.bit_length() - 1}-element workload per step, "
+                  f"{args.steps} steps, one thread")
+    else:
+        sample = (f"serial oracle exclusive add-scan of the workload's first {m} elements per step "
+                  f"({args.steps} steps + {args.warmup} warm-up would exceed {REF_FULL_STEPS} whole scans), "
+                  "one thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "Gelem/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
@@ -657,7 +713,8 @@ def run_op(args):
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default: 3000 for this library, 20 for the reference arm)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--n", type=int, default=N_HEADLINE)
@@ -672,6 +729,8 @@ def main(argv=None):
                                     "digit_sort"],
                    default="scan", help="scan: the benchmark; the others run one call repeatedly for profiling")
     args = p.parse_args(argv)
+    if args.steps is None:
+        args.steps = 20 if args.impl == "reference" else 3000
     if args.warmup < 3 and args.impl == "ours":
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
