@@ -233,13 +233,13 @@ inline cudaError_t allow_dynamic_smem(const void *kernel, int bytes, std::atomic
 // read the count launch's total through a restrict pointer right after the
 // wait sometimes got an earlier call's total).
 template <typename... Params, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned threads, cudaStream_t s,
-                             Args... args)
+cudaError_t launch_dependent_smem(void (*kernel)(Params...), unsigned grid, unsigned threads, size_t smem,
+                                  cudaStream_t s, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -247,6 +247,13 @@ cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned threads, cudaStream_t s,
+                             Args... args)
+{
+    return launch_dependent_smem(kernel, grid, threads, 0, s, args...);
 }
 
 }  // namespace devscan

@@ -26,6 +26,7 @@
 #pragma once
 
 #include "core.cuh"
+#include "grid_sync.cuh"
 #include "pipeline.cuh"
 
 namespace devscan {
@@ -183,6 +184,20 @@ struct PolicyCarryIn<P, decltype(void(P::kCarryIn))> {
     static constexpr bool value = P::kCarryIn;
 };
 
+// A skippable policy (P::kSkippable) may find at launch that the launch
+// before it already did the work: when P::may_skip(args), the kernel was
+// launched as a programmatic dependent of that launch, waits for it, and
+// returns if P::skip(args) -- before it touches a ticket, a status word or a
+// barrier.
+template <class P, class = void>
+struct PolicySkippable {
+    static constexpr bool value = false;
+};
+template <class P>
+struct PolicySkippable<P, decltype(void(P::kSkippable))> {
+    static constexpr bool value = P::kSkippable;
+};
+
 template <class P, class = void>
 struct PolicyScratch {
     static constexpr size_t value = 0;
@@ -303,6 +318,12 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
     auto *ctrl = reinterpret_cast<typename G::Ctrl *>(smem + G::kCtrlBase);
     const Op op;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if constexpr (PolicySkippable<P>::value) {
+        if (P::may_skip(args)) {   // launched as a programmatic dependent of the launch that decides
+            wait_primary_grid();
+            if (P::skip(args)) return;
+        }
+    }
 
     if (tid == 0) {
         for (int s = 0; s < SA; ++s) {

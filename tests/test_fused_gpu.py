@@ -23,7 +23,7 @@ def ds():
     return m
 
 
-@pytest.fixture(params=["lookback", "pipelined", "l2"])
+@pytest.fixture(params=["default", "lookback", "pipelined", "l2"])
 def mode(request, ds):
     ds.set_carry_mode(request.param)
     yield request.param
@@ -88,6 +88,64 @@ def test_config_compact_gt(ds, sel):
     from stream_compaction_device_gb300 import workloads as wl
     v = wl.compaction_values()
     check_compact_gt(ds, v, wl.threshold_for(sel))
+    assert ds.device_status() == 0
+
+
+def drain_capture_backoff(ds, n=1 << 24):
+    """After a capture gives up, the stream's next 16 capture launches return
+    at once and leave the call to the pipelined launch; 17 calls that keep
+    nothing bring the stream back to capturing (the 17th captures)."""
+    v = torch.full((n,), -5, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(v)
+    cnt = torch.empty(1, dtype=torch.int32, device="cuda")
+    for _ in range(17):
+        ds.compact_greater(v, 0, out=out, count=cnt)
+    assert int(cnt.item()) == 0
+
+
+@pytest.mark.parametrize("sel", [0.0, 0.001, 0.05, 0.10, 0.115, 0.12, 0.125, 0.13, 0.20, 1.0])
+def test_compact_gt_capture_band(ds, sel):
+    """The default form on the 2^26 workload around the selectivity where the
+    one-pass capture stops fitting in shared memory (about 12% kept): each
+    call either captures and writes, or gives up and the pipelined launch
+    behind it does the compaction (and the next calls skip the capture); the
+    result is the oracle's either way."""
+    from stream_compaction_device_gb300 import workloads as wl
+    v = wl.compaction_values()
+    t = {0.0: I32_MAX, 1.0: I32_MIN}.get(sel)
+    drain_capture_backoff(ds)
+    for _ in range(2):   # and again, after whichever outcome the first call had
+        check_compact_gt(ds, v, wl.threshold_for(sel) if t is None else t)
+    assert ds.device_status() == 0
+
+
+@pytest.mark.parametrize("pattern", ["dense_tail", "dense_late_in_ranges", "dense_head", "alternating"])
+def test_compact_gt_capture_gives_up(ds, pattern):
+    """Inputs whose kept values bunch up where a one-pass capture meets them
+    late or early: the capture gives up part-way and the pipelined launch
+    behind it writes the result; a sparse call during the back-off that
+    follows, and one after it, get the oracle's result too."""
+    n = 1 << 24
+    rng = np.random.default_rng(sum(map(ord, pattern)))
+    v = rng.integers(-1000, 0, n, dtype=np.int32)                 # nothing kept at threshold 0 ...
+    i = np.arange(n)
+    if pattern == "dense_tail":                                    # ... except the last 3% (all kept)
+        dense = i >= n - n // 32
+    elif pattern == "dense_late_in_ranges":                        # the last fifth of every 16,384
+        dense = (i % 16384) >= 13107
+    elif pattern == "dense_head":                                  # the first 3%
+        dense = i < n // 32
+    else:                                                          # every other 4,096 (half kept)
+        dense = ((i // 4096) % 2) == 1
+    v[dense] = rng.integers(1, 1000, int(dense.sum()), dtype=np.int32)
+    sparse = rng.random(n) < 0.01
+    v[sparse] = rng.integers(1, 1000, int(sparse.sum()), dtype=np.int32)
+    drain_capture_backoff(ds)
+    check_compact_gt(ds, v, 0)
+    w = rng.integers(-1000, 1000, n, dtype=np.int32)
+    check_compact_gt(ds, w, 979)                                   # about 1% kept, during the back-off
+    drain_capture_backoff(ds)
+    check_compact_gt(ds, w, 979)                                   # and captured again
     assert ds.device_status() == 0
 
 
