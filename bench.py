@@ -18,8 +18,9 @@ is needed between steps.  Prints one JSON line:
   cpu_baseline_mt  the blocked three-phase scan on every host core
   extra      the inclusive / max / xor sweep, the bracket check and bracket
              scan, the segmented scan, the fold and one rank's share of the
-             sharded scan at N = 2^28; compaction (flags and
-             fused predicate), the split, the 32-pass and the 8-bit radix
+             sharded scan at N = 2^28; compaction (flags; fused predicate
+             by default, two-launch and pipelined alone), the split, the
+             32-pass and the 8-bit radix
              sorts at N = 2^26; fp32 add at N = 2^24; N = 65,536 latency; the
              reduce-then-scan carry.  Back-to-back calls between one pair of
              events (device time per call), except the rows that flush L2
@@ -556,6 +557,18 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
         comp_gt2[f"{int(sel * 100)}%"] = r
     ds.set_carry_mode(args.carry)
     out["compaction_gt_fused_two_launch_2^26"] = comp_gt2
+    # the pipelined form alone (the default runs a capture launch first)
+    comp_gt3 = {}
+    ds.set_carry_mode("pipelined")
+    for sel in wl.SELECTIVITIES:
+        t = wl.threshold_for(sel)
+        med, _ = time_events(lambda: ds.compact_greater(dv, t, dout, cnt), reps, 3)
+        k = int(cnt.item())
+        r = row(nc, med, 4 * nc + 4 * k + 4)
+        r["kept"] = k
+        comp_gt3[f"{int(sel * 100)}%"] = r
+    ds.set_carry_mode(args.carry)
+    out["compaction_gt_fused_pipelined_2^26"] = comp_gt3
 
     # split and radix sort at N = 2^26
     keys = torch.from_numpy(wl.radix_keys(nc).view(np.int32)).cuda()
