@@ -564,7 +564,7 @@ cudaError_t set_pipeline_smem(void (*kernel)(typename P::Args, unsigned, unsigne
 // per SM:
 //   stream   every warp owns a contiguous range of its block's chunk and
 //            reads it in rounds of 1,024 values (eight 128-bit loads per lane
-//            in flight, as the fold kernel reads).  It ranks a round's kept
+//            in flight, allocating no L1 lines).  It ranks a round's kept
 //            values with one warp scan of its eight rows' counts (packed into
 //            the bytes of two words) and appends them, in order, to its own
 //            region of shared memory;
@@ -587,18 +587,35 @@ constexpr int kCaptureThreads = 1024;
 constexpr unsigned kCaptureRound = 1024;      // values a warp reads per round
 constexpr unsigned kCaptureSlack = 64;        // kept values a warp may run ahead of its share
 constexpr unsigned kCaptureBackoff = 16;      // capture launches a stream skips after one gave up
-constexpr size_t kCaptureSmem = 216 * 1024;   // the warps' regions
-constexpr unsigned kCaptureWarpCap = static_cast<unsigned>(kCaptureSmem / 4 / (kCaptureThreads / 32));   // 1,728
+// The warps' regions: 192 KB keeps the SM's shared-memory carveout at
+// 196 KB and leaves 60 KB of L1 for the loads in flight (measured at 2^26,
+// 1% kept: 216 KB regions, 28 KB of L1, took 60.0 us; 192 KB, 52.3 us;
+// 160 and 128 KB, 53.5 and 53.3 us).
+constexpr size_t kCaptureSmem = 192 * 1024;
+
+// A 128-bit load that allocates no L1 line (the capture's shared memory
+// leaves L1 small, and a line a load allocates holds L1 space until its data
+// arrives; 4% faster at 216 KB of regions).
+__device__ __forceinline__ uint4 ld_no_l1(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 
 __device__ __forceinline__ uint32_t byte_sum(uint32_t w) { return (w & 0xffu) + ((w >> 8) & 0xffu) + ((w >> 16) & 0xffu) + (w >> 24); }
 
-__global__ void __launch_bounds__(kCaptureThreads, 1)
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 1)
 compact_gt_capture_kernel(const uint32_t *__restrict__ in, int32_t threshold, uint32_t *__restrict__ out,
                           int32_t *__restrict__ count, size_t n, size_t chunk, uint32_t *__restrict__ block_sums,
                           DevState *st, unsigned spin_limit)
 {
-    constexpr int NW = kCaptureThreads / 32;
-    extern __shared__ __align__(16) uint32_t s_kept[];   // NW regions of kCaptureWarpCap values
+    constexpr int NW = THREADS / 32;
+    constexpr unsigned CAP = static_cast<unsigned>(kCaptureSmem / 4 / NW);   // values per warp region
+    extern __shared__ __align__(16) uint32_t s_kept[];   // NW regions of CAP values
     __shared__ uint32_t s_wcnt[NW];
     __shared__ uint32_t s_base, s_total;
     __shared__ int s_abort;
@@ -609,7 +626,7 @@ compact_gt_capture_kernel(const uint32_t *__restrict__ in, int32_t threshold, ui
     const size_t wpart = chunk / NW;   // a multiple of kCaptureRound
     const size_t wb = begin + static_cast<size_t>(warp) * wpart;
     const size_t we = wb + wpart < end ? wb + wpart : (wb < end ? end : wb);   // [wb, we), maybe empty
-    uint32_t *region = s_kept + static_cast<size_t>(warp) * kCaptureWarpCap;
+    uint32_t *region = s_kept + static_cast<size_t>(warp) * CAP;
     const volatile unsigned *abort_flag = &st->capture_abort;
     // the pipelined launch behind this one may start its blocks as these
     // leave; it waits for this grid before it reads the outcome
@@ -629,35 +646,41 @@ compact_gt_capture_kernel(const uint32_t *__restrict__ in, int32_t threshold, ui
     uint32_t kept = 0;
     bool give_up = false;
     unsigned round = 0;
-    for (size_t s = wb; s < we; s += kCaptureRound, ++round) {
-        uint4 q[8];
-        uint32_t valid[8];
+    // a round's values: rows r = 0 .. 7 of 128, lane L holding 4 L .. 4 L + 3
+    auto load_round = [&](size_t s, uint4 (&q)[8]) {
         if (s + kCaptureRound <= we) {
             const uint4 *v4 = reinterpret_cast<const uint4 *>(in + s);
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                q[r] = __ldcs(v4 + r * 32 + lane);
-                valid[r] = 0xfu;
-            }
+            for (int r = 0; r < 8; ++r) q[r] = ld_no_l1(v4 + r * 32 + lane);
         } else {   // the input's ragged end
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
-                uint32_t v[4], m = 0;
+                uint32_t v[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const size_t e = s + static_cast<size_t>(r * 128 + lane * 4 + j);
                     v[j] = e < we ? in[e] : 0u;
-                    m |= (e < we ? 1u : 0u) << j;
                 }
                 q[r] = make_uint4(v[0], v[1], v[2], v[3]);
-                valid[r] = m;
             }
         }
-        // another warp's verdict, every fourth round (read while the values load)
+    };
+    // ranks a round and appends its kept values; false: stop (this warp
+    // gave up, or another warp did)
+    auto take_round = [&](size_t s, const uint4 (&q)[8]) -> bool {
+        const bool full = s + kCaptureRound <= we;
+        // another warp's verdict, every fourth round
         const unsigned stop = (round & 3u) == 3u ? __shfl_sync(kFullMask, *abort_flag, 0) : 0u;
         uint32_t nib[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) nib[r] = greater_mask(q[r].x, q[r].y, q[r].z, q[r].w, threshold) & valid[r];
+        for (int r = 0; r < 8; ++r) {
+            uint32_t valid = 0xfu;
+            if (!full) {
+                const size_t e = s + static_cast<size_t>(r * 128 + lane * 4);
+                valid = e >= we ? 0u : (we - e >= 4 ? 0xfu : (1u << (we - e)) - 1u);
+            }
+            nib[r] = greater_mask(q[r].x, q[r].y, q[r].z, q[r].w, threshold) & valid;
+        }
         const uint32_t pa = __popc(nib[0]) | (__popc(nib[1]) << 8) | (__popc(nib[2]) << 16) | (__popc(nib[3]) << 24);
         const uint32_t pb = __popc(nib[4]) | (__popc(nib[5]) << 8) | (__popc(nib[6]) << 16) | (__popc(nib[7]) << 24);
         uint32_t ia = pa, ib = pb;   // a row keeps at most 128, so the bytes never carry
@@ -672,14 +695,13 @@ compact_gt_capture_kernel(const uint32_t *__restrict__ in, int32_t threshold, ui
         const uint32_t ta = __shfl_sync(kFullMask, ia, 31), tb = __shfl_sync(kFullMask, ib, 31);
         const uint32_t xa = ia - pa, xb = ib - pb;
         const uint32_t round_total = byte_sum(ta) + byte_sum(tb);
-        const size_t done = (s + kCaptureRound < we ? s + kCaptureRound : we) - wb;
+        const size_t done = (full ? s + kCaptureRound : we) - wb;
         const uint32_t after = kept + round_total;
-        const bool over = after > kCaptureWarpCap ||
-                          static_cast<uint64_t>(after) * wpart >
-                              static_cast<uint64_t>(kCaptureWarpCap) * done + static_cast<uint64_t>(kCaptureSlack) * wpart;
+        const bool over = after > CAP || static_cast<uint64_t>(after) * wpart >
+                                             static_cast<uint64_t>(CAP) * done + static_cast<uint64_t>(kCaptureSlack) * wpart;
         if (stop != 0u || over) {   // (warp-uniform)
             give_up = over;
-            break;
+            return false;
         }
         uint32_t at = kept;
 #pragma unroll
@@ -694,12 +716,21 @@ compact_gt_capture_kernel(const uint32_t *__restrict__ in, int32_t threshold, ui
             at += (tot >> sh) & 0xffu;
         }
         kept = after;
+        ++round;
+        return true;
+    };
+    // (holding two rounds in registers, the next loading while this one is
+    // taken, at 512 threads and 120 registers, measured the same)
+    for (size_t s = wb; s < we; s += kCaptureRound) {
+        uint4 q[8];
+        load_round(s, q);
+        if (!take_round(s, q)) break;
     }
     if (give_up && lane == 0) atomicOr(&st->capture_abort, 1u);
     if (lane == 0) s_wcnt[warp] = kept;
     __syncthreads();
     if (warp == 0) {
-        const uint32_t v = __reduce_add_sync(kFullMask, s_wcnt[lane]);   // NW == 32
+        const uint32_t v = __reduce_add_sync(kFullMask, lane < NW ? s_wcnt[lane] : 0u);
         if (lane == 0) {
             block_sums[blockIdx.x] = v;
             s_total = v;
@@ -754,7 +785,7 @@ cudaError_t launch_compact_gt_capture(const uint32_t *in, int32_t threshold, uin
                                       const Workspace &ws, unsigned spin_limit, cudaStream_t s)
 {
     static std::atomic<unsigned long long> smem_set{0};
-    const void *kernel = reinterpret_cast<const void *>(&compact_gt_capture_kernel);
+    const void *kernel = reinterpret_cast<const void *>(&compact_gt_capture_kernel<kCaptureThreads>);
     cudaError_t e = allow_dynamic_smem(kernel, static_cast<int>(kCaptureSmem), smem_set);
     if (e != cudaSuccess) return e;
     const size_t unit = static_cast<size_t>(kCaptureThreads / 32) * kCaptureRound;   // a round per warp
