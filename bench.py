@@ -681,6 +681,11 @@ def run_op(args):
         f = torch.from_numpy(wl.predicate_flags(v, wl.threshold_for(0.5))).cuda()
         out, cnt = torch.empty_like(dv), torch.empty(1, dtype=torch.int32, device="cuda")
         fn = lambda: ds.compact(dv, f, out, cnt)
+    elif args.op in ("compact_gt1", "compact_gt50"):
+        dv = torch.from_numpy(wl.compaction_values(n)).cuda()
+        t = wl.threshold_for(0.01 if args.op == "compact_gt1" else 0.5)
+        out, cnt = torch.empty_like(dv), torch.empty(1, dtype=torch.int32, device="cuda")
+        fn = lambda: ds.compact_greater(dv, t, out, cnt)
     elif args.op == "f32scan":
         x = torch.from_numpy(wl.unit_floats(n)).cuda()
         out = torch.empty_like(x)
@@ -738,7 +743,8 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
-    p.add_argument("--op", choices=["scan", "f32scan", "compact50", "segscan", "bracket_check", "split", "sort32",
+    p.add_argument("--op", choices=["scan", "f32scan", "compact50", "compact_gt1", "compact_gt50", "segscan",
+                                    "bracket_check", "split", "sort32",
                                     "digit_sort"],
                    default="scan", help="scan: the benchmark; the others run one call repeatedly for profiling")
     args = p.parse_args(argv)
