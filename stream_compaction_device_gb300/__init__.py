@@ -152,6 +152,31 @@ def sharded_scan(shard: torch.Tensor, out: torch.Tensor | None = None, inclusive
     return fn(shard, carry, out, op=op, stream=stream, as_uint32=as_uint32)
 
 
+def sharded_compact(values: torch.Tensor, flags: torch.Tensor | None = None, threshold: int | None = None,
+                    out: torch.Tensor | None = None, group=None, stream=None):
+    """This rank's part of the order-preserving compaction of an array split
+    into contiguous shards, shard r on rank r of ``group`` (in rank order).
+    The library compacts the shard (the values whose flag is nonzero, or the
+    values greater than ``threshold``), the ranks exchange their kept counts
+    (one all-gather of one count each), and the library folds the counts of
+    the ranks before this one into this rank's output offset and all of them
+    into the total.  Returns (out, count, offset, total), all on the device:
+    the first ``count`` elements of ``out`` are this rank's kept values,
+    elements offset .. offset + count - 1 of the whole compaction."""
+    import torch.distributed as dist
+    if (flags is None) == (threshold is None):
+        raise ValueError("give either flags or a threshold")
+    rank = dist.get_rank(group) if dist.is_available() and dist.is_initialized() else 0
+    if threshold is None:
+        out, count = compact(values, flags, out, stream=stream)
+    else:
+        out, count = compact_greater(values, threshold, out, stream=stream)
+    counts = exchange_totals(count, group)
+    offset = reduce(counts[:rank], "add", stream=stream)
+    total = reduce(counts, "add", stream=stream)
+    return out, count, offset, total
+
+
 def _segscan(direction: str, x: torch.Tensor, heads: torch.Tensor, out, op: str, stream, dtype_override=None):
     _check_cuda(x, "x")
     _check_cuda(heads, "heads")

@@ -186,3 +186,53 @@ def test_sharded_scan_through_a_one_rank_nccl_group(ds, tmp_path):
             assert np.array_equal(got, oracle.scan(x, op, False)), op
     finally:
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# sharded compaction: each shard compacted, the counts folded into offsets
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("parts", [2, 3, 4])
+@pytest.mark.parametrize("by_threshold", [True, False], ids=["predicate", "flags"])
+@pytest.mark.parametrize("sel", [0.01, 0.5])
+def test_sharded_compaction_matches_whole_array(ds, parts, by_threshold, sel):
+    """P shards of one array, compacted one after another on one GPU through
+    the calls one rank of sharded_compact makes: each shard's compaction,
+    then the fold of the kept counts of the shards before it (its offset)
+    and of all of them (the total).  The shards' kept values, placed at
+    their offsets, are the oracle's compaction of the whole array."""
+    from stream_compaction_device_gb300 import workloads as wl
+    n = (1 << 22) + 12_345
+    v = wl.compaction_values(n, seed=11)
+    t = wl.threshold_for(sel)
+    ref = oracle.compact(v, wl.predicate_flags(v, t))
+    outs, counts = [], []
+    for shard in np.array_split(v, parts):
+        dv = to_dev(shard)
+        if by_threshold:
+            o, c = ds.compact_greater(dv, t)
+        else:
+            o, c = ds.compact(dv, torch.from_numpy(wl.predicate_flags(shard, t)).cuda())
+        outs.append(o)
+        counts.append(c)
+    counts = torch.cat(counts)
+    whole = np.empty(ref.size, np.int32)
+    for r in range(parts):
+        off = int(ds.reduce(counts[:r]).item())
+        k = int(counts[r].item())
+        assert off == int(counts[:r].sum().item())
+        whole[off:off + k] = from_dev(outs[r][:k], np.int32)
+    assert int(ds.reduce(counts).item()) == ref.size
+    assert np.array_equal(whole, ref)
+    assert ds.device_status() == 0
+
+
+def test_sharded_compaction_single_process(ds):
+    """Without a process group sharded_compact is the plain compaction:
+    offset 0 and total = count."""
+    from stream_compaction_device_gb300 import workloads as wl
+    v = wl.compaction_values(1_000_003, seed=12)
+    t = wl.threshold_for(0.2)
+    ref = oracle.compact(v, wl.predicate_flags(v, t))
+    out, cnt, off, tot = ds.sharded_compact(to_dev(v), threshold=t)
+    assert (int(cnt.item()), int(off.item()), int(tot.item())) == (ref.size, 0, ref.size)
+    assert np.array_equal(from_dev(out[: ref.size], np.int32), ref)
