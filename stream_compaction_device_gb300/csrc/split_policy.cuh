@@ -2,6 +2,8 @@
 // zero-count helper both split kernels use.
 #pragma once
 
+#include <type_traits>
+
 #include "core.cuh"
 #include "pipeline_l2.cuh"
 #include "stage.cuh"
@@ -56,24 +58,31 @@ __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], c
     const unsigned o_phase = out_aligned ? static_cast<unsigned>(ones_at & 3) : 0u;
     const unsigned o_base = out_aligned ? ((z_phase + zeros + 3u) & ~3u) : zeros;
     // one store per key, its slot chosen by a select (a branch per key
-    // diverges on random bits); a whole part needs no bounds test
-    const bool whole = part_len == static_cast<unsigned>(32 * 4 * VECS);
+    // diverges on random bits); whole parts (all but the input's last) take
+    // a copy of the loop without the bounds test
     const uint32_t o0 = o_base + o_phase;
-    uint32_t row_base = 0;
+    auto stage_keys = [&](auto whole_part) {
+        constexpr bool WHOLE = decltype(whole_part)::value;
+        uint32_t row_base = 0;
 #pragma unroll
-    for (int q = 0; q < VECS; ++q) {
-        uint32_t zr = row_base + ((excl >> (8 * q)) & 0xffu);
-        const uint32_t li0 = static_cast<uint32_t>((q * 32 + lane) * 4);   // index inside the part
+        for (int q = 0; q < VECS; ++q) {
+            uint32_t zr = row_base + ((excl >> (8 * q)) & 0xffu);
+            const uint32_t li0 = static_cast<uint32_t>((q * 32 + lane) * 4);   // index inside the part
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t li = li0 + j;
-            const uint32_t z = (zmask[q] >> j) & 1u;
-            const uint32_t pos = z ? z_phase + zr : o0 + (li - zr);
-            if (whole || li < part_len) stage[pos] = x[q][j];
-            zr += z;
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t li = li0 + j;
+                const uint32_t z = (zmask[q] >> j) & 1u;
+                const uint32_t pos = z ? z_phase + zr : o0 + (li - zr);
+                if (WHOLE || li < part_len) stage[pos] = x[q][j];
+                zr += z;
+            }
+            row_base += (tot >> (8 * q)) & 0xffu;
         }
-        row_base += (tot >> (8 * q)) & 0xffu;
-    }
+    };
+    if (part_len == static_cast<unsigned>(32 * 4 * VECS))
+        stage_keys(std::true_type{});
+    else
+        stage_keys(std::false_type{});
     __syncwarp();
     if (COUNT_NEXT) {
         // also count bit next_bit's zeros by the output part they land in
