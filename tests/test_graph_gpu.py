@@ -1,7 +1,9 @@
 """The library's calls inside a CUDA graph: after one warm-up on the
 capturing stream (which sets up that stream's workspace and scratch), a
 capture of scans (cluster, L2-resident and pipelined sizes), the two-launch
-compaction, the standalone split, the 32-pass sort, the 8-bit digit sort and
+compaction, the fused-predicate compaction (its capture launch and the
+pipelined launch behind it, on inputs that keep 1% in one replay and
+everything in the next), the standalone split, the 32-pass sort, the 8-bit digit sort and
 one shard's calls of the sharded scan (its fold, the fold of the gathered
 totals, its scan from that carry) replays with new inputs and matches the
 CPU oracle each time.  The kernels keep their
@@ -29,6 +31,7 @@ def test_graph_capture_and_replay(ds):
     rng = np.random.default_rng(2024)
     n_small, n_mid, n_big = 50_000, (1 << 21) + 3, (1 << 24) + 5
     nc, nk = (1 << 23) + 7, (1 << 20) + 5
+    ng = (1 << 22) + 7
 
     def fresh():
         return {
@@ -38,6 +41,7 @@ def test_graph_capture_and_replay(ds):
             "v": rng.integers(-2**31, 2**31, nc, dtype=np.int32),
             "f": (rng.random(nc) < 0.4).astype(np.uint8),
             "k": rng.integers(0, 2**32, nk, dtype=np.uint32),
+            "g": rng.integers(-1000, 1000, ng, dtype=np.int32),   # about 1% above 979
         }
 
     h = fresh()
@@ -47,6 +51,8 @@ def test_graph_capture_and_replay(ds):
     out, cnt = torch.empty_like(v), torch.empty(1, dtype=torch.int32, device="cuda")
     ko, work, tmp = torch.empty_like(k), torch.empty_like(k), torch.empty_like(k)
     work2 = torch.empty_like(k)
+    gv = to_dev(h["g"])
+    gout, gcnt = torch.empty_like(gv), torch.empty(1, dtype=torch.int32, device="cuda")
     totals = torch.empty(3, dtype=torch.int32, device="cuda")
     carry, ysh = torch.empty(1, dtype=torch.int32, device="cuda"), torch.empty_like(xs)
 
@@ -55,6 +61,7 @@ def test_graph_capture_and_replay(ds):
         ds.scan_inclusive(xm, ym)                       # L2-resident cooperative scan
         ds.scan_inclusive(xb, yb, op="xor", as_uint32=True)   # the pipeline
         ds.compact(v, f, out=out, count=cnt)            # count launch, then write launch
+        ds.compact_greater(gv, 979, out=gout, count=gcnt)   # capture launch, pipelined launch behind it
         ds.split_bit(k, 9, out=ko)
         work.copy_(k)
         ds.radix_sort(work, tmp)
@@ -75,9 +82,11 @@ def test_graph_capture_and_replay(ds):
         run()
     torch.cuda.synchronize()
 
-    for _ in range(3):
+    for rep in range(4):
         h = fresh()
-        for dst, src in ((xs, h["xs"]), (xm, h["xm"]), (xb, h["xb"]), (v, h["v"]), (k, h["k"])):
+        if rep % 2 == 1:   # everything kept: the capture gives up (then the stream backs off)
+            h["g"] = rng.integers(980, 2000, ng, dtype=np.int32)
+        for dst, src in ((xs, h["xs"]), (xm, h["xm"]), (xb, h["xb"]), (v, h["v"]), (k, h["k"]), (gv, h["g"])):
             dst.copy_(to_dev(src))
         f.copy_(torch.from_numpy(h["f"]).cuda())
         t01 = rng.integers(-10**6, 10**6, 2, dtype=np.int32)
@@ -93,6 +102,9 @@ def test_graph_capture_and_replay(ds):
         kk = int(cnt.item())
         ref_c = oracle.compact(h["v"], h["f"])
         assert kk == ref_c.size and np.array_equal(out[:kk].cpu().numpy(), ref_c)
+        kg = int(gcnt.item())
+        ref_g = h["g"][h["g"] > 979]
+        assert kg == ref_g.size and np.array_equal(gout[:kg].cpu().numpy(), ref_g)
         assert np.array_equal(from_dev(ko, np.uint32), oracle.split_bit(h["k"], 9)[0])
         assert np.array_equal(from_dev(work, np.uint32), np.sort(h["k"]))
         assert np.array_equal(from_dev(work2, np.uint32), np.sort(h["k"]))
