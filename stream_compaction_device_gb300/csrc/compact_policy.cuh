@@ -5,6 +5,7 @@
 #include "core.cuh"
 #include "pipeline_l2.cuh"
 #include "stage.cuh"
+#include "capture.cuh"
 
 namespace devscan {
 
@@ -236,13 +237,6 @@ struct CompactPolicy {
     }
 };
 
-// Keep mask of four int32 values against a threshold: bit j set when
-// (int32) v_j > t.
-__device__ __forceinline__ uint32_t greater_mask(uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3, int32_t t)
-{
-    return (static_cast<int32_t>(v0) > t ? 1u : 0u) | (static_cast<int32_t>(v1) > t ? 2u : 0u) |
-           (static_cast<int32_t>(v2) > t ? 4u : 0u) | (static_cast<int32_t>(v3) > t ? 8u : 0u);
-}
 
 // ---------------------------------------------------------------------------
 // Pipelined compaction with the predicate evaluated in the kernel (keep
@@ -276,12 +270,19 @@ struct CompactGtPolicy {
         size_t n;
         unsigned num_tiles;
         bool out_aligned;
-        const unsigned *skip = nullptr;   // nonzero word: a capture launch already wrote the result
+        size_t capture_chunk = 0;            // nonzero: try the one-pass capture first (a cooperative launch)
+        uint32_t *block_sums = nullptr;      // the capture's block totals (one word per block)
     };
-    // the launch returns at once when the capture launch before it succeeded
-    static constexpr bool kSkippable = true;
-    __device__ static bool may_skip(const Args &a) { return a.skip != nullptr; }
-    __device__ static bool skip(const Args &a) { return *reinterpret_cast<const volatile unsigned *>(a.skip) != 0u; }
+    // the kernel first tries the one-pass capture (capture.cuh) and returns
+    // when it wrote the result
+    static constexpr bool kCapturing = true;
+    __device__ static bool may_capture(const Args &a) { return a.capture_chunk != 0; }
+    template <int NW, unsigned CAP>
+    __device__ static bool capture(const Args &a, uint32_t *smem, DevState *st, unsigned spin_limit)
+    {
+        return capture_gt<NW, CAP>(a.in, a.threshold, a.out, a.count, a.n, a.capture_chunk, a.block_sums, st,
+                                   spin_limit, smem);
+    }
     __device__ static unsigned tile_len(const Args &a, unsigned t)
     {
         const size_t rem = a.n - static_cast<size_t>(t) * kTile;

@@ -97,9 +97,8 @@ template <> __device__ __forceinline__ float from_bits<float>(uint32_t b) { retu
 //   cursor : rolling position for refreshing status slots that recent
 //            launches did not use (so no stale word outlives 2^30 epochs).
 //   zeros  : zero counts per bit for the split / radix sort.
-//   capture_abort / capture_done / capture_wait : the fused-predicate
-//            compaction's capture launch, the pipelined launch that stands
-//            behind it, and the back-off after a capture gave up.
+//   capture_abort / capture_wait : the fused-predicate compaction's
+//            one-pass capture, and the back-off after a capture gave up.
 // ---------------------------------------------------------------------------
 struct DevState {
     unsigned epoch;
@@ -109,10 +108,9 @@ struct DevState {
     unsigned grid_arrive;   // blocks that reached the grid barrier, or that handed in their totals
                             // (the last one of those resets it)
     unsigned grid_depart;   // blocks that left it; the last one resets both
-    unsigned capture_abort; // a fused-predicate capture launch gave up (reset by its last block to leave)
-    unsigned capture_done;  // the last capture launch wrote the result (the fallback launch then returns)
-    unsigned capture_wait;  // capture launches still to skip after one gave up (a back-off)
-    unsigned pad[7];
+    unsigned capture_abort; // a fused-predicate capture gave up (reset by its last block to leave)
+    unsigned capture_wait;  // calls still to skip the capture after one gave up (a back-off)
+    unsigned pad[8];
     unsigned zeros[48];
 };
 static_assert(sizeof(DevState) == 256, "DevState is 256 bytes in every workspace layout");

@@ -184,18 +184,18 @@ struct PolicyCarryIn<P, decltype(void(P::kCarryIn))> {
     static constexpr bool value = P::kCarryIn;
 };
 
-// A skippable policy (P::kSkippable) may find at launch that the launch
-// before it already did the work: when P::may_skip(args), the kernel was
-// launched as a programmatic dependent of that launch, waits for it, and
-// returns if P::skip(args) -- before it touches a ticket, a status word or a
-// barrier.
+// A capturing policy (P::kCapturing) may do the whole job before the
+// pipeline starts: when P::may_capture(args) (a cooperative launch), every
+// block first runs P::capture over the whole of its dynamic shared memory
+// and returns when it wrote the result; otherwise the pipeline starts from
+// its usual state, which the capture does not touch.
 template <class P, class = void>
-struct PolicySkippable {
+struct PolicyCapturing {
     static constexpr bool value = false;
 };
 template <class P>
-struct PolicySkippable<P, decltype(void(P::kSkippable))> {
-    static constexpr bool value = P::kSkippable;
+struct PolicyCapturing<P, decltype(void(P::kCapturing))> {
+    static constexpr bool value = P::kCapturing;
 };
 
 template <class P, class = void>
@@ -318,10 +318,12 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
     auto *ctrl = reinterpret_cast<typename G::Ctrl *>(smem + G::kCtrlBase);
     const Op op;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if constexpr (PolicySkippable<P>::value) {
-        if (P::may_skip(args)) {   // launched as a programmatic dependent of the launch that decides
-            wait_primary_grid();
-            if (P::skip(args)) return;
+    if constexpr (PolicyCapturing<P>::value) {
+        if (P::may_capture(args)) {
+            constexpr int NW = G::kThreads / 32;
+            constexpr unsigned CAP = static_cast<unsigned>(G::kSmemBytes / 4 / NW);   // values per warp region
+            if (P::template capture<NW, CAP>(args, reinterpret_cast<uint32_t *>(smem), st, spin_limit)) return;
+            __syncthreads();   // every warp has left its region before the set-up below reuses the memory
         }
     }
 
