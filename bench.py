@@ -557,7 +557,7 @@ def run_extras(args, ds, wl, d_in, d_out, peak):
         comp_gt2[f"{int(sel * 100)}%"] = r
     ds.set_carry_mode(args.carry)
     out["compaction_gt_fused_two_launch_2^26"] = comp_gt2
-    # the pipelined form alone (the default runs a capture launch first)
+    # the pipelined form alone (the default tries the one-pass capture first)
     comp_gt3 = {}
     ds.set_carry_mode("pipelined")
     for sel in wl.SELECTIVITIES:

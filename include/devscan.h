@@ -229,13 +229,13 @@ devscan_status compact_i32(const int32_t *in, const uint8_t *flags, int32_t *out
  * compare).  No flag array is read, so the traffic is 4 bytes per element
  * plus 4 per kept element.  Arguments, limits and errors as compact_i32,
  * without flags.
- * From 2^19 elements (in 16-byte aligned) the call queues two launches: a
- * cooperative launch (one block per SM) that reads the values once and
- * keeps the kept ones in shared memory, which succeeds while they fit (at
- * 2^26 elements, up to about 10% kept), and a pipelined launch that does the
- * compaction when it did not.  After a capture gives up, the stream skips
- * the capture for its next 16 calls.  That state lives in the stream's
- * workspace and affects only which launch does the work, never the result.
+ * From 2^19 elements (in 16-byte aligned) the call is one cooperative launch
+ * (one block per SM): it first reads the values once and keeps the kept ones
+ * in shared memory, which succeeds while they fit (at 2^26 elements, up to
+ * about 10% kept), and otherwise goes on as a pipeline that reads them again.
+ * After a capture gives up, the stream skips it for its next 16 calls.  That
+ * state lives in the stream's workspace and affects only how the work is
+ * done, never the result.
  * Smaller or unaligned inputs take a single-pass kernel. */
 devscan_status compact_gt_i32(const int32_t *in, int32_t threshold, int32_t *out,
                               int32_t *count, size_t n, cudaStream_t stream);

@@ -45,7 +45,7 @@ __device__ __forceinline__ uint32_t greater_mask(uint32_t v0, uint32_t v1, uint3
 // ---------------------------------------------------------------------------
 constexpr unsigned kCaptureRound = 1024;      // values a warp reads per round
 constexpr unsigned kCaptureSlack = 64;        // kept values a warp may run ahead of its share
-constexpr unsigned kCaptureBackoff = 16;      // capture launches a stream skips after one gave up
+constexpr unsigned kCaptureBackoff = 16;      // calls a stream skips the capture for after one gave up
 
 // A 128-bit load that allocates no L1 line (the capture's shared memory
 // leaves L1 small, and a line a load allocates holds L1 space until its data

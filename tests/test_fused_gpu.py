@@ -92,9 +92,9 @@ def test_config_compact_gt(ds, sel):
 
 
 def drain_capture_backoff(ds, n=1 << 24):
-    """After a capture gives up, the stream's next 16 capture launches return
-    at once and leave the call to the pipelined launch; 17 calls that keep
-    nothing bring the stream back to capturing (the 17th captures)."""
+    """After a capture gives up, the stream's next 16 calls skip it and run
+    the pipeline; 17 calls that keep nothing bring the stream back to
+    capturing (the 17th captures)."""
     v = torch.full((n,), -5, dtype=torch.int32, device="cuda")
     out = torch.empty_like(v)
     cnt = torch.empty(1, dtype=torch.int32, device="cuda")
@@ -107,8 +107,8 @@ def drain_capture_backoff(ds, n=1 << 24):
 def test_compact_gt_capture_band(ds, sel):
     """The default form on the 2^26 workload around the selectivity where the
     one-pass capture stops fitting in shared memory (about 10% kept): each
-    call either captures and writes, or gives up and the pipelined launch
-    behind it does the compaction (and the next calls skip the capture); the
+    call either captures and writes, or gives up and the kernel goes on as
+    the pipeline (and the next calls skip the capture); the
     result is the oracle's either way."""
     from stream_compaction_device_gb300 import workloads as wl
     v = wl.compaction_values()
@@ -122,8 +122,8 @@ def test_compact_gt_capture_band(ds, sel):
 @pytest.mark.parametrize("pattern", ["dense_tail", "dense_late_in_ranges", "dense_head", "alternating"])
 def test_compact_gt_capture_gives_up(ds, pattern):
     """Inputs whose kept values bunch up where a one-pass capture meets them
-    late or early: the capture gives up part-way and the pipelined launch
-    behind it writes the result; a sparse call during the back-off that
+    late or early: the capture gives up part-way and the kernel goes on as
+    the pipeline; a sparse call during the back-off that
     follows, and one after it, get the oracle's result too."""
     n = 1 << 24
     rng = np.random.default_rng(sum(map(ord, pattern)))

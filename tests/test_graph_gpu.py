@@ -1,9 +1,9 @@
 """The library's calls inside a CUDA graph: after one warm-up on the
 capturing stream (which sets up that stream's workspace and scratch), a
 capture of scans (cluster, L2-resident and pipelined sizes), the two-launch
-compaction, the fused-predicate compaction (its capture launch and the
-pipelined launch behind it, on inputs that keep 1% in one replay and
-everything in the next), the standalone split, the 32-pass sort, the 8-bit digit sort and
+compaction, the fused-predicate compaction (one cooperative launch that
+captures or goes on as the pipeline, on inputs that keep 1% in one replay
+and everything in the next), the standalone split, the 32-pass sort, the 8-bit digit sort and
 one shard's calls of the sharded scan (its fold, the fold of the gathered
 totals, its scan from that carry) replays with new inputs and matches the
 CPU oracle each time.  The kernels keep their
@@ -61,7 +61,7 @@ def test_graph_capture_and_replay(ds):
         ds.scan_inclusive(xm, ym)                       # L2-resident cooperative scan
         ds.scan_inclusive(xb, yb, op="xor", as_uint32=True)   # the pipeline
         ds.compact(v, f, out=out, count=cnt)            # count launch, then write launch
-        ds.compact_greater(gv, 979, out=gout, count=gcnt)   # capture launch, pipelined launch behind it
+        ds.compact_greater(gv, 979, out=gout, count=gcnt)   # cooperative: capture, or the pipeline
         ds.split_bit(k, 9, out=ko)
         work.copy_(k)
         ds.radix_sort(work, tmp)
