@@ -62,7 +62,8 @@ __device__ __forceinline__ uint4 ld_no_l1(const uint4 *p)
 __device__ __forceinline__ uint32_t byte_sum(uint32_t w) { return (w & 0xffu) + ((w >> 8) & 0xffu) + ((w >> 16) & 0xffu) + (w >> 24); }
 
 // Returns true when the capture wrote the result (out, *count); false when it
-// gave up or was skipped, and then the caller does the compaction.  Every
+// gave up, and then the caller does the compaction.  The caller checks the
+// back-off first (capture_backoff) and calls this only when it is zero.  Every
 // block of the grid returns the same unless a grid-barrier wait ran out (the
 // error word then says so).  NW warps per block; s_kept: NW regions of CAP
 // values; chunk: the elements of each block, a multiple of NW rounds.
@@ -86,15 +87,6 @@ __device__ __forceinline__ bool capture_gt(const uint32_t *__restrict__ in, int3
     const volatile unsigned *abort_flag = &st->capture_abort;
     // a capture on this stream gave up lately: leave it to the pipeline
     // (every block reads the count before any block can leave)
-    const unsigned backoff = *reinterpret_cast<const volatile unsigned *>(&st->capture_wait);
-    if (backoff != 0u) {
-        __syncthreads();
-        if (tid == 0 && atomicAdd(&st->grid_depart, 1u) == blocks - 1) {
-            st->capture_wait = backoff - 1u;
-            st->grid_depart = 0u;
-        }
-        return false;
-    }
     uint32_t kept = 0;
     bool give_up = false;
     unsigned round = 0;
@@ -231,6 +223,25 @@ __device__ __forceinline__ bool capture_gt(const uint32_t *__restrict__ in, int3
         st->grid_depart = 0u;
     }
     return !abort;
+}
+
+// The stream's back-off: capture attempts still to skip after one gave up.
+// Every thread reads it (one word, so no barrier is needed for the block to
+// agree).
+__device__ __forceinline__ unsigned capture_backoff(const DevState *st)
+{
+    return *reinterpret_cast<const volatile unsigned *>(&st->capture_wait);
+}
+
+// A skipped attempt counts one off the back-off.  Called by one thread of
+// every block, after that block's read of the back-off: the last block to
+// arrive writes the new count and resets the arrival counter.
+__device__ __forceinline__ void capture_skip_depart(DevState *st, unsigned backoff, unsigned blocks)
+{
+    if (atomicAdd(&st->grid_depart, 1u) == blocks - 1) {
+        st->capture_wait = backoff - 1u;
+        st->grid_depart = 0u;
+    }
 }
 
 // The capture's chunk per block for a grid of `blocks`: whole rounds for

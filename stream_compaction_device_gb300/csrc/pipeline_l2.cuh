@@ -26,6 +26,7 @@
 #pragma once
 
 #include "core.cuh"
+#include "capture.cuh"
 #include "grid_sync.cuh"
 #include "pipeline.cuh"
 
@@ -318,12 +319,20 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
     auto *ctrl = reinterpret_cast<typename G::Ctrl *>(smem + G::kCtrlBase);
     const Op op;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // a capturing policy's back-off: nonzero when this call skips the capture
+    // (its departure is counted by a look-back warp below, off the start)
+    unsigned skipped_backoff = 0;
     if constexpr (PolicyCapturing<P>::value) {
         if (P::may_capture(args)) {
-            constexpr int NW = G::kThreads / 32;
-            constexpr unsigned CAP = static_cast<unsigned>(G::kSmemBytes / 4 / NW);   // values per warp region
-            if (P::template capture<NW, CAP>(args, reinterpret_cast<uint32_t *>(smem), st, spin_limit)) return;
-            __syncthreads();   // every warp has left its region before the set-up below reuses the memory
+            const unsigned backoff = capture_backoff(st);
+            if (backoff == 0u) {
+                constexpr int NW = G::kThreads / 32;
+                constexpr unsigned CAP = static_cast<unsigned>(G::kSmemBytes / 4 / NW);   // values per warp region
+                if (P::template capture<NW, CAP>(args, reinterpret_cast<uint32_t *>(smem), st, spin_limit)) return;
+                __syncthreads();   // every warp has left its region before the set-up below reuses the memory
+            } else {
+                skipped_backoff = backoff;
+            }
         }
     }
 
@@ -505,6 +514,8 @@ pipeline_l2_kernel(typename P::Args args, unsigned num_tiles, unsigned long long
     if (warp >= G::kFirstLookbackWarp) {
         // ------------------------------------------------ look-back warp r
         const unsigned r = static_cast<unsigned>(warp - G::kFirstLookbackWarp);
+        if constexpr (PolicyCapturing<P>::value)
+            if (skipped_backoff != 0u && r == 0 && lane == 0) capture_skip_depart(st, skipped_backoff, gridDim.x);
         for (unsigned k = 0;; ++k) {
             if (!mbar_wait(&ctrl->rec_pending[r], k & 1u, wait_limit)) {
                 if (lane == 0) atomicOr(&st->error, kErrTimeout);
