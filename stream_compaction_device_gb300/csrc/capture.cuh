@@ -85,8 +85,6 @@ __device__ __forceinline__ bool capture_gt(const uint32_t *__restrict__ in, int3
     const size_t we = wb + wpart < end ? wb + wpart : (wb < end ? end : wb);   // [wb, we), maybe empty
     uint32_t *region = s_kept + static_cast<size_t>(warp) * CAP;
     const volatile unsigned *abort_flag = &st->capture_abort;
-    // a capture on this stream gave up lately: leave it to the pipeline
-    // (every block reads the count before any block can leave)
     uint32_t kept = 0;
     bool give_up = false;
     unsigned round = 0;
