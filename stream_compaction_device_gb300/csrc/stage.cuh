@@ -93,36 +93,26 @@ __device__ __forceinline__ void write_run_scalar(uint32_t *__restrict__ out, siz
 // Copy a run staged in phase with its destination: element i of the run sits
 // at stage[(g0 & 3) + i] (stage 16-byte aligned) and goes to out[g0 + i], out
 // 16-byte aligned.  Shared chunk k then maps to output chunk g0 / 4 + k, so
-// every whole chunk is one 128-bit load and one 128-bit store; only the two
-// ragged end chunks are stored element by element.  Elements at or past
-// `limit` are never written.
+// every whole chunk is one 128-bit load and one 128-bit store.  The words of
+// the two ragged end chunks (at most three each) take a thread each, threads
+// 0-3 the head and 4-7 the tail, after the loop: no thread branches off
+// inside it.  Elements at or past `limit` are never written.
 template <int THREADS>
 __device__ __forceinline__ void write_run_direct(uint32_t *__restrict__ out, size_t g0, unsigned cnt,
                                                  const uint32_t *stage, int tid, size_t limit)
 {
+    static_assert(THREADS >= 8, "threads 0-7 store the ragged ends");
     if (cnt == 0 || g0 >= limit) return;   // (a start past the end only follows a timed-out wait)
     const unsigned a = static_cast<unsigned>(g0 & 3);
     const size_t room = limit - (g0 - a);   // words of out from the first chunk's start
     const unsigned end = a + cnt;
     const unsigned stop = room < end ? static_cast<unsigned>(room) : end;   // words [a, stop) are written
-    const unsigned chunks = (stop + 3) >> 2;
+    const unsigned kb = (a + 3) >> 2, ke = stop >> 2;                      // the whole chunks: [kb, ke)
     uint4 *dst = reinterpret_cast<uint4 *>(out) + (g0 >> 2);
     const uint4 *src = reinterpret_cast<const uint4 *>(stage);
-    for (unsigned k = tid; k < chunks; k += THREADS) {
-        const uint4 v = src[k];
-        const unsigned w0 = 4 * k;
-        if (w0 >= a && w0 + 4 <= stop) {
-            st_stream(dst + k, v);
-        } else {
-            uint32_t *o = reinterpret_cast<uint32_t *>(dst + k);
-            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const unsigned w = w0 + j;
-                if (w >= a && w < stop) o[j] = vv[j];
-            }
-        }
-    }
+    for (unsigned k = kb + tid; k < ke; k += THREADS) st_stream(dst + k, src[k]);
+    const unsigned w = tid < 4 ? a + tid : max(4 * ke, 4 * kb) + (tid - 4);
+    if (tid < 8 && w < stop && (tid >= 4 || w < 4 * kb)) reinterpret_cast<uint32_t *>(dst)[w] = stage[w];
 }
 
 // write_run_direct that also counts the run's keys whose bit `nb` is 0, by
@@ -135,39 +125,34 @@ __device__ __forceinline__ void write_run_direct_count(uint32_t *__restrict__ ou
                                                        const uint32_t *stage, int tid, size_t limit, int nb,
                                                        uint32_t &c0, uint32_t &c1)
 {
+    static_assert(THREADS >= 8, "threads 0-7 store the ragged ends");
     if (cnt == 0 || g0 >= limit) return;
     const unsigned a = static_cast<unsigned>(g0 & 3);
     const size_t room = limit - (g0 - a);
     const unsigned end = a + cnt;
     const unsigned stop = room < end ? static_cast<unsigned>(room) : end;
-    const unsigned chunks = (stop + 3) >> 2;
+    const unsigned kb = (a + 3) >> 2, ke = stop >> 2;
     // staged word w lands at g0 - a + w: the next part starts at word `next`
     const unsigned next = 512u - static_cast<unsigned>((g0 - a) & 511u);
     uint4 *dst = reinterpret_cast<uint4 *>(out) + (g0 >> 2);
     const uint4 *src = reinterpret_cast<const uint4 *>(stage);
     const uint32_t sel = byte_sel(nb);
     const int nbb = nb & 7;
-    for (unsigned k = tid; k < chunks; k += THREADS) {
+    for (unsigned k = kb + tid; k < ke; k += THREADS) {
         const uint4 v = src[k];
-        const unsigned w0 = 4 * k;
-        uint32_t z;
-        if (w0 >= a && w0 + 4 <= stop) {
-            st_stream(dst + k, v);
-            z = 4u - ones_at_bit(v, sel, nbb);
-        } else {
-            uint32_t *o = reinterpret_cast<uint32_t *>(dst + k);
-            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-            z = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const unsigned w = w0 + j;
-                if (w >= a && w < stop) {
-                    o[j] = vv[j];
-                    z += ((vv[j] >> nb) & 1u) ^ 1u;
-                }
-            }
-        }
-        if (w0 < next)
+        st_stream(dst + k, v);
+        const uint32_t z = 4u - ones_at_bit(v, sel, nbb);
+        if (4 * k < next)
+            c0 += z;
+        else
+            c1 += z;
+    }
+    const unsigned w = tid < 4 ? a + tid : max(4 * ke, 4 * kb) + (tid - 4);
+    if (tid < 8 && w < stop && (tid >= 4 || w < 4 * kb)) {
+        const uint32_t key = stage[w];
+        reinterpret_cast<uint32_t *>(dst)[w] = key;
+        const uint32_t z = ((key >> nb) & 1u) ^ 1u;
+        if (w < next)
             c0 += z;
         else
             c1 += z;
