@@ -193,8 +193,9 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
 // the count pass plus the pipelined split (12 per key), without a chain
 // between tiles.
 // ---------------------------------------------------------------------------
-constexpr int kSplitPart = 512, kSplitCountThreads = 512, kSplitStageParts = 32, kSplitStages = 3,
+constexpr int kSplitPart = 1024, kSplitCountThreads = 512, kSplitStageParts = 16, kSplitStages = 3,
               kSplitWriteWarps = 8;
+constexpr int kSplitRows = kSplitPart / 128;   // 16-byte loads per lane and part
 constexpr unsigned kSplitCountWaitLimit = 1u << 18;
 constexpr unsigned kSplitMaxCountBlocks = 512;   // chunk totals and carries share the workspace's tile sums
 constexpr int kSortOffsetThreads = 1024;
@@ -221,14 +222,14 @@ split_count_kernel(const uint32_t *__restrict__ keys, size_t n, int bit, unsigne
     const unsigned p0 = blockIdx.x * chunk, p1 = p0 + chunk < parts ? p0 + chunk : parts;
     const unsigned whole = static_cast<unsigned>(n / kSplitPart);
     const unsigned q1 = p1 < whole ? p1 : (p0 > whole ? p0 : whole);   // [p0, q1): whole parts
-    // phase 1: a part per warp; lane L reads the part's 16-byte groups L, L + 32, L + 64, L + 96
+    // phase 1: a part per warp; lane L reads the part's 16-byte groups L, L + 32, L + 64, ...
     const bool streamed = stream_parts<kSplitPart * 4, SP, NSTG>(
         reinterpret_cast<const uint8_t *>(keys), p0, q1, s_ring, s_full, kSplitCountWaitLimit,
         [&](unsigned p, const uint8_t *part) {
             const uint4 *k4 = reinterpret_cast<const uint4 *>(part);
             uint32_t z = 0;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) z += zeros_of(k4[g * 32 + lane], bit);
+            for (int g = 0; g < kSplitRows; ++g) z += zeros_of(k4[g * 32 + lane], bit);
             z = __reduce_add_sync(kFullMask, z);
             if (lane == 0) off[p] = z;
         });
@@ -258,12 +259,11 @@ split_count_kernel(const uint32_t *__restrict__ keys, size_t n, int bit, unsigne
 }
 
 // Warp w of block b splits part b * kSplitWriteWarps + w.  COUNT_NEXT: it
-// also adds, per 512-position part of `out`, the keys it writes there whose
-// bit next_bit is 0 to next_cnt (the next pass's part counts, in a sort).
-// Five blocks per SM (48 registers): the counting form otherwise takes 54
-// registers and four blocks, and measured 5% slower over a sort.
+// also adds, per part of `out`, the keys it writes there whose bit next_bit
+// is 0 to next_cnt (the next pass's part counts, in a sort).  Four blocks per
+// SM (64 registers).
 template <bool OUT_ALIGNED, bool COUNT_NEXT>
-__global__ void __launch_bounds__(kSplitWriteWarps * 32, 5)
+__global__ void __launch_bounds__(kSplitWriteWarps * 32, 4)
 split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out, size_t n, int bit, unsigned parts,
                    ChunkDiv chunk, const uint32_t *off, const uint32_t *carry, const unsigned *zeros,
                    int next_bit, uint32_t *__restrict__ next_cnt)
@@ -278,12 +278,12 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
     if (p >= parts) return;   // the whole warp: no barrier follows
     const size_t b = static_cast<size_t>(p) * kSplitPart;
     const unsigned part_len = n - b < static_cast<size_t>(kSplitPart) ? static_cast<unsigned>(n - b) : kSplitPart;
-    uint32_t x[4][4], zmask[4];
+    uint32_t x[kSplitRows][4], zmask[kSplitRows];
     if (part_len == static_cast<unsigned>(kSplitPart)) {
         const uint4 *k4 = reinterpret_cast<const uint4 *>(keys + b);
         const uint32_t sel = byte_sel(bit);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kSplitRows; ++q) {
             const uint4 u = __ldcs(k4 + q * 32 + lane);
             x[q][0] = u.x;
             x[q][1] = u.y;
@@ -293,7 +293,7 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
         }
     } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kSplitRows; ++q) {
             uint32_t m = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -307,7 +307,7 @@ split_write_kernel(const uint32_t *__restrict__ keys, uint32_t *__restrict__ out
     wait_primary_grid();   // the count launch's offsets, carries and Z (the keys need no wait)
     const size_t zeros_at = static_cast<size_t>(off[p]) + carry[chunk.of(p)];
     const size_t ones_at = static_cast<size_t>(*zeros) + (b - zeros_at);
-    split_write_warp<4, COUNT_NEXT>(x, zmask, part_len, zeros_at, ones_at, lane, s_stage[warp], out, OUT_ALIGNED, n,
+    split_write_warp<kSplitRows, COUNT_NEXT>(x, zmask, part_len, zeros_at, ones_at, lane, s_stage[warp], out, OUT_ALIGNED, n,
                                     next_bit, next_cnt);
 }
 

@@ -28,13 +28,14 @@ __device__ __forceinline__ unsigned zeros_of(uint4 q, int bit)
 // ---------------------------------------------------------------------------
 
 // One consume warp's part of a split (bit j of zmask[q] marks key x[q][j] as
-// a zero; part_len keys are real): ranks the zeros with one scan of the four
-// rows' counts packed into the bytes of a word, stages the zeros from word
-// zeros_at % 4 and the ones from the next 16-byte boundary after them (plus
-// ones_at % 4) in its private `stage` area (kWarpItems + 12 words), and
-// writes both runs out in whole 128-bit chunks where they line up.
+// a zero; part_len keys are real; 128 * VECS keys in a whole part): ranks the
+// zeros with one scan of the rows' counts packed four to a word (a byte per
+// row: a row holds at most 128 keys), stages the zeros from word zeros_at % 4
+// and the ones from the next 16-byte boundary after them (plus ones_at % 4)
+// in its private `stage` area (128 * VECS + 12 words), and writes both runs
+// out in whole 128-bit chunks where they line up.
 // COUNT_NEXT: the writes also count the keys whose bit next_bit is 0 by the
-// 512-position output part they land in, and add those counts to
+// (128 * VECS)-position output part they land in, and add those counts to
 // next_cnt[part] (at most four atomics per part).
 template <int VECS, bool COUNT_NEXT = false>
 __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], const uint32_t (&zmask)[VECS],
@@ -42,18 +43,33 @@ __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], c
                                                  uint32_t *stage, uint32_t *out, bool out_aligned, size_t n,
                                                  int next_bit = 0, uint32_t *next_cnt = nullptr)
 {
-    static_assert(VECS == 4, "the four rows' counts share one word");
-    uint32_t packed = 0;
+    static_assert(VECS == 4 || VECS == 8, "whole words of four row counts");
+    constexpr int WORDS = VECS / 4;
+    constexpr int PART = 128 * VECS;
+    constexpr int kPartShift = VECS == 4 ? 9 : 10;
+    uint32_t packed[WORDS], inc[WORDS], excl[WORDS], tot[WORDS];
 #pragma unroll
-    for (int q = 0; q < VECS; ++q) packed |= static_cast<uint32_t>(__popc(zmask[q])) << (8 * q);
-    uint32_t inc = packed;
+    for (int w = 0; w < WORDS; ++w) {
+        packed[w] = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) packed[w] |= static_cast<uint32_t>(__popc(zmask[4 * w + q])) << (8 * q);
+        inc[w] = packed[w];
+    }
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t u = __shfl_up_sync(kFullMask, inc, d);
-        if (lane >= d) inc += u;
+#pragma unroll
+        for (int w = 0; w < WORDS; ++w) {
+            const uint32_t u = __shfl_up_sync(kFullMask, inc[w], d);
+            if (lane >= d) inc[w] += u;
+        }
     }
-    const uint32_t excl = inc - packed, tot = __shfl_sync(kFullMask, inc, 31);
-    const uint32_t zeros = (tot & 0xffu) + ((tot >> 8) & 0xffu) + ((tot >> 16) & 0xffu) + (tot >> 24);
+    uint32_t zeros = 0;
+#pragma unroll
+    for (int w = 0; w < WORDS; ++w) {
+        excl[w] = inc[w] - packed[w];
+        tot[w] = __shfl_sync(kFullMask, inc[w], 31);
+        zeros += (tot[w] & 0xffu) + ((tot[w] >> 8) & 0xffu) + ((tot[w] >> 16) & 0xffu) + (tot[w] >> 24);
+    }
     const unsigned z_phase = out_aligned ? static_cast<unsigned>(zeros_at & 3) : 0u;
     const unsigned o_phase = out_aligned ? static_cast<unsigned>(ones_at & 3) : 0u;
     const unsigned o_base = out_aligned ? ((z_phase + zeros + 3u) & ~3u) : zeros;
@@ -66,7 +82,7 @@ __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], c
         uint32_t row_base = 0;
 #pragma unroll
         for (int q = 0; q < VECS; ++q) {
-            uint32_t zr = row_base + ((excl >> (8 * q)) & 0xffu);
+            uint32_t zr = row_base + ((excl[q / 4] >> (8 * (q % 4))) & 0xffu);
             const uint32_t li0 = static_cast<uint32_t>((q * 32 + lane) * 4);   // index inside the part
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -76,10 +92,10 @@ __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], c
                 if (WHOLE || li < part_len) stage[pos] = x[q][j];
                 zr += z;
             }
-            row_base += (tot >> (8 * q)) & 0xffu;
+            row_base += (tot[q / 4] >> (8 * (q % 4))) & 0xffu;
         }
     };
-    if (part_len == static_cast<unsigned>(32 * 4 * VECS))
+    if (part_len == static_cast<unsigned>(PART))
         stage_keys(std::true_type{});
     else
         stage_keys(std::false_type{});
@@ -88,17 +104,18 @@ __device__ __forceinline__ void split_write_warp(const uint32_t (&x)[VECS][4], c
         // also count bit next_bit's zeros by the output part they land in
         uint32_t c[4] = {0u, 0u, 0u, 0u};
         if (out_aligned) {
-            write_run_direct_count<32>(out, zeros_at, zeros, stage, lane, n, next_bit, c[0], c[1]);
-            write_run_direct_count<32>(out, ones_at, part_len - zeros, stage + o_base, lane, n, next_bit, c[2], c[3]);
+            write_run_direct_count<32, PART>(out, zeros_at, zeros, stage, lane, n, next_bit, c[0], c[1]);
+            write_run_direct_count<32, PART>(out, ones_at, part_len - zeros, stage + o_base, lane, n, next_bit, c[2],
+                                             c[3]);
         } else {
-            write_run_scalar_count<32>(out, zeros_at, zeros, stage, 0, lane, n, next_bit, c[0], c[1]);
-            write_run_scalar_count<32>(out, ones_at, part_len - zeros, stage, static_cast<int>(zeros), lane, n,
-                                       next_bit, c[2], c[3]);
+            write_run_scalar_count<32, PART>(out, zeros_at, zeros, stage, 0, lane, n, next_bit, c[0], c[1]);
+            write_run_scalar_count<32, PART>(out, ones_at, part_len - zeros, stage, static_cast<int>(zeros), lane, n,
+                                             next_bit, c[2], c[3]);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[i] = __reduce_add_sync(kFullMask, c[i]);
         if (lane == 0) {
-            const size_t zp = zeros_at >> 9, op = ones_at >> 9;
+            const size_t zp = zeros_at >> kPartShift, op = ones_at >> kPartShift;
             if (c[0] != 0) atomicAdd(next_cnt + zp, c[0]);
             if (c[1] != 0) atomicAdd(next_cnt + zp + 1, c[1]);
             if (c[2] != 0) atomicAdd(next_cnt + op, c[2]);

@@ -116,11 +116,11 @@ __device__ __forceinline__ void write_run_direct(uint32_t *__restrict__ out, siz
 }
 
 // write_run_direct that also counts the run's keys whose bit `nb` is 0, by
-// the 512-position output part they land in: c0 for the part of out[g0],
-// c1 for the next one (a run of at most 512 keys spans two parts at most).
+// the PART-position output part they land in: c0 for the part of out[g0],
+// c1 for the next one (a run of at most PART keys spans two parts at most).
 // A 16-byte chunk of out never straddles two parts, so each chunk adds its
 // count to one of the two.
-template <int THREADS>
+template <int THREADS, int PART>
 __device__ __forceinline__ void write_run_direct_count(uint32_t *__restrict__ out, size_t g0, unsigned cnt,
                                                        const uint32_t *stage, int tid, size_t limit, int nb,
                                                        uint32_t &c0, uint32_t &c1)
@@ -133,7 +133,8 @@ __device__ __forceinline__ void write_run_direct_count(uint32_t *__restrict__ ou
     const unsigned stop = room < end ? static_cast<unsigned>(room) : end;
     const unsigned kb = (a + 3) >> 2, ke = stop >> 2;
     // staged word w lands at g0 - a + w: the next part starts at word `next`
-    const unsigned next = 512u - static_cast<unsigned>((g0 - a) & 511u);
+    static_assert(PART % 4 == 0 && (PART & (PART - 1)) == 0, "parts of whole chunks, a power of two");
+    const unsigned next = PART - static_cast<unsigned>((g0 - a) & (PART - 1));
     uint4 *dst = reinterpret_cast<uint4 *>(out) + (g0 >> 2);
     const uint4 *src = reinterpret_cast<const uint4 *>(stage);
     const uint32_t sel = byte_sel(nb);
@@ -160,18 +161,18 @@ __device__ __forceinline__ void write_run_direct_count(uint32_t *__restrict__ ou
 }
 
 // write_run_scalar with the same count as write_run_direct_count.
-template <int THREADS>
+template <int THREADS, int PART>
 __device__ __forceinline__ void write_run_scalar_count(uint32_t *__restrict__ out, size_t g0, unsigned cnt,
                                                        const uint32_t *stage, int s0, int tid, size_t limit, int nb,
                                                        uint32_t &c0, uint32_t &c1)
 {
-    const size_t first_part = g0 >> 9;
+    const size_t first_part = g0 / PART;
     for (unsigned e = tid; e < cnt; e += THREADS) {
         if (g0 + e >= limit) continue;
         const uint32_t k = stage[s0 + static_cast<int>(e)];
         out[g0 + e] = k;
         const uint32_t z = ((k >> nb) & 1u) ^ 1u;
-        if (((g0 + e) >> 9) == first_part)
+        if ((g0 + e) / PART == first_part)
             c0 += z;
         else
             c1 += z;
