@@ -269,9 +269,9 @@ devscan_status bracket_scan_i32(const int32_t *in, int32_t *out, int32_t *result
  *   keys, out : device uint32[n], not overlapping (DEVSCAN_ERR_INVALID);
  *   bit       : 0..31, else DEVSCAN_ERR_INVALID;
  *   n         : at most INT32_MAX, else DEVSCAN_ERR_INVALID.
- * From 2^20 keys (keys 16-byte aligned): a launch counting every 512-key
+ * From 2^20 keys (keys 16-byte aligned): a launch counting every 1,024-key
  * part's zeros into part offsets and Z, then a warp per part writing its two
- * runs; one word per 512 keys of per-stream scratch is allocated
+ * runs; one word per 1,024 keys of per-stream scratch is allocated
  * stream-ordered on first use (DEVSCAN_ERR_NOMEM if that fails).  Below, a
  * zero-count pass, then the single-pass split.
  * ------------------------------------------------------------------------- */
@@ -283,8 +283,8 @@ devscan_status split_bit_u32(const uint32_t *keys, uint32_t *out, int bit, size_
  * counts the zeros of bit b+1 while it scatters, and one count pass runs
  * before pass 0.  From 2^20 keys (keys and tmp 16-byte aligned) each pass
  * is the two-launch split, whose write launch counts bit b+1's zeros per
- * 512-key part of its output, plus a small launch turning those counts into
- * the next pass's offsets; 2 words per 512 keys of per-stream scratch are
+ * 1,024-key part of its output, plus a small launch turning those counts into
+ * the next pass's offsets; 2 words per 1,024 keys of per-stream scratch are
  * allocated stream-ordered on first use (DEVSCAN_ERR_NOMEM if that fails).
  * Otherwise each pass is the pipelined (or one-tile) split, which needs only
  * the total zero count of bit b+1.

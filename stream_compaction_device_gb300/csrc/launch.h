@@ -82,13 +82,12 @@ cudaError_t launch_compact(const int32_t *in, const uint8_t *flags, int32_t *out
 cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned *zeros, const Workspace &ws,
                                cudaStream_t s);
 
-// A standalone split in two launches: zeros counted per 512-key part (their
+// A standalone split in two launches: zeros counted per 1,024-key part (their
 // offsets and the total into *zeros), then a warp per part writes its runs;
 // part_words: split_part_words(n) words of per-stream scratch.  Taken for
 // 16-byte-aligned keys from kSplitTwoPassMinN keys and in carry mode 4;
 // measured on GB300 it beats the count pass plus the pipelined split at every
-// size from 2^20 (139 against 170 us at 2^26).  A sort's passes keep the
-// pipeline, which counts the next bit's zeros as it goes.
+// size from 2^20 (131 against 170 us at 2^26).
 constexpr size_t kSplitTwoPassMinN = size_t(1) << 20;
 size_t split_part_words(size_t n);
 cudaError_t launch_split_two_pass(const uint32_t *keys, uint32_t *out, size_t n, int bit, unsigned *zeros,
@@ -96,9 +95,9 @@ cudaError_t launch_split_two_pass(const uint32_t *keys, uint32_t *out, size_t n,
 
 // The 32-pass LSD sort from the two-launch split: one zero count of bit 0,
 // then per bit a write launch that also counts the next bit's zeros per
-// 512-key part of its output (at most four global atomics per part) and a
+// 1,024-key part of its output (at most four global atomics per part) and a
 // small launch turning those counts into the next pass's offsets.  Measured
-// on GB300 at 2^26 keys: 3.65 ms against 4.15 ms for the pipelined splits.  keys and
+// on GB300 at 2^26 keys: 2.85 ms against 4.15 ms for the pipelined splits.  keys and
 // tmp 16-byte aligned; the sorted keys end in `keys`; part_words:
 // sort_part_words(n) words of per-stream scratch; *zeros: a device word.
 // Taken from kSortTwoPassMinN keys (default or carry mode 4).

@@ -183,7 +183,7 @@ cudaError_t launch_count_zeros(const uint32_t *keys, size_t n, int bit, unsigned
 
 // ---------------------------------------------------------------------------
 // Two-launch split (a standalone split, which must count the zeros first
-// anyway): a block per SM streams its chunk of 512-key parts through shared
+// anyway): a block per SM streams its chunk of 1,024-key parts through shared
 // memory, counts every part's zeros and turns the counts into offsets within
 // the chunk; the last block to finish scans the chunk totals into chunk
 // carries and the total Z.  The write launch, a programmatic dependent of the
