@@ -27,11 +27,12 @@
 
 namespace devscan {
 
-constexpr int kSortThreads = 512;
+constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kSortRows = 16;                          // rows of 32 keys per warp
+constexpr int kSortRows = 32;                          // rows of 32 keys per warp
 constexpr int kSortTile = kSortThreads * kSortRows;    // 8,192 keys
 constexpr int kSortBuckets = 1 << kRadixDigitBits;     // 256
+static_assert(kSortThreads >= kSortBuckets, "a thread per digit in the per-tile digit scan");
 
 __device__ __forceinline__ unsigned digit_of(uint32_t key, int shift) { return (key >> shift) & (kSortBuckets - 1); }
 
@@ -150,23 +151,24 @@ __device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *s_tmp, i
 }
 
 // Rows ranked with the hardware match instead of ballots: every fourth.
-constexpr unsigned kMatchRows = 0x1111u;
+constexpr unsigned kMatchRows = 0x11111111u;
 
 // keys_in -> keys_out by the digit at `shift`; run_start[d * tiles + tile]:
 // the first output position of the tile's keys of digit d.  Block b sorts
 // tile tile0 + b; FULL: every tile of the launch holds kSortTile keys (the
 // ragged last tile gets a launch of its own), which drops the bounds checks.
-// Three blocks per SM cap the kernel at 40 registers, and the keys and ranks
-// of a warp's 16 rows then spill about 130 bytes per thread to local memory;
-// measured at 2^26 keys the sort is still 2% faster than with two blocks and
-// 64 registers (the extra warps hide the ranking's shared-memory latency).
+// Eight warps of 32 rows each: the per-tile work on the warps' digit
+// counters (clearing, the digit scan over the warps, the staging offsets)
+// is half that of sixteen warps of 16 rows, and measured at 2^26 keys the
+// sort takes 1.12 against 1.20 ms.  Three blocks per SM (80 registers, about
+// 30 bytes of spills per thread) beat two blocks without spills (1.21 ms).
 template <bool FULL>
 __global__ void __launch_bounds__(kSortThreads, 3)
 radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict__ keys_out, size_t n, int shift,
                      unsigned tiles, unsigned tile0, const uint32_t *__restrict__ run_start)
 {
     // per-warp digit counters; then each (warp, digit)'s first staged position
-    __shared__ uint32_t s_wcount[kSortWarps][kSortBuckets];   // 16 KB
+    __shared__ uint32_t s_wcount[kSortWarps][kSortBuckets];   // 8 KB
     __shared__ uint32_t s_keys[kSortTile];                     // 32 KB: the tile sorted by digit
     __shared__ uint32_t s_delta[kSortBuckets];                 // output position - staged position, per digit
     __shared__ uint32_t s_tmp[8];
@@ -178,8 +180,10 @@ radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict_
 
     for (int i = tid; i < kSortWarps * kSortBuckets; i += kSortThreads) (&s_wcount[0][0])[i] = 0;
     if (tid < kSortBuckets) s_delta[tid] = run_start[static_cast<size_t>(tid) * tiles + tile];   // the run's start
-    // keys of this warp's 512 that exist (the last tile is ragged)
-    const unsigned wlen = FULL ? 512u : (n > wbase ? static_cast<unsigned>(n - wbase < 512 ? n - wbase : 512) : 0u);
+    // keys of this warp's kWarpKeys that exist (the last tile is ragged)
+    constexpr unsigned kWarpKeys = kSortRows * 32;
+    const unsigned wlen = FULL ? kWarpKeys
+                               : (n > wbase ? static_cast<unsigned>(n - wbase < kWarpKeys ? n - wbase : kWarpKeys) : 0u);
     uint32_t key[kSortRows];
 #pragma unroll
     for (int r = 0; r < kSortRows; ++r) {
@@ -189,7 +193,7 @@ radix_scatter_kernel(const uint32_t *__restrict__ keys_in, uint32_t *__restrict_
     __syncthreads();
 
     // rank within the warp: row by row (input order), equal digits grouped;
-    // two rows' ranks (below 512) share a register's 16-bit halves
+    // two rows' ranks (below kWarpKeys) share a register's 16-bit halves
     uint32_t rank2[kSortRows / 2];
 #pragma unroll
     for (int r = 0; r < kSortRows / 2; ++r) rank2[r] = 0;
