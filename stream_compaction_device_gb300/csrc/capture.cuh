@@ -111,7 +111,7 @@ __device__ __forceinline__ bool capture_gt(const uint32_t *__restrict__ in, int3
     // gave up, or another warp did)
     auto take_round = [&](size_t s, const uint4 (&q)[8]) -> bool {
         const bool full = s + kCaptureRound <= we;
-        // another warp's verdict, every fourth round
+        // whether another warp gave up, read every fourth round
         const unsigned stop = (round & 3u) == 3u ? __shfl_sync(kFullMask, *abort_flag, 0) : 0u;
         uint32_t nib[8];
 #pragma unroll
@@ -181,7 +181,7 @@ __device__ __forceinline__ bool capture_gt(const uint32_t *__restrict__ in, int3
     // grid barrier; a block stops waiting once any warp has given up
     __syncthreads();
     if (tid == 0) {
-        __threadfence();   // the block's total (and its warps' verdicts) before its arrival
+        __threadfence();   // the block's total (and its warps' give-up flags) before its arrival
         atomicAdd(&st->grid_arrive, 1u);
         int abort = 0;
         unsigned spins = 0;
