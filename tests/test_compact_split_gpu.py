@@ -212,7 +212,9 @@ def gpu_sort_digits(ds, k: np.ndarray, koff=0):
 
 def test_sort_digits_sizes(ds):
     rng = np.random.default_rng(9)
-    for n in (1, 2, 3, 15, 16, 17, 100, 4095, 4096, 4097, 65_537, 1_000_003):
+    # around a warp's 1,024 keys and the 8,192-key tile of the scatter
+    for n in (1, 2, 3, 15, 16, 17, 100, 1023, 1024, 1025, 4095, 4096, 4097, 8191, 8192, 8193, 8192 + 1025,
+              2 * 8192 + 7000, 65_537, 1_000_003):
         k = rng.integers(0, 2**32, n, dtype=np.uint32)
         k[: min(n, 6)] = np.array([0, 2**32 - 1, 7, 7, 2**31, 2**31 - 1], dtype=np.uint32)[: min(n, 6)]
         assert np.array_equal(gpu_sort_digits(ds, k), oracle.sort_lsd(k)), f"n={n}"
@@ -282,7 +284,7 @@ def test_default_two_launch_boundaries(ds):
     keys) and to the two-launch compaction (2^23 elements), aligned and not."""
     ds.set_carry_mode("default")
     rng = np.random.default_rng(8)
-    for n in ((1 << 20) - 1, 1 << 20, (1 << 20) + 3):
+    for n in ((1 << 20) - 1, 1 << 20, (1 << 20) + 3, (1 << 20) + 1023, (1 << 20) + 1025):   # 1,024-key parts
         k = rng.integers(0, 2**32, n, dtype=np.uint32)
         assert np.array_equal(gpu_split(ds, k, 23), oracle.split_bit(k, 23)[0]), n
         assert np.array_equal(gpu_split(ds, k, 0, koff=1, ooff=2), oracle.split_bit(k, 0)[0]), n
