@@ -12,8 +12,9 @@
 //      keys it is 2M counts, which the L2-resident scan takes) turns it into
 //      every (digit, tile) run's first output position: all keys of smaller
 //      digits, plus the keys of digit d in earlier tiles;
-//   3. radix_scatter_kernel: every tile ranks its keys stably by digit -- rows
-//      of 32 consecutive keys in input order, the lanes with equal digits
+//   3. radix_scatter_kernel: every tile ranks its keys stably by digit --
+//      eight warps of 32 rows, each row 32 consecutive keys in input order,
+//      the lanes with equal digits
 //      grouped by eight ballots (three rows in four) or the hardware match
 //      (every fourth row), one counter row per warp in shared memory --
 //      stages the tile sorted by digit and writes each digit's keys as one
